@@ -1,0 +1,429 @@
+"""Pins for the CPU oracle: closed forms, invariants, library special cases and
+brute force on tiny inputs. None of these compares the oracle with itself.
+
+Each check lives in a `check_*` helper that takes the oracle module, so the
+planted-mistake tests at the bottom can run the same checks against a copy of
+the oracle with one deliberate error and confirm that some check fails.
+"""
+import json
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.h3_oracle as O
+from dit_transformer_block_gb300 import inputs as I
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def bf16_values(a):
+    """Round arbitrary float64 data to bf16 with torch (a library cast), for inputs."""
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).double().numpy()
+
+
+# ------------------------------------------------------------------ rounding
+def check_round_bf16(o):
+    g = GOLD["bf16_ties"]
+    assert np.array_equal(o.round_bf16(np.array(g["x"])), np.array(g["y"]))
+    # library pin: torch's float32 -> bfloat16 cast (round to nearest even)
+    x = rng(1).standard_normal(20000).astype(np.float32) * np.float32(3.0)
+    x = np.concatenate([x, np.float32([0.0, -0.0, 1e-39, -3e-40, 3.3e38, 1.0e-30])])
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(o.round_bf16(x.astype(np.float64)), ref)
+    # every bf16-valued input maps to itself
+    assert np.array_equal(o.round_bf16(ref), ref)
+
+
+def test_round_bf16():
+    check_round_bf16(O)
+
+
+# ---------------------------------------------------------- a1 modulation
+def check_layer_norm(o):
+    g = GOLD["layer_norm_1234"]
+    y = o.layer_norm(np.array([g["x"]]), g["eps"])[0]
+    assert np.allclose(y * math.sqrt(5.0), g["y_times_sqrt5"], rtol=0, atol=1e-14)
+    x = rng(2).standard_normal((7, 96)) * 3 + 1.5
+    y = o.layer_norm(x, 0.0)
+    assert np.allclose(y.mean(-1), 0, atol=1e-13)
+    assert np.allclose(y.var(-1), 1, atol=1e-12)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (96,), eps=1e-6).numpy()
+    assert np.allclose(o.layer_norm(x, 1e-6), ref, rtol=1e-12, atol=1e-12)
+
+
+def check_mod_norm_residual(o):
+    r = rng(3).standard_normal((5, 64)).astype(np.float32).astype(np.float64)
+    delta = bf16_values(rng(4).standard_normal((5, 64)))
+    zeros = np.zeros(64)
+    # gate = 0: the residual comes back bit for bit
+    r2, _ = o.mod_norm_residual(r, delta, zeros)
+    assert np.array_equal(r2, r)
+    # the residual add is r + gate * delta (float32 store); small exact values
+    gate = np.full(64, 0.5)
+    d = np.full((5, 64), 2.0)
+    r3, _ = o.mod_norm_residual(r, d, gate)
+    assert np.array_equal(r3, (r + 1.0).astype(np.float32).astype(np.float64))
+    # scale = shift = 0: plain LayerNorm, rounded to bf16
+    _, h = o.mod_norm_residual(r, shift=zeros, scale=zeros, eps=1e-6)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(r), (64,), eps=1e-6)
+    assert np.all(np.abs(h - ref.numpy()) <= 2.0 ** -8 * np.abs(ref.numpy()))
+    # scale = -1: the normalised term vanishes and h is exactly shift
+    g = GOLD["modulate_scale_minus_one"]
+    shift = np.tile(np.array(g["shift"]), 16)
+    _, h = o.mod_norm_residual(r, shift=shift, scale=-np.ones(64))
+    assert np.array_equal(h, np.broadcast_to(shift, h.shape))
+    # scale doubles the normalised term: (1 + 1) * LN
+    _, h1 = o.mod_norm_residual(r, shift=zeros, scale=np.ones(64))
+    assert np.allclose(h1, 2 * o.layer_norm(r, 1e-6), rtol=2 ** -8, atol=0)
+
+
+def test_layer_norm():
+    check_layer_norm(O)
+
+
+def test_mod_norm_residual():
+    check_mod_norm_residual(O)
+
+
+# ------------------------------------------------------ a2 RMSNorm + RoPE
+def check_rms_norm(o):
+    g = GOLD["rms_norm_3_4"]
+    y = o.rms_norm(np.array([g["x"]]), np.array(g["gain"]), 0.0)[0]
+    assert np.allclose(y * 5 / math.sqrt(2), g["y_times_5_over_sqrt2"], atol=1e-14)
+    x = rng(5).standard_normal((6, 3, 128)) * 4
+    ones = np.ones(128)
+    y = o.rms_norm(x, ones, 0.0)
+    assert np.allclose(np.sqrt((y * y).mean(-1)), 1.0, atol=1e-13)
+    assert np.allclose(o.rms_norm(7.5 * x, ones, 0.0), y, atol=1e-13)
+    gain = 1 + 0.1 * rng(6).standard_normal(128)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (128,), torch.from_numpy(gain), eps=1e-6)
+    assert np.allclose(o.rms_norm(x, gain, 1e-6), ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def check_rope(o):
+    g = GOLD["rope_angles_4_2_2"]
+    phi = o.rope_angles(np.array([g["pos"]]), g["axis_dims"], g["theta"])[0]
+    assert np.allclose(phi, g["phi"], rtol=1e-14, atol=0)
+    q = GOLD["rope_quarter_turn"]
+    y = o.rope_apply(np.array(q["x"]).reshape(1, 1, 4), np.array([q["phi"]]))
+    assert np.allclose(y.reshape(-1), q["y"], atol=1e-15)
+    # section-local exponent for the 32/48/48 split: pair 8 of the h section
+    phi = o.rope_angles(np.array([[0, 1, 0]]), (32, 48, 48), 1e4)[0]
+    assert math.isclose(phi[16 + 8], 1e4 ** (-16 / 48), rel_tol=1e-14)
+    assert np.all(phi[:16] == 0) and np.all(phi[40:] == 0)
+    x = rng(7).standard_normal((9, 2, 128))
+    pos = rng(8).integers(0, 80, size=(9, 3))
+    phi = o.rope_angles(pos, (32, 48, 48), 1e4)
+    y = o.rope_apply(x, phi)
+    # norm of every pair is preserved
+    assert np.allclose(np.hypot(y[..., 0::2], y[..., 1::2]),
+                       np.hypot(x[..., 0::2], x[..., 1::2]), atol=1e-13)
+    # turning back by -phi restores the input; position 0 is the identity
+    assert np.allclose(o.rope_apply(y, -phi), x, atol=1e-13)
+    assert np.array_equal(o.rope_apply(x, np.zeros_like(phi)), x)
+    # complex-number form: (x0 + i x1) * exp(i phi)
+    z = (x[..., 0::2] + 1j * x[..., 1::2]) * np.exp(1j * phi)[:, None, :]
+    assert np.allclose(y[..., 0::2], z.real, atol=1e-13)
+    assert np.allclose(y[..., 1::2], z.imag, atol=1e-13)
+    # relative-position property: <R(q,m), R(k,n)> depends on m - n only
+    qv = rng(9).standard_normal((1, 1, 128))
+    kv = rng(10).standard_normal((1, 1, 128))
+    def dot(m, n):
+        pm = o.rope_angles(np.array([[m, 2 * m, 3]]), (32, 48, 48), 1e4)
+        pn = o.rope_angles(np.array([[n, 2 * n, 3]]), (32, 48, 48), 1e4)
+        return float((o.rope_apply(qv, pm) * o.rope_apply(kv, pn)).sum())
+    assert math.isclose(dot(5, 2), dot(40, 37), rel_tol=1e-11, abs_tol=1e-11)
+    assert not math.isclose(dot(5, 2), dot(5, 3), rel_tol=1e-6)
+
+
+def check_qk_norm_rope(o):
+    # norm first, then rope: with all positions 0 the result is the rounded RMSNorm
+    x = bf16_values(rng(11).standard_normal((4, 3, 128)))
+    gain = 1 + 0.1 * rng(12).standard_normal(128)
+    pos0 = np.zeros((4, 3), np.int64)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (128,), torch.from_numpy(gain), eps=1e-6)
+    y0 = o.qk_norm_rope(x, gain, pos0, (32, 48, 48), 1e4, 1e-6)
+    assert np.all(np.abs(y0 - ref.numpy()) <= 2.0 ** -8 * np.abs(ref.numpy()))
+    # the output row has RMS equal to the RMS of the gain-scaled unit vector:
+    # with gain = 1 the rotated row keeps unit RMS (up to bf16 rounding)
+    pos = rng(13).integers(0, 60, size=(4, 3))
+    y = o.qk_norm_rope(x, np.ones(128), pos, (32, 48, 48), 1e4, 0.0)
+    assert np.allclose(np.sqrt((y * y).mean(-1)), 1.0, atol=4e-3)
+
+
+def test_rms_norm():
+    check_rms_norm(O)
+
+
+def test_rope():
+    check_rope(O)
+
+
+def test_qk_norm_rope():
+    check_qk_norm_rope(O)
+
+
+# ---------------------------------------------------------- a3 attention
+def check_attention(o):
+    g = GOLD["attention_two_keys"]
+    q = np.zeros((3, 1, 2)); q[0, 0] = [1, 0]
+    k = np.zeros((3, 1, 2)); k[1, 0] = [1, 0]; k[2, 0] = [50, 0]
+    v = np.zeros((3, 1, 2)); v[0, 0] = [4, 0]; v[1, 0] = [0, 8]; v[2, 0] = [99, 99]
+    out = o.attention(q, k, v, L=2, scale=g["scale"], rows=[0])
+    assert np.allclose(out[0, 0], g["out"], atol=1e-15)
+    r = rng(14)
+    S, L, H, Dh = 40, 33, 2, 16
+    q = bf16_values(r.standard_normal((S, H, Dh)))
+    k = bf16_values(r.standard_normal((S, H, Dh)))
+    v = bf16_values(r.standard_normal((S, H, Dh)))
+    out = o.attention(q, k, v, L, 0.25)
+    # library pin: scaled_dot_product_attention in float64 on the valid rows
+    t = lambda a: torch.from_numpy(a[:L]).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), scale=0.25)
+    assert np.allclose(out, ref.permute(1, 0, 2).numpy(), rtol=2 ** -8, atol=1e-12)
+    # brute force, one element by explicit loops
+    i, h, d = 7, 1, 3
+    logits = [sum(q[i, h, c] * k[j, h, c] for c in range(Dh)) * 0.25 for j in range(L)]
+    m = max(logits)
+    w = [math.exp(x - m) for x in logits]
+    val = sum(w[j] * v[j, h, d] for j in range(L)) / sum(w)
+    assert abs(out[i, h, d] - val) <= 2 ** -8 * abs(val) + 1e-15
+    # rows sum to one: constant V passes through unchanged
+    assert np.array_equal(o.attention(q, k, np.ones_like(v), L, 0.25), np.ones((L, H, Dh)))
+    # identical keys: the output is the mean of V
+    kk = np.broadcast_to(k[:1], k.shape).copy()
+    assert np.allclose(o.attention(q, kk, v, L, 0.25), O.round_bf16(v[:L].mean(0, keepdims=True)).repeat(L, 0),
+                       atol=1e-15)
+    # one dominant logit selects that value row
+    kd = np.zeros_like(k); kd[5] = 1.0
+    qd = np.ones_like(q)
+    assert np.allclose(o.attention(qd, kd, v, L, 100.0), np.broadcast_to(v[5], (L, H, Dh)), atol=1e-15)
+    # pad rows of K, V do not matter; a row subset equals the full result
+    k2, v2 = k.copy(), v.copy(); k2[L:] = 1e3; v2[L:] = -7
+    assert np.array_equal(o.attention(q, k2, v2, L, 0.25), out)
+    assert np.array_equal(o.attention(q, k, v, L, 0.25, rows=[3, 30, 0]), out[[3, 30, 0]])
+
+
+def test_attention():
+    check_attention(O)
+
+
+# ------------------------------------------------------ a4 / a5 GEMM, SwiGLU
+def check_linear(o):
+    r = rng(15)
+    x = r.integers(-8, 9, size=(5, 12)).astype(np.float64)
+    w = r.integers(-8, 9, size=(7, 12)).astype(np.float64)
+    exact = np.array([[sum(x[i, c] * w[j, c] for c in range(12)) for j in range(7)] for i in range(5)])
+    assert np.array_equal(o.linear(x, w), exact)   # |values| < 2^8: bf16-exact
+    x = bf16_values(r.standard_normal((6, 20)))
+    w = bf16_values(r.standard_normal((3, 20)))
+    ref = torch.from_numpy(x) @ torch.from_numpy(w).T
+    assert np.all(np.abs(o.linear(x, w) - ref.numpy()) <= 2.0 ** -8 * np.abs(ref.numpy()))
+
+
+def check_swiglu(o):
+    g = GOLD["silu_points"]
+    assert np.allclose(o.silu(np.array(g["g"])), g["silu"], rtol=1e-15, atol=0)
+    assert math.isclose(o.silu(np.array([40.0]))[0], 40.0, rel_tol=1e-15)
+    assert abs(o.silu(np.array([-40.0]))[0]) < 1e-15
+    r = rng(16)
+    gu = bf16_values(r.standard_normal((5, 24)) * 2)
+    ref = torch.nn.functional.silu(torch.from_numpy(gu[:, :12])) * torch.from_numpy(gu[:, 12:])
+    assert np.allclose(o.swiglu(gu), ref.numpy(), rtol=2 ** -8, atol=1e-30)
+    # halves are [gate | up]: gate 0 zeroes the output whatever the up half holds
+    gu0 = gu.copy(); gu0[:, :12] = 0
+    assert np.array_equal(o.swiglu(gu0), np.zeros((5, 12)))
+
+
+def test_linear():
+    check_linear(O)
+
+
+def test_swiglu():
+    check_swiglu(O)
+
+
+# ------------------------------------------------------------ a6 the block
+def tiny_block(shape=None, seed=0):
+    shape = shape or I.BlockShape(S=24, L=21, D=64, H=2, Dh=32, F=96, axis_dims=(16, 8, 8),
+                                  pos_kind="3d", grid=(2, 3, 4), n_tail=3)
+    inp = I.block_inputs(shape, seed)
+    n = {k: (v.double().numpy() if torch.is_tensor(v) and v.is_floating_point() else v.numpy())
+         for k, v in inp.items()}
+    return shape, n
+
+
+def run_block(o, shape, n, rows=None, inter=False, **over):
+    args = dict(n)
+    args.update(over)
+    return o.block_forward(args["resid"], args["mod"], args["w_qkv"], args["w_o"], args["w_gu"],
+                           args["w_down"], args["q_gain"], args["k_gain"], args["pos"],
+                           L=shape.L, heads=shape.H, head_dim=shape.Dh,
+                           axis_dims=shape.axis_dims, theta=shape.theta, rows=rows,
+                           return_intermediates=inter)
+
+
+def torch_block(shape, n):
+    """The block written with torch float64 library routines (layer_norm,
+    rms_norm, scaled_dot_product_attention, silu) and a complex-number RoPE,
+    with bf16 rounding at the same hand-off points. Returns every hand-off."""
+    T = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    rb = lambda t: t.float().to(torch.bfloat16).double()
+    L, D, H, Dh = shape.L, shape.D, shape.H, shape.Dh
+    r = T(n["resid"])[:L]
+    mod = T(n["mod"])
+    ln = lambda x: torch.nn.functional.layer_norm(x, (D,), eps=1e-6)
+    h1 = rb(ln(r) * (1 + mod[1]) + mod[0])
+    qkv = rb(h1 @ T(n["w_qkv"]).T)
+    q, k, v = (qkv[:, i * D:(i + 1) * D].reshape(L, H, Dh) for i in range(3))
+    pos = T(n["pos"])[:L]
+    ang = []
+    for a, d in enumerate(shape.axis_dims):
+        if d:
+            ang.append(pos[:, a:a + 1] * shape.theta ** (-torch.arange(0, d, 2, dtype=torch.float64) / d))
+    ang = torch.cat(ang, 1)[:, None, :]
+    def rope(x):
+        z = torch.complex(x[..., 0::2], x[..., 1::2]) * torch.polar(torch.ones_like(ang), ang)
+        return torch.stack([z.real, z.imag], -1).reshape(x.shape)
+    q = rb(rope(torch.nn.functional.rms_norm(q, (Dh,), T(n["q_gain"]), eps=1e-6)))
+    k = rb(rope(torch.nn.functional.rms_norm(k, (Dh,), T(n["k_gain"]), eps=1e-6)))
+    a = torch.nn.functional.scaled_dot_product_attention(q.permute(1, 0, 2), k.permute(1, 0, 2),
+                                                         v.permute(1, 0, 2))
+    a = rb(a.permute(1, 0, 2).reshape(L, D))
+    o = rb(a @ T(n["w_o"]).T)
+    r = (r + mod[2] * o).float().double()
+    h2 = rb(ln(r) * (1 + mod[4]) + mod[3])
+    gu = rb(h2 @ T(n["w_gu"]).T)
+    F = gu.shape[1] // 2
+    u = rb(torch.nn.functional.silu(gu[:, :F]) * gu[:, F:])
+    f = rb(u @ T(n["w_down"]).T)
+    r = (r + mod[5] * f).float().double()
+    out = dict(h1=h1, q=q, k=k, v=v, a=a, o=o, h2=h2, gu=gu, u=u, f=f, r=r)
+    return {key: val.numpy() for key, val in out.items()}
+
+
+def close_bf16(x, ref):
+    """bf16 hand-off agreement: elementwise 2e-2 * max(1, |ref|), rel-L2 1e-2."""
+    x, ref = np.asarray(x).reshape(ref.shape), np.asarray(ref)
+    ok_el = np.all(np.abs(x - ref) <= 2e-2 * np.maximum(1.0, np.abs(ref)))
+    ok_l2 = np.linalg.norm(x - ref) <= 1e-2 * np.linalg.norm(ref)
+    return ok_el and ok_l2
+
+
+def check_block(o):
+    shape, n = tiny_block()
+    out, mids = run_block(o, shape, n, inter=True)
+    ref = torch_block(shape, n)
+    for key in ("h1", "q", "k", "v", "a", "o", "h2", "gu", "u", "f"):
+        assert close_bf16(mids[key], ref[key]), key
+    assert close_bf16(out, ref["r"])
+    # zero output projections leave the residual untouched
+    z = run_block(o, shape, n, w_o=np.zeros_like(n["w_o"]), w_down=np.zeros_like(n["w_down"]))
+    assert np.array_equal(z, n["resid"][:shape.L])
+    # zero gates too
+    mod0 = n["mod"].copy(); mod0[2] = 0; mod0[5] = 0
+    assert np.array_equal(run_block(o, shape, n, mod=mod0), n["resid"][:shape.L])
+    # pad-row garbage does not reach valid rows
+    r2 = n["resid"].copy(); r2[shape.L:] = 1e4
+    p2 = n["pos"].copy(); p2[shape.L:] = 77
+    assert np.array_equal(run_block(o, shape, n, resid=r2, pos=p2), out)
+    # a subset of rows equals the same rows of the full evaluation
+    rows = [17, 2, 0]
+    assert np.array_equal(run_block(o, shape, n, rows=rows), out[rows])
+
+
+def test_block():
+    check_block(O)
+
+
+# --------------------------------------------- planted mistakes are caught
+def _mutant(**repl):
+    m = types.ModuleType("oracle_mutant")
+    m.__dict__.update({k: v for k, v in O.__dict__.items() if not k.startswith("__")})
+    for name, fn in repl.items():
+        m.__dict__[name] = fn
+    # functions look their helpers up in their own globals: rebind them
+    for k, v in list(m.__dict__.items()):
+        if isinstance(v, types.FunctionType) and k not in repl:
+            m.__dict__[k] = types.FunctionType(v.__code__, m.__dict__, v.__name__, v.__defaults__,
+                                               v.__closure__)
+            m.__dict__[k].__kwdefaults__ = v.__kwdefaults__
+    return m
+
+
+def _rope_wrong_sign(x, phi):
+    return O.rope_apply(x, -phi)
+
+
+def _rope_half_split(x, phi):
+    x = np.asarray(x, np.float64)
+    h = x.shape[-1] // 2
+    c, s = np.cos(phi)[:, None, :], np.sin(phi)[:, None, :]
+    out = np.empty_like(x)
+    out[..., :h] = x[..., :h] * c - x[..., h:] * s
+    out[..., h:] = x[..., :h] * s + x[..., h:] * c
+    return out
+
+
+def _angles_global_exponent(pos, axis_dims, theta):
+    hd = sum(axis_dims)
+    pos = np.asarray(pos, np.float64)
+    cols = []
+    for a, d in enumerate(axis_dims):
+        if d:
+            j = np.arange(d // 2)
+            cols.append(pos[:, a:a + 1] * theta ** (-2.0 * j / hd))
+    return np.concatenate(cols, 1)
+
+
+def _mod_no_one_plus(resid, delta=None, gate=None, shift=None, scale=None, eps=1e-6):
+    r = np.asarray(resid, np.float64)
+    if delta is not None:
+        r = O.round_f32(r + gate[None] * delta)
+    h = None if scale is None else O.round_bf16(O.layer_norm(r, eps) * scale[None] + shift[None])
+    return r, h
+
+
+def _swiglu_swapped(gu):
+    F = gu.shape[-1] // 2
+    return O.round_bf16(O.silu(gu[..., F:]) * gu[..., :F])
+
+
+def _ln_no_center(x, eps):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt((x * x).mean(-1, keepdims=True) + eps)
+
+
+def _attn_no_max_mask(q, k, v, L, scale, rows=None):
+    return O.attention(q, k, v, k.shape[0], scale, rows=rows if rows is not None else np.arange(L))
+
+
+def _softmax_wrong_axis(z, axis=-1):
+    return O.softmax(z, axis=0)
+
+
+@pytest.mark.parametrize("name,mut,checks", [
+    ("rope sign", dict(rope_apply=_rope_wrong_sign), ["check_rope"]),
+    ("rope half-split pairing", dict(rope_apply=_rope_half_split), ["check_rope"]),
+    ("rope global exponent", dict(rope_angles=_angles_global_exponent), ["check_rope"]),
+    ("modulation without 1+", dict(mod_norm_residual=_mod_no_one_plus), ["check_mod_norm_residual"]),
+    ("swiglu halves swapped", dict(swiglu=_swiglu_swapped), ["check_swiglu"]),
+    ("layernorm not centred", dict(layer_norm=_ln_no_center), ["check_layer_norm"]),
+    ("attention keys past L", dict(attention=_attn_no_max_mask), ["check_attention"]),
+    ("softmax over queries", dict(softmax=_softmax_wrong_axis), ["check_attention"]),
+    ("block with swapped rope", dict(rope_apply=_rope_wrong_sign), ["check_block"]),
+    ("block with swapped swiglu", dict(swiglu=_swiglu_swapped), ["check_block"]),
+])
+def test_planted_mistake_is_caught(name, mut, checks):
+    m = _mutant(**mut)
+    for c in checks:
+        with pytest.raises(AssertionError):
+            globals()[c](m)
