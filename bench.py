@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of one joint audio-video DiT block forward on GB300.
+
+A step is one pass of the whole block (modulation + LN, QKV projection, Q/K
+RMSNorm + RoPE, valid-length attention, output projection, residual +
+modulation + LN, gate/up projection with SwiGLU, down projection, residual)
+over the packed sequence of 58,758 valid tokens in a 58,816-token buffer
+(hidden 5376, 42 x 128 heads, SwiGLU inner 14336, 3-axis RoPE 32/48/48), the
+workload of the vLLM-Omni MiniMax H3 blog, section 3.1.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun), every rank runs its own
+replica of the block on its own GPU ("replicas only": the block has no
+exchange step on one GPU) and the time is the maximum over ranks.
+--impl reference times the CPU oracle (plain NumPy FP64) on a bounded sample
+of the same workload, extrapolated to one block.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DiT block fwd ms & attention TFLOP/s at 58,758-token packed seq; % of BF16 peak"
+WORKLOAD = ("full DiT block forward: packed sequence L=58758 valid of S=58816, D=5376, "
+            "42 heads x 128, SwiGLU F=14336, 3-axis RoPE 32/48/48")
+
+
+def args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ----------------------------------------------------------------- work model
+def block_work(S, L, D, H, Dh, F):
+    """Algorithmic FLOPs and bytes of one block (valid rows only)."""
+    attn = 4.0 * L * L * H * Dh
+    gemm = 2.0 * L * D * (3 * D) + 2.0 * L * D * D + 2.0 * L * D * (2 * F) + 2.0 * L * F * D
+    # bytes of the HBM-bound stages, as launched (unfused between kernels)
+    mnr = L * D * (4 + 2) + L * D * (4 + 2 + 4 + 2) + L * D * (4 + 2 + 4)
+    qk = 2 * L * D * 2 * 2
+    return dict(attn_flop=attn, gemm_flop=gemm, elementwise_bytes=mnr + qk)
+
+
+# -------------------------------------------------------------- clock sampler
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------- CPU baseline leg
+def oracle_sample(shape, n_kv=512, n_q=8, seed=3):
+    """Times the oracle on a bounded sample of one block and extrapolates.
+
+    Sample: the key/value stage (LayerNorm + K and V projections + K
+    RMSNorm/RoPE) for n_kv rows, and the per-query path (LayerNorm, Q
+    projection, Q RMSNorm/RoPE, attention over all L keys, output projection,
+    residual + LayerNorm, gate/up projection, SwiGLU, down projection,
+    residual) for n_q rows. One block = L x (t_kv / n_kv + t_q / n_q).
+    """
+    import numpy as np
+    import torch
+
+    import oracle.h3_oracle as O
+    from dit_transformer_block_gb300 import inputs as I
+
+    g = torch.Generator().manual_seed(seed)
+    D, H, Dh, F, L = shape.D, shape.H, shape.Dh, shape.F, shape.L
+    bf = lambda *s, std=1.0: (torch.randn(*s, generator=g) * std).to(torch.bfloat16).double().numpy()
+    w_qkv = bf(3 * D, D, std=0.02)
+    w_o = bf(D, D, std=0.02)
+    w_gu = bf(2 * F, D, std=0.02)
+    w_down = bf(D, F, std=0.02)
+    gain = 1 + 0.1 * torch.randn(Dh, generator=g).double().numpy()
+    mod = 0.1 * torch.randn(6, D, generator=g).double().numpy()
+    pos = I.positions_3d(shape.S, L).numpy()
+    x_kv = bf(n_kv, D)
+    x_q = bf(n_q, D)
+    # keys/values of the full sequence for the query rows to attend to
+    # (drawn, not computed: their cost is the K/V stage timed above)
+    k_all = bf(L, H, Dh)
+    v_all = bf(L, H, Dh)
+
+    t0 = time.perf_counter()
+    _, h = O.mod_norm_residual(x_kv, shift=mod[0], scale=mod[1])
+    k = O.linear(h, w_qkv[D:2 * D]).reshape(n_kv, H, Dh)
+    O.qk_norm_rope(k, gain, pos[:n_kv], shape.axis_dims, shape.theta, shape.eps_qk)
+    O.linear(h, w_qkv[2 * D:])
+    t_kv = time.perf_counter() - t0
+
+    t0 = time.perf_counter()
+    r = x_q
+    _, h1 = O.mod_norm_residual(r, shift=mod[0], scale=mod[1])
+    q = O.linear(h1, w_qkv[:D]).reshape(n_q, H, Dh)
+    q = O.qk_norm_rope(q, gain, pos[L - n_q:L], shape.axis_dims, shape.theta, shape.eps_qk)
+    qf = np.zeros((L, H, Dh))
+    rows = np.arange(L - n_q, L)
+    qf[rows] = q
+    a = O.attention(qf, k_all, v_all, L, Dh ** -0.5, rows=rows).reshape(n_q, D)
+    o = O.linear(a, w_o)
+    r, h2 = O.mod_norm_residual(r, o, mod[2], mod[3], mod[4])
+    u = O.swiglu(O.linear(h2, w_gu))
+    f = O.linear(u, w_down)
+    O.mod_norm_residual(r, f, mod[5])
+    t_q = time.perf_counter() - t0
+    ms = L * (t_kv / n_kv + t_q / n_q) * 1e3
+    desc = (f"oracle (NumPy FP64) on {n_kv} key/value rows + {n_q} full query rows of the "
+            f"L={L} block, extrapolated linearly to all rows")
+    return ms, desc, t_kv + t_q
+
+
+def cpu_cores():
+    try:
+        import numpy  # noqa: F401
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from dit_transformer_block_gb300 import inputs as I
+    shape = I.FULL
+    times = []
+    desc = ""
+    for i in range(a.warmup + a.steps):
+        ms, desc, _ = oracle_sample(shape, n_kv=256, n_q=4, seed=100 + i)
+        if i >= a.warmup:
+            times.append(ms)
+    value = statistics.mean(times)
+    cores = cpu_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "ms",
+            "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": round(value, 1), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": round(value, 1), "unit": "ms", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 1), "unit": "ms", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def profile_traffic(kernel_file: str, profile_md: str):
+    """DRAM bytes per launch recorded in a committed ncu summary, if the
+    kernel source it was taken from is unchanged."""
+    p = os.path.join(ROOT, "profiles", profile_md)
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", text)
+    if not m or not h:
+        return None
+    src = open(os.path.join(ROOT, "dit_transformer_block_gb300", "csrc", kernel_file), "rb").read()
+    if not hashlib.sha256(src).hexdigest().startswith(h.group(1)):
+        return None
+    return float(m.group(1))
+
+
+def run_ours(a):
+    import torch
+    import torch.distributed as dist
+
+    from dit_transformer_block_gb300 import build, h3
+    from dit_transformer_block_gb300 import inputs as I
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    h3.lib()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    shape = I.FULL
+    S, L, D, H, Dh, F = shape.S, shape.L, shape.D, shape.H, shape.Dh, shape.F
+    inp = I.block_inputs(shape, seed=3 + rank, device=dev)
+    cfg = h3.block_config(S, L, D, H, Dh, F, shape.axis_dims, shape.theta, shape.eps_ln,
+                          shape.eps_qk)
+    ws = torch.empty(h3.block_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    weights = h3.block_weights(inp)
+    resid = inp["resid"].clone()
+    stream = torch.cuda.current_stream()
+
+    nev = h3.BLOCK_STAGES + 1
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(a.steps)]
+    for row in events:  # create the event handles before they are handed to the library
+        for e in row:
+            e.record(stream)
+
+    for _ in range(a.warmup):
+        h3.block_forward(cfg, weights, resid, inp["mod"], inp["pos"], ws)
+    h3.check_device_error()
+
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_uuid(torch, local)) as clocks:
+        time.sleep(0.3)
+        t_start.record(stream)
+        for k in range(a.steps):
+            h3.block_forward(cfg, weights, resid, inp["mod"], inp["pos"], ws, events=events[k])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    h3.check_device_error()
+    if not bool(torch.isfinite(resid[:L]).all()):
+        raise RuntimeError("non-finite block output")
+    total_ms = t_start.elapsed_time(t_end)
+    stage_ms = [statistics.mean(events[k][i].elapsed_time(events[k][i + 1])
+                                for k in range(a.steps)) for i in range(h3.BLOCK_STAGES)]
+    step_ms = total_ms / a.steps
+    if world > 1:
+        t = torch.tensor([step_ms] + stage_ms, device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, stage_ms = t[0].item(), t[1:].tolist()
+
+    # ---- end to end through the C-ABI with host buffers
+    pin = lambda t: t.detach().to("cpu").pin_memory()
+    h_resid, h_mod, h_pos = pin(inp["resid"]), pin(inp["mod"]), pin(inp["pos"])
+    h_out = torch.empty_like(h_resid).pin_memory()
+    d_resid = torch.empty_like(inp["resid"])
+    d_mod = torch.empty_like(inp["mod"])
+    d_pos = torch.empty_like(inp["pos"])
+    h2d = h_resid.numel() * 4 + h_mod.numel() * 4 + h_pos.numel() * 4
+    d2h = h_out.numel() * 4
+
+    def e2e_step():
+        d_resid.copy_(h_resid, non_blocking=True)
+        d_mod.copy_(h_mod, non_blocking=True)
+        d_pos.copy_(h_pos, non_blocking=True)
+        h3.block_forward(cfg, weights, d_resid, d_mod, d_pos, ws)
+        h_out.copy_(d_resid, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(a.e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / a.e2e_steps
+    barrier()
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+    h3.check_device_error()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    pk = peaks()
+    work = block_work(S, L, D, H, Dh, F)
+    attn_ms = stage_ms[3]
+    gemm_ms = stage_ms[1] + stage_ms[4] + stage_ms[6] + stage_ms[7]
+    ew_ms = stage_ms[0] + stage_ms[2] + stage_ms[5] + stage_ms[8]
+    attn_tf = work["attn_flop"] / attn_ms / 1e9
+    gemm_tf = work["gemm_flop"] / gemm_ms / 1e9
+    traffic = profile_traffic("h3_attention.cu", "attention_full_size.md")
+    cpu = None
+    if not a.no_cpu_baseline and world == 1:
+        ms, desc, secs = oracle_sample(shape)
+        cpu = {"value": round(ms, 1), "unit": "ms", "cores": cpu_cores(), "kind": "oracle",
+               "sample": desc + f" ({secs:.1f} s of CPU work)"}
+    value = step_ms / world  # whole-job ms per block forward (replicas)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "ms", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(step_ms, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded: x~N(0,1), W~N(0,0.02) bf16; FP32 residual and modulation)",
+        "config": {"workload": WORKLOAD, "S": S, "L": L, "D": D, "heads": H, "head_dim": Dh,
+                   "ffn": F, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (no flush between steps)"},
+        "attention_ms": round(attn_ms, 3), "attention_tflops": round(attn_tf, 1),
+        "attention_frac_bf16_peak": round(attn_tf / pk["bf16_sustained"], 3),
+        "gemm_ms": round(gemm_ms, 3), "gemm_tflops": round(gemm_tf, 1),
+        "gemm_frac_bf16_peak": round(gemm_tf / pk["bf16_sustained"], 3),
+        "elementwise_ms": round(ew_ms, 3),
+        "elementwise_gbs": round(work["elementwise_bytes"] / ew_ms / 1e6, 1),
+        "stages_ms": {n: round(t, 3) for n, t in zip(h3.STAGE_NAMES, stage_ms)},
+        "roofline": {"bound": "tensor", "kernel": "attention_kernel",
+                     "achieved": round(attn_tf, 1), "peak": pk["bf16_sustained"],
+                     "unit": "TFLOP/s", "frac": round(attn_tf / pk["bf16_sustained"], 3),
+                     "traffic": traffic,
+                     "peak_source": f"{pk['source']} bf16 sustained (kernel timed inside a long step)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": h3.BLOCK_STAGES * a.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    a = args()
+    if a.impl == "reference":
+        return run_reference(a)
+    return run_ours(a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

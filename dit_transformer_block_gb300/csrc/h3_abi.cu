@@ -1,0 +1,459 @@
+// C-ABI boundary of libh3block: argument validation, error reporting, TMA
+// descriptor creation, and the block forward composed from the kernels.
+// Every entry point validates on the host and launches nothing on error.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "h3_internal.cuh"
+
+namespace h3 {
+
+namespace {
+thread_local char g_msg[512] = "";
+uint64_t g_timeout_ns = 2000000000ull;
+constexpr int kMaxDevices = 64;
+
+// Device error word: first nonzero code recorded by a bounded wait.
+__device__ uint32_t g_dev_error_word;
+
+struct DeviceState {
+  bool ready = false;
+  uint32_t* err_word = nullptr;
+  int sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+h3_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev >= kMaxDevices) return fail(H3_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dev_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    d.err_word = static_cast<uint32_t*>(p);
+    d.sms = sms;
+    d.ready = true;
+  }
+  *out = &d;
+  return H3_OK;
+}
+
+__global__ void wait_timeout_kernel(DevErr err) {
+  __shared__ uint64_t b;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&b), 1);
+    fence_mbar_init();
+    // nothing ever arrives: the wait must run out and record its code
+    mbar_wait(smem_u32(&b), 0, err, ERR_WAIT_PROBE);
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+const char* err_code_name(uint32_t c) {
+  switch (c) {
+    case ERR_WAIT_GEMM_PRODUCER: return "gemm TMA producer";
+    case ERR_WAIT_GEMM_MMA: return "gemm MMA issuer";
+    case ERR_WAIT_GEMM_EPILOGUE: return "gemm epilogue";
+    case ERR_WAIT_ATTN_PRODUCER: return "attention TMA producer";
+    case ERR_WAIT_ATTN_MMA: return "attention MMA issuer";
+    case ERR_WAIT_ATTN_SOFTMAX: return "attention softmax";
+    case ERR_WAIT_PROBE: return "wait-timeout probe";
+    default: return "unknown";
+  }
+}
+}  // namespace
+
+h3_status fail(h3_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+h3_status cuda_fail(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return H3_OK;
+  return fail(H3_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+void clear_error() { g_msg[0] = '\0'; }
+
+h3_status dev_err(DevErr* out) {
+  DeviceState* d = nullptr;
+  h3_status st = device_state(&d);
+  if (st != H3_OK) return st;
+  out->word = d->err_word;
+  out->timeout_ns = g_timeout_ns;
+  return H3_OK;
+}
+
+int num_sms() {
+  DeviceState* d = nullptr;
+  if (device_state(&d) != H3_OK) return 1;
+  return d->sms;
+}
+
+h3_status make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (g_encode == nullptr)
+    return fail(H3_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(H3_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llux%llu stride %llu",
+                static_cast<int>(r), static_cast<unsigned long long>(inner),
+                static_cast<unsigned long long>(outer),
+                static_cast<unsigned long long>(row_stride_bytes));
+  return H3_OK;
+}
+
+}  // namespace h3
+
+using namespace h3;
+
+#define H3_REQUIRE(cond, code, ...) \
+  do {                              \
+    if (!(cond)) return fail(code, __VA_ARGS__); \
+  } while (0)
+
+static h3_status check_rows(int S, int L) {
+  H3_REQUIRE(S >= 0 && L >= 0, H3_ERR_INVALID_ARG, "negative size (S=%d, L=%d)", S, L);
+  H3_REQUIRE(L <= S, H3_ERR_INVALID_ARG, "L=%d exceeds the buffer rows S=%d", L, S);
+  return H3_OK;
+}
+
+extern "C" {
+
+int h3_version(void) { return (1 << 16) | 0; }
+
+const char* h3_last_error(void) { return g_msg; }
+
+const char* h3_status_string(h3_status s) {
+  switch (s) {
+    case H3_OK: return "H3_OK";
+    case H3_ERR_INVALID_ARG: return "H3_ERR_INVALID_ARG";
+    case H3_ERR_UNSUPPORTED: return "H3_ERR_UNSUPPORTED";
+    case H3_ERR_MISALIGNED: return "H3_ERR_MISALIGNED";
+    case H3_ERR_WORKSPACE: return "H3_ERR_WORKSPACE";
+    case H3_ERR_CUDA: return "H3_ERR_CUDA";
+    case H3_ERR_TIMEOUT: return "H3_ERR_TIMEOUT";
+  }
+  return "H3_ERR_UNKNOWN";
+}
+
+void h3_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns ? ns : 2000000000ull; }
+
+h3_status h3_check_device_error(h3_stream_t stream) {
+  clear_error();
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t code = 0;
+  e = cudaMemcpyFromSymbol(&code, g_dev_error_word, sizeof(code));
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (code != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    return fail(H3_ERR_TIMEOUT, "bounded wait ran out in %s (code 0x%x)", err_code_name(code),
+                code);
+  }
+  return H3_OK;
+}
+
+h3_status h3_debug_wait_timeout(uint64_t timeout_ns, h3_stream_t stream) {
+  clear_error();
+  DevErr err;
+  h3_status st = dev_err(&err);
+  if (st != H3_OK) return st;
+  err.timeout_ns = timeout_ns;
+  wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);
+  return cuda_fail(cudaGetLastError(), "wait-timeout probe launch");
+}
+
+h3_status h3_mod_norm_residual(float* resid, const void* delta, const float* gate,
+                               const float* shift, const float* scale, void* normed, int S,
+                               int L, int D, float eps, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(resid != nullptr, H3_ERR_INVALID_ARG, "resid is NULL");
+  H3_REQUIRE(delta != nullptr || normed != nullptr, H3_ERR_INVALID_ARG,
+             "neither delta nor normed given: nothing to do");
+  H3_REQUIRE(delta == nullptr || gate != nullptr, H3_ERR_INVALID_ARG, "delta given without gate");
+  H3_REQUIRE(normed == nullptr || (shift != nullptr && scale != nullptr), H3_ERR_INVALID_ARG,
+             "normed given without shift and scale");
+  H3_REQUIRE(D > 0 && D % 8 == 0, H3_ERR_UNSUPPORTED, "D=%d must be a positive multiple of 8", D);
+  H3_REQUIRE(D <= 8192, H3_ERR_UNSUPPORTED, "D=%d exceeds 8192", D);
+  H3_REQUIRE(eps >= 0.f, H3_ERR_INVALID_ARG, "eps < 0");
+  H3_REQUIRE(aligned16(resid) && aligned16(delta) && aligned16(gate) && aligned16(shift) &&
+                 aligned16(scale) && aligned16(normed),
+             H3_ERR_MISALIGNED, "a pointer is not 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_mod_norm_residual(resid, delta, gate, shift, scale, normed, L, D, eps,
+                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_qk_norm_rope(void* q, void* k, const float* q_gain, const float* k_gain,
+                          const int32_t* pos, const int* axis_dims, int S, int L, int H, int Dh,
+                          float theta, float eps, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(q && k && q_gain && k_gain && pos && axis_dims, H3_ERR_INVALID_ARG,
+             "a required pointer is NULL");
+  H3_REQUIRE(Dh == 128, H3_ERR_UNSUPPORTED, "head_dim %d unsupported (128 only)", Dh);
+  H3_REQUIRE(H > 0, H3_ERR_INVALID_ARG, "H=%d", H);
+  int sum = 0;
+  for (int a = 0; a < 3; ++a) {
+    H3_REQUIRE(axis_dims[a] >= 0 && axis_dims[a] % 2 == 0, H3_ERR_INVALID_ARG,
+               "axis_dims[%d]=%d must be even and >= 0", a, axis_dims[a]);
+    sum += axis_dims[a];
+  }
+  H3_REQUIRE(sum == Dh, H3_ERR_INVALID_ARG, "axis_dims sum %d != head_dim %d", sum, Dh);
+  H3_REQUIRE(theta > 0.f && eps >= 0.f, H3_ERR_INVALID_ARG, "theta must be > 0 and eps >= 0");
+  H3_REQUIRE(aligned16(q) && aligned16(k) && aligned16(q_gain) && aligned16(k_gain),
+             H3_ERR_MISALIGNED, "q, k and the gains must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_qk_norm_rope(q, k, static_cast<int64_t>(H) * Dh, q_gain, k_gain, pos, axis_dims,
+                             L, H, theta, eps, reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_attention_varlen(const void* q, const void* k, const void* v, void* o, int S,
+                              int L, int H, int Dh, float softmax_scale, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(q && k && v && o, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  H3_REQUIRE(Dh == 128, H3_ERR_UNSUPPORTED, "head_dim %d unsupported (128 only)", Dh);
+  H3_REQUIRE(H > 0 && H <= 65535, H3_ERR_INVALID_ARG, "H=%d", H);
+  H3_REQUIRE(softmax_scale > 0.f, H3_ERR_INVALID_ARG, "softmax_scale must be > 0");
+  H3_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(o), H3_ERR_MISALIGNED,
+             "q, k, v, o must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  const int64_t ld = static_cast<int64_t>(H) * Dh;
+  return launch_attention(q, k, v, ld, o, ld, L, H, softmax_scale,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_swiglu(const void* gate_up, void* out, int S, int L, int F, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(gate_up && out, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  H3_REQUIRE(F > 0 && F % 8 == 0, H3_ERR_UNSUPPORTED, "F=%d must be a positive multiple of 8", F);
+  H3_REQUIRE(aligned16(gate_up) && aligned16(out), H3_ERR_MISALIGNED,
+             "gate_up and out must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_swiglu(gate_up, out, L, F, reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_linear(const void* x, const void* w, void* y, int S, int L, int N, int K,
+                    h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(x && w && y, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  H3_REQUIRE(N > 0 && N % 256 == 0, H3_ERR_UNSUPPORTED, "N=%d must be a multiple of 256", N);
+  H3_REQUIRE(K > 0 && K % 64 == 0, H3_ERR_UNSUPPORTED, "K=%d must be a multiple of 64", K);
+  H3_REQUIRE(aligned16(x) && aligned16(w) && aligned16(y), H3_ERR_MISALIGNED,
+             "x, w, y must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_gemm(x, K, w, K, y, N, L, N, K, GEMM_STORE_BF16,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_linear_swiglu(const void* x, const void* w_gu, void* out, int S, int L, int F, int K,
+                           h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(x && w_gu && out, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  H3_REQUIRE(F > 0 && F % 128 == 0, H3_ERR_UNSUPPORTED, "F=%d must be a multiple of 128", F);
+  H3_REQUIRE(K > 0 && K % 64 == 0, H3_ERR_UNSUPPORTED, "K=%d must be a multiple of 64", K);
+  H3_REQUIRE(aligned16(x) && aligned16(w_gu) && aligned16(out), H3_ERR_MISALIGNED,
+             "x, w_gu, out must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_gemm(x, K, w_gu, K, out, F, L, F, K, GEMM_SWIGLU,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+static h3_status check_block_config(const h3_block_config* c) {
+  H3_REQUIRE(c != nullptr, H3_ERR_INVALID_ARG, "config is NULL");
+  h3_status st = check_rows(c->S, c->L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(c->Dh == 128, H3_ERR_UNSUPPORTED, "head_dim %d unsupported (128 only)", c->Dh);
+  H3_REQUIRE(c->H > 0 && c->D == c->H * c->Dh, H3_ERR_INVALID_ARG, "D=%d != H*Dh=%d", c->D,
+             c->H * c->Dh);
+  H3_REQUIRE(c->D % 256 == 0 && c->D <= 8192, H3_ERR_UNSUPPORTED,
+             "D=%d must be a multiple of 256 and at most 8192", c->D);
+  H3_REQUIRE(c->F > 0 && c->F % 128 == 0, H3_ERR_UNSUPPORTED, "F=%d must be a multiple of 128",
+             c->F);
+  int sum = 0;
+  for (int a = 0; a < 3; ++a) {
+    H3_REQUIRE(c->axis_dims[a] >= 0 && c->axis_dims[a] % 2 == 0, H3_ERR_INVALID_ARG,
+               "axis_dims[%d]=%d must be even and >= 0", a, c->axis_dims[a]);
+    sum += c->axis_dims[a];
+  }
+  H3_REQUIRE(sum == c->Dh, H3_ERR_INVALID_ARG, "axis_dims sum %d != head_dim %d", sum, c->Dh);
+  H3_REQUIRE(c->theta > 0.f && c->eps_ln >= 0.f && c->eps_qk >= 0.f, H3_ERR_INVALID_ARG,
+             "theta must be > 0 and the epsilons >= 0");
+  return H3_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace slices (bf16, S rows each): h [D] (h1, later h2), qkv [3D],
+// attn [D], proj [D] (attention projection, later FFN down), ffn [F].
+struct BlockWs {
+  size_t h, qkv, attn, proj, ffn, total;
+};
+static BlockWs block_ws(const h3_block_config* c) {
+  BlockWs w;
+  const size_t row = static_cast<size_t>(c->S) * 2;
+  size_t off = 0;
+  w.h = off;    off += align256(row * c->D);
+  w.qkv = off;  off += align256(row * 3 * c->D);
+  w.attn = off; off += align256(row * c->D);
+  w.proj = off; off += align256(row * c->D);
+  w.ffn = off;  off += align256(row * c->F);
+  w.total = off;
+  return w;
+}
+
+size_t h3_block_workspace_bytes(const h3_block_config* cfg) {
+  clear_error();
+  if (check_block_config(cfg) != H3_OK) return 0;
+  return block_ws(cfg).total;
+}
+
+static h3_status block_forward_impl(const h3_block_config* cfg, const h3_block_weights* w,
+                                    float* resid, const float* mod, const int32_t* pos,
+                                    void* workspace, size_t workspace_bytes, h3_stream_t stream,
+                                    void* const* events, int num_events) {
+  clear_error();
+  h3_status st = check_block_config(cfg);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(w != nullptr, H3_ERR_INVALID_ARG, "weights struct is NULL");
+  H3_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_down && w->q_gain && w->k_gain,
+             H3_ERR_INVALID_ARG, "a weight pointer is NULL");
+  H3_REQUIRE(resid && mod && pos, H3_ERR_INVALID_ARG, "resid, mod and pos must not be NULL");
+  const BlockWs ws = block_ws(cfg);
+  H3_REQUIRE(workspace != nullptr && workspace_bytes >= ws.total, H3_ERR_WORKSPACE,
+             "workspace of %zu bytes given, %zu needed", workspace_bytes, ws.total);
+  H3_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, H3_ERR_MISALIGNED,
+             "workspace must be 256-byte aligned");
+  H3_REQUIRE(aligned16(w->w_qkv) && aligned16(w->w_o) && aligned16(w->w_gu) &&
+                 aligned16(w->w_down) && aligned16(w->q_gain) && aligned16(w->k_gain) &&
+                 aligned16(resid) && aligned16(mod),
+             H3_ERR_MISALIGNED, "weights, gains, resid and mod must be 16-byte aligned");
+  H3_REQUIRE(events == nullptr || num_events == H3_BLOCK_STAGES + 1, H3_ERR_INVALID_ARG,
+             "events: %d given, %d expected", num_events, H3_BLOCK_STAGES + 1);
+  if (events != nullptr)
+    for (int i = 0; i <= H3_BLOCK_STAGES; ++i)
+      H3_REQUIRE(events[i] != nullptr, H3_ERR_INVALID_ARG, "events[%d] is NULL", i);
+  if (cfg->L == 0) return H3_OK;
+
+  const int L = cfg->L, D = cfg->D, H = cfg->H, F = cfg->F;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  void* h = base + ws.h;
+  uint8_t* qkv = base + ws.qkv;
+  void* attn = base + ws.attn;
+  void* proj = base + ws.proj;
+  void* ffn = base + ws.ffn;
+  const float* shift1 = mod;
+  const float* scale1 = mod + D;
+  const float* gate1 = mod + 2 * D;
+  const float* shift2 = mod + 3 * D;
+  const float* scale2 = mod + 4 * D;
+  const float* gate2 = mod + 5 * D;
+  const int64_t ld_qkv = 3LL * D;
+  auto mark = [&](int i) -> h3_status {
+    if (events == nullptr) return H3_OK;
+    return cuda_fail(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s), "event record");
+  };
+#define H3_STAGE(i, call)                          \
+  do {                                             \
+    if ((st = mark(i)) != H3_OK) return st;        \
+    if ((st = (call)) != H3_OK) return st;         \
+  } while (0)
+
+  // 0: h1 = LN(r) * (1 + scale1) + shift1
+  H3_STAGE(0, launch_mod_norm_residual(resid, nullptr, nullptr, shift1, scale1, h, L, D,
+                                       cfg->eps_ln, s));
+  // 1: [q | k | v] = h1 W_qkv^T
+  H3_STAGE(1, launch_gemm(h, D, w->w_qkv, D, qkv, ld_qkv, L, 3 * D, D, GEMM_STORE_BF16, s));
+  // 2: q, k <- RoPE(RMSNorm(q, k)) per head
+  H3_STAGE(2, launch_qk_norm_rope(qkv, qkv + 2LL * D, ld_qkv, w->q_gain, w->k_gain, pos,
+                                  cfg->axis_dims, L, H, cfg->theta, cfg->eps_qk, s));
+  // 3: a = softmax(q k^T / sqrt(Dh)) v over keys < L
+  H3_STAGE(3, launch_attention(qkv, qkv + 2LL * D, qkv + 4LL * D, ld_qkv, attn, D, L, H,
+                               1.0f / sqrtf(static_cast<float>(cfg->Dh)), s));
+  // 4: o = a W_o^T
+  H3_STAGE(4, launch_gemm(attn, D, w->w_o, D, proj, D, L, D, D, GEMM_STORE_BF16, s));
+  // 5: r <- r + gate1 * o ; h2 = LN(r) * (1 + scale2) + shift2
+  H3_STAGE(5, launch_mod_norm_residual(resid, proj, gate1, shift2, scale2, h, L, D, cfg->eps_ln,
+                                       s));
+  // 6: s = SiLU(h2 W_g^T) * (h2 W_u^T), SwiGLU fused in the projection's epilogue
+  H3_STAGE(6, launch_gemm(h, D, w->w_gu, D, ffn, F, L, F, D, GEMM_SWIGLU, s));
+  // 7: f = s W_down^T
+  H3_STAGE(7, launch_gemm(ffn, F, w->w_down, F, proj, D, L, D, F, GEMM_STORE_BF16, s));
+  // 8: r <- r + gate2 * f
+  H3_STAGE(8, launch_mod_norm_residual(resid, proj, gate2, nullptr, nullptr, nullptr, L, D,
+                                       cfg->eps_ln, s));
+#undef H3_STAGE
+  return mark(H3_BLOCK_STAGES);
+}
+
+h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w, float* resid,
+                           const float* mod, const int32_t* pos, void* workspace,
+                           size_t workspace_bytes, h3_stream_t stream) {
+  return block_forward_impl(cfg, w, resid, mod, pos, workspace, workspace_bytes, stream, nullptr,
+                            0);
+}
+
+h3_status h3_block_forward_events(const h3_block_config* cfg, const h3_block_weights* w,
+                                  float* resid, const float* mod, const int32_t* pos,
+                                  void* workspace, size_t workspace_bytes, h3_stream_t stream,
+                                  void* const* events, int num_events) {
+  H3_REQUIRE(events != nullptr, H3_ERR_INVALID_ARG, "events is NULL");
+  return block_forward_impl(cfg, w, resid, mod, pos, workspace, workspace_bytes, stream, events,
+                            num_events);
+}
+
+}  // extern "C"

@@ -1,0 +1,287 @@
+// HBM-bound single-pass kernels of the DiT block: SwiGLU, per-head Q/K
+// RMSNorm + RoPE, and FP32 modulation + LayerNorm + residual. Each reads its
+// operands once with 16-byte (or 8-byte) vector loads, reduces with warp
+// shuffles, and writes its result once; only rows < L are touched.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "h3_internal.cuh"
+
+namespace h3 {
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+
+// ------------------------------------------------------------------ SwiGLU
+// vLLM-Omni H3 blog, section 3.2 (#6283): SiLU(g) * u in one launch.
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ uint32_t swiglu_pair(uint32_t g, uint32_t u) {
+  return pack_bf16x2(silu_f(bf16_lo(g)) * bf16_lo(u), silu_f(bf16_hi(g)) * bf16_hi(u));
+}
+
+constexpr int SWIGLU_THREADS = 256;
+constexpr int SWIGLU_UNROLL = 4;
+
+__global__ void __launch_bounds__(SWIGLU_THREADS)
+    swiglu_kernel(const uint4* __restrict__ gu, uint4* __restrict__ out, int L, int F8) {
+  for (int row = blockIdx.x; row < L; row += gridDim.x) {
+    const uint4* g_row = gu + static_cast<int64_t>(row) * 2 * F8;
+    const uint4* u_row = g_row + F8;
+    uint4* o_row = out + static_cast<int64_t>(row) * F8;
+    for (int c0 = threadIdx.x; c0 < F8; c0 += SWIGLU_THREADS * SWIGLU_UNROLL) {
+      uint4 g[SWIGLU_UNROLL], u[SWIGLU_UNROLL];
+#pragma unroll
+      for (int i = 0; i < SWIGLU_UNROLL; ++i) {
+        const int c = c0 + i * SWIGLU_THREADS;
+        if (c < F8) {
+          g[i] = ld_stream(g_row + c);
+          u[i] = ld_stream(u_row + c);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < SWIGLU_UNROLL; ++i) {
+        const int c = c0 + i * SWIGLU_THREADS;
+        if (c < F8) {
+          uint4 r;
+          r.x = swiglu_pair(g[i].x, u[i].x);
+          r.y = swiglu_pair(g[i].y, u[i].y);
+          r.z = swiglu_pair(g[i].z, u[i].z);
+          r.w = swiglu_pair(g[i].w, u[i].w);
+          __stcs(o_row + c, r);
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------ Q/K RMSNorm + RoPE
+// vLLM-Omni H3 blog, section 3.2 (#5990) and section 3.1 (per-token RoPE rows).
+// One warp owns one (row, tensor) pair: lanes 0-15 and 16-31 each cover one
+// 128-wide head (8 channels = 4 rotation pairs per lane), so a head's RMS is a
+// 16-lane shuffle reduction and every lane needs the angles of only its own
+// four pairs, computed once per row.
+constexpr int QK_HEAD_DIM = 128;
+constexpr int QK_WARPS = 8;
+constexpr int QK_BATCH = 8;  // head pairs loaded per batch (16 heads)
+
+struct RopeTable {
+  double omega[QK_HEAD_DIM / 2];  // angle per unit position for each pair
+  int axis[QK_HEAD_DIM / 2];      // which position (t, h, w) drives the pair
+};
+
+__global__ void __launch_bounds__(QK_WARPS * 32)
+    qk_norm_rope_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
+                        int64_t row_stride, const float* __restrict__ q_gain,
+                        const float* __restrict__ k_gain, const int32_t* __restrict__ pos,
+                        int L, int H, float eps, const RopeTable tab) {
+  const int warp = blockIdx.x * QK_WARPS + (threadIdx.x >> 5);
+  const int row = warp >> 1;
+  if (row >= L) return;
+  const int which = warp & 1;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 15;   // 8-channel slice of the head
+  const int half = lane >> 4;  // even / odd head of each pair
+
+  __nv_bfloat16* base = (which ? k : q) + static_cast<int64_t>(row) * row_stride + sub * 8;
+  const float* gp = (which ? k_gain : q_gain) + sub * 8;
+  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gp));
+  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp + 4));
+  const float gain[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+
+  // Angles of this lane's pairs: formed and reduced modulo 2*pi in FP64,
+  // then sin/cos in FP32 on an argument in [-pi, pi].
+  const int32_t p3[3] = {__ldg(pos + 3 * row), __ldg(pos + 3 * row + 1), __ldg(pos + 3 * row + 2)};
+  float cs[4], sn[4];
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
+  constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int pr = sub * 4 + t;
+    const double phi = static_cast<double>(p3[tab.axis[pr]]) * tab.omega[pr];
+    const double turns = rint(phi * kInvTwoPi);
+    const float red = static_cast<float>(fma(-turns, kTwoPi, phi));
+    sincosf(red, &sn[t], &cs[t]);
+  }
+
+  for (int h0 = 0; h0 < H; h0 += 2 * QK_BATCH) {
+    uint4 v[QK_BATCH];
+#pragma unroll
+    for (int i = 0; i < QK_BATCH; ++i) {
+      const int head = h0 + 2 * i + half;
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (head < H) v[i] = *reinterpret_cast<const uint4*>(base + head * QK_HEAD_DIM);
+    }
+#pragma unroll
+    for (int i = 0; i < QK_BATCH; ++i) {
+      const int head = h0 + 2 * i + half;
+      if (h0 + 2 * i >= H) break;  // uniform across the warp
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      float x[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = bf16_lo(w[j]);
+        x[2 * j + 1] = bf16_hi(w[j]);
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
+#pragma unroll
+      for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      const float inv = rsqrtf(ss * (1.0f / QK_HEAD_DIM) + eps);
+      uint32_t o[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float a = x[2 * t] * inv * gain[2 * t];
+        const float b = x[2 * t + 1] * inv * gain[2 * t + 1];
+        o[t] = pack_bf16x2(a * cs[t] - b * sn[t], a * sn[t] + b * cs[t]);
+      }
+      if (head < H)
+        *reinterpret_cast<uint4*>(base + head * QK_HEAD_DIM) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// ----------------------------------------- modulation + LayerNorm + residual
+// vLLM-Omni H3 blog, section 3.2 (#6281, #6878): FP32 modulation,
+// normalisation and residual in one pass. One CTA per row; each thread keeps
+// VPT float4 of the row in registers between the residual update and the
+// two-pass mean/variance.
+constexpr int MNR_THREADS = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red[] may still be read from a previous call
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = (lane < MNR_THREADS / 32) ? red[lane] : 0.f;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
+  return t;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(MNR_THREADS)
+    mod_norm_residual_kernel(float* __restrict__ resid, const __nv_bfloat16* __restrict__ delta,
+                             const float* __restrict__ gate, const float* __restrict__ shift,
+                             const float* __restrict__ scale, __nv_bfloat16* __restrict__ normed,
+                             int D, float eps) {
+  __shared__ float red[MNR_THREADS / 32];
+  const int row = blockIdx.x;
+  const int D4 = D >> 2;
+  float4* rrow = reinterpret_cast<float4*>(resid + static_cast<int64_t>(row) * D);
+  float4 x[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = threadIdx.x + v * MNR_THREADS;
+    x[v] = c < D4 ? rrow[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (delta != nullptr) {
+    const uint2* drow = reinterpret_cast<const uint2*>(delta + static_cast<int64_t>(row) * D);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = threadIdx.x + v * MNR_THREADS;
+      if (c < D4) {
+        const uint2 d = __ldcs(drow + c);
+        const float4 g = __ldg(reinterpret_cast<const float4*>(gate) + c);
+        x[v].x = fmaf(g.x, bf16_lo(d.x), x[v].x);
+        x[v].y = fmaf(g.y, bf16_hi(d.x), x[v].y);
+        x[v].z = fmaf(g.z, bf16_lo(d.y), x[v].z);
+        x[v].w = fmaf(g.w, bf16_hi(d.y), x[v].w);
+        rrow[c] = x[v];
+      }
+    }
+  }
+  if (normed == nullptr) return;
+  float s = 0.f;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) s += (x[v].x + x[v].y) + (x[v].z + x[v].w);
+  const float mean = block_sum(s, red) / static_cast<float>(D);
+  float s2 = 0.f;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = threadIdx.x + v * MNR_THREADS;
+    if (c < D4) {
+      const float a = x[v].x - mean, b = x[v].y - mean, cc = x[v].z - mean, d = x[v].w - mean;
+      s2 += (a * a + b * b) + (cc * cc + d * d);
+    }
+  }
+  const float var = block_sum(s2, red) / static_cast<float>(D);
+  const float rstd = rsqrtf(var + eps);
+  uint2* hrow = reinterpret_cast<uint2*>(normed + static_cast<int64_t>(row) * D);
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = threadIdx.x + v * MNR_THREADS;
+    if (c < D4) {
+      const float4 sc = __ldg(reinterpret_cast<const float4*>(scale) + c);
+      const float4 sh = __ldg(reinterpret_cast<const float4*>(shift) + c);
+      const float h0 = fmaf((x[v].x - mean) * rstd, 1.0f + sc.x, sh.x);
+      const float h1 = fmaf((x[v].y - mean) * rstd, 1.0f + sc.y, sh.y);
+      const float h2 = fmaf((x[v].z - mean) * rstd, 1.0f + sc.z, sh.z);
+      const float h3v = fmaf((x[v].w - mean) * rstd, 1.0f + sc.w, sh.w);
+      __stcs(hrow + c, make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3v)));
+    }
+  }
+}
+
+}  // namespace
+
+h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream_t s) {
+  const int F8 = F / 8;
+  const int grid = std::min(L, num_sms() * 8);
+  swiglu_kernel<<<grid, SWIGLU_THREADS, 0, s>>>(static_cast<const uint4*>(gate_up),
+                                                static_cast<uint4*>(out), L, F8);
+  return cuda_fail(cudaGetLastError(), "swiglu launch");
+}
+
+h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float* q_gain,
+                              const float* k_gain, const int32_t* pos, const int* axis_dims,
+                              int L, int H, float theta, float eps, cudaStream_t s) {
+  RopeTable tab;
+  int pr = 0;
+  for (int a = 0; a < 3; ++a) {
+    const int d = axis_dims[a];
+    for (int j = 0; j < d / 2; ++j, ++pr) {
+      tab.omega[pr] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(d));
+      tab.axis[pr] = a;
+    }
+  }
+  const int64_t warps = 2LL * L;
+  const int grid = static_cast<int>((warps + QK_WARPS - 1) / QK_WARPS);
+  qk_norm_rope_kernel<<<grid, QK_WARPS * 32, 0, s>>>(
+      static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k), row_stride, q_gain, k_gain,
+      pos, L, H, eps, tab);
+  return cuda_fail(cudaGetLastError(), "qk_norm_rope launch");
+}
+
+h3_status launch_mod_norm_residual(float* resid, const void* delta, const float* gate,
+                                   const float* shift, const float* scale, void* normed, int L,
+                                   int D, float eps, cudaStream_t s) {
+  const int vpt = (D / 4 + MNR_THREADS - 1) / MNR_THREADS;
+  const auto* d = static_cast<const __nv_bfloat16*>(delta);
+  auto* n = static_cast<__nv_bfloat16*>(normed);
+#define H3_MNR_CASE(V)                                                              \
+  case V:                                                                           \
+    mod_norm_residual_kernel<V><<<L, MNR_THREADS, 0, s>>>(resid, d, gate, shift, scale, n, D, \
+                                                          eps);                     \
+    break;
+  switch (vpt) {
+    H3_MNR_CASE(1)
+    H3_MNR_CASE(2)
+    H3_MNR_CASE(3)
+    H3_MNR_CASE(4)
+    H3_MNR_CASE(5)
+    H3_MNR_CASE(6)
+    H3_MNR_CASE(7)
+    H3_MNR_CASE(8)
+    default:
+      return fail(H3_ERR_UNSUPPORTED, "mod_norm_residual: D=%d exceeds 8192", D);
+  }
+#undef H3_MNR_CASE
+  return cuda_fail(cudaGetLastError(), "mod_norm_residual launch");
+}
+
+}  // namespace h3

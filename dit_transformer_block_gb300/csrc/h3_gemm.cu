@@ -1,0 +1,295 @@
+// tcgen05 GEMM for the block projections: C[:L] = epilogue(A[:L] @ B^T),
+// bf16 operands, FP32 accumulation in tensor memory, bf16 output.
+//
+// The matrix multiplies are the ones the fused small ops of the vLLM-Omni H3
+// blog (section 3.2) sit around: QKV, attention output, FFN gate/up, FFN down.
+//
+// Design (one CTA per SM, persistent over output tiles):
+//   * tile 128 x 256 (M x N), K step 64; A and B are K-major in global memory
+//     and land in shared memory through TMA with 128-byte swizzle;
+//   * a 4-stage ring of (A 16 KB + B 32 KB) stages, full/empty mbarriers;
+//   * warp 0: TMA producer (one lane); warp 1: TMEM allocator and MMA issuer
+//     (one lane, tcgen05.mma M=128 N=256 K=16); warps 2-5: epilogue, each owns
+//     the 32 TMEM lanes (= tile rows) its warp index selects;
+//   * two 256-column FP32 accumulators in TMEM so the epilogue of one tile
+//     overlaps the main loop of the next;
+//   * rows >= L are zero-filled by TMA on load and never stored.
+// Epilogues: plain bf16 store, or SwiGLU where the B tile's first 128 rows are
+// gate rows and the last 128 the matching up rows, and the 128 output columns
+// are SiLU(g) * u (both rounded to bf16 first, like the unfused path).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "h3_internal.cuh"
+
+namespace h3 {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BYTES = BN * BK * 2;        // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;              // two accumulators of BN columns
+constexpr int GROUP_M = 16;                 // raster: 16 M-blocks per N sweep
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+
+struct GemmArgs {
+  void* C;
+  int64_t ldc;
+  int M, N, K;            // M = valid rows; N = output columns
+  int num_m, num_n, num_k;
+  int num_tiles;
+  int ep;                 // GemmEpilogue
+  int b_half_rows;        // SwiGLU: row offset of the up half inside B
+  DevErr err;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
+  const int group_size = GROUP_M * a.num_n;
+  const int group = tile / group_size;
+  const int first_m = group * GROUP_M;
+  const int gm = min(a.num_m - first_m, GROUP_M);
+  const int r = tile - group * group_size;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* full = bars;                 // [STAGES]
+  uint64_t* empty = bars + STAGES;       // [STAGES]
+  uint64_t* tfull = bars + 2 * STAGES;   // [2]
+  uint64_t* tempty = tfull + 2;          // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 4);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, a, mb, nb);
+        int b_row0, b_row1;
+        if (a.ep == GEMM_SWIGLU) {
+          b_row0 = nb * (BN / 2);
+          b_row1 = a.b_half_rows + nb * (BN / 2);
+        } else {
+          b_row0 = nb * BN;
+          b_row1 = nb * BN + BN / 2;
+        }
+        for (int kb = 0; kb < a.num_k; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, ERR_WAIT_GEMM_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const int kx = kb * BK;
+          tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, fb, kx, mb * BM);
+          tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB, fb, kx, b_row0);
+          tma_load_2d(smem_u32(sB + stage * B_BYTES + B_BYTES / 2), &tmB, fb, kx, b_row1);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, a.err, ERR_WAIT_GEMM_MMA)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < a.num_k; ++kb) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, a.err, ERR_WAIT_GEMM_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + k * 32, 16, 1024);
+            mma_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&tfull[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------------ epilogue warps
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, a, mb, nb);
+      if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, a.err, ERR_WAIT_GEMM_EPILOGUE)) break;
+      tc_fence_after();
+      const int row = mb * BM + quarter * 32 + lane;
+      const bool row_ok = row < a.M;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+      __nv_bfloat16* crow =
+          static_cast<__nv_bfloat16*>(a.C) + static_cast<int64_t>(row) * a.ldc;
+      if (a.ep == GEMM_SWIGLU) {
+        const int col0 = nb * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2 / 32; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(t_row + c * 32, g);
+          tmem_ld32(t_row + BN / 2 + c * 32, u);
+          tmem_ld_wait();
+          tmem_reg_fence(g);
+          tmem_reg_fence(u);
+          uint32_t o[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = round_to_bf16(__uint_as_float(g[2 * j]));
+            const float g1 = round_to_bf16(__uint_as_float(g[2 * j + 1]));
+            const float u0 = round_to_bf16(__uint_as_float(u[2 * j]));
+            const float u1 = round_to_bf16(__uint_as_float(u[2 * j + 1]));
+            o[j] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+          }
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + col0 + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          }
+        }
+      } else {
+        const int col0 = nb * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(t_row + c * 32, v);
+          tmem_ld_wait();
+          tmem_reg_fence(v);
+          uint32_t o[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            o[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + col0 + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                      int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return cuda_fail(e, "gemm: set shared memory size");
+    attr_done[dev] = true;
+  }
+  GemmArgs a{};
+  a.C = C;
+  a.ldc = ldc;
+  a.M = L;
+  a.N = N;
+  a.K = K;
+  a.ep = ep;
+  const int b_rows = (ep == GEMM_SWIGLU) ? 2 * N : N;
+  const int tile_n = (ep == GEMM_SWIGLU) ? BN / 2 : BN;
+  a.b_half_rows = (ep == GEMM_SWIGLU) ? N : 0;
+  a.num_m = (L + BM - 1) / BM;
+  a.num_n = N / tile_n;
+  a.num_k = (K + BK - 1) / BK;
+  a.num_tiles = a.num_m * a.num_n;
+  h3_status st = dev_err(&a.err);
+  if (st != H3_OK) return st;
+
+  CUtensorMap tmA, tmB;
+  st = make_tmap_bf16_2d(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(L),
+                         static_cast<uint64_t>(lda) * 2, BK, BM);
+  if (st != H3_OK) return st;
+  st = make_tmap_bf16_2d(&tmB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(b_rows),
+                         static_cast<uint64_t>(ldb) * 2, BK, BN / 2);
+  if (st != H3_OK) return st;
+  const int grid = std::min(a.num_tiles, num_sms());
+  gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, a);
+  return cuda_fail(cudaGetLastError(), "gemm launch");
+}
+
+}  // namespace h3

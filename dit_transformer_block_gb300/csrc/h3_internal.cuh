@@ -1,0 +1,50 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/h3block.h"
+#include "h3_ptx.cuh"
+
+namespace h3 {
+
+// ---- error state (h3_abi.cu)
+h3_status fail(h3_status s, const char* fmt, ...);
+h3_status cuda_fail(cudaError_t e, const char* what);
+void clear_error();
+// Device error word and wait limit for kernels launched on the current device.
+h3_status dev_err(DevErr* out);
+int num_sms();
+
+// ---- TMA descriptors (h3_abi.cu). A 2D bf16 tensor of `outer` rows x `inner`
+// elements with the given row stride, boxes of box_inner x box_outer, 128-byte
+// swizzle, zero fill outside the tensor.
+h3_status make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ---- kernel launchers (arguments already validated)
+h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream_t s);
+h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float* q_gain,
+                              const float* k_gain, const int32_t* pos, const int* axis_dims,
+                              int L, int H, float theta, float eps, cudaStream_t s);
+h3_status launch_mod_norm_residual(float* resid, const void* delta, const float* gate,
+                                   const float* shift, const float* scale, void* normed, int L,
+                                   int D, float eps, cudaStream_t s);
+
+enum GemmEpilogue : int {
+  GEMM_STORE_BF16 = 0,   // C = bf16(acc)
+  GEMM_SWIGLU = 1,       // B rows [gate | up] of F each; C[:, j] = SiLU(g) * u, width F
+};
+// C[:L, :] = epilogue(A[:L, :K] @ B^T). A row stride lda, B [N, K] row stride
+// ldb, C row stride ldc (elements). For GEMM_SWIGLU, N is the width of C (= F)
+// and B holds 2N rows.
+h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                      int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s);
+
+// o[:L] = attention(q, k, v); q/k/v rows of stride ld_in elements, o of ld_out.
+h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
+                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s);
+
+}  // namespace h3

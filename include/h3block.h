@@ -1,0 +1,228 @@
+/*
+ * h3block — forward pass of one joint audio-video DiT block (MiniMax H3
+ * style) on a single NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the vLLM-Omni MiniMax H3 serving blog ("vLLM-Omni 上的
+ * MiniMax H3：从系统级优化到基于 FastVideo FastH3 的实时服务"):
+ *   section 3.1  one packed sequence of text, audio and video tokens; the
+ *                attention backend takes the valid length and does no work on
+ *                the structural tail padding; RoPE rows come from each
+ *                token's own positions; hidden width 5,376.
+ *   section 3.2  fused Q/K RMSNorm + RoPE (#5990), merged FP32 modulation +
+ *                normalisation + residual (#6281, #6878), fused SwiGLU in
+ *                place of separate SiLU and multiply launches (#6283), all
+ *                around the block's matrix multiplies.
+ *
+ * Conventions shared by every call
+ *   - Pointers are device memory owned by the caller (unless a parameter says
+ *     "host"). The library never allocates, frees or keeps a pointer after the
+ *     call returns.
+ *   - Tensors are row-major and contiguous. A "packed sequence" tensor has S
+ *     buffer rows of which the first L are valid. Rows >= L of every output
+ *     are left exactly as they were, and rows >= L of every input are never
+ *     read (pad rows may hold anything).
+ *   - bf16 tensors are passed as void* (IEEE bfloat16, 2 bytes per element).
+ *   - Base pointers must be 16-byte aligned, else H3_ERR_MISALIGNED.
+ *   - Work is queued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream). Calls return as soon as the work is queued and never
+ *     synchronise. Argument errors are detected on the host before anything
+ *     is launched; nothing is launched when a call returns an error.
+ *   - L == 0 is an empty sequence: the call does nothing and returns H3_OK.
+ *   - The device's current CUDA device must be the one that owns the memory.
+ *   - Every device-side wait is bounded. A wait that runs out records a code
+ *     in a device error word; h3_check_device_error() reports it.
+ */
+#ifndef H3BLOCK_H_
+#define H3BLOCK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum h3_status {
+  H3_OK = 0,
+  H3_ERR_INVALID_ARG = 1,   /* null pointer, negative size, L > S, ...        */
+  H3_ERR_UNSUPPORTED = 2,   /* a size this build has no kernel for            */
+  H3_ERR_MISALIGNED = 3,    /* a pointer or row stride not 16-byte aligned    */
+  H3_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required     */
+  H3_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed              */
+  H3_ERR_TIMEOUT = 6        /* a bounded device wait ran out (see below)      */
+} h3_status;
+
+/* ABI-identical to cudaStream_t. */
+typedef struct CUstream_st* h3_stream_t;
+
+/* Library version, (major << 16) | minor. */
+int h3_version(void);
+
+/* Message for the last error returned on the calling host thread (never NULL;
+ * "" when the last call succeeded). Valid until the next call on that thread. */
+const char* h3_last_error(void);
+
+/* Name of a status code. */
+const char* h3_status_string(h3_status s);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device. Returns H3_ERR_TIMEOUT (message names the waiting kernel
+ * role) when a bounded wait in an earlier kernel ran out, H3_ERR_CUDA when the
+ * stream reports an error, else H3_OK. */
+h3_status h3_check_device_error(h3_stream_t stream);
+
+/* Per-wait limit in nanoseconds used by kernels launched after this call
+ * (default 2e9). Host-side setting, process-wide. 0 restores the default. */
+void h3_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * a1 — FP32 modulation + normalisation + residual (blog section 3.2, #6281,
+ * #6878), one pass per row:
+ *   if delta != NULL:  resid[i,:] <- resid[i,:] + gate[:] * delta[i,:]   (FP32)
+ *   if normed != NULL: normed[i,:] <- bf16( LN(resid[i,:]) * (1 + scale[:]) + shift[:] )
+ * where LN is LayerNorm without affine over D with epsilon eps, computed in FP32
+ * from the updated residual.
+ *   resid  [S, D] float32, in/out          delta  [S, D] bf16 or NULL
+ *   gate   [D] float32 (required iff delta) shift, scale [D] float32 (required iff normed)
+ *   normed [S, D] bf16 or NULL
+ * At least one of delta / normed must be given. D % 8 == 0, D <= 8192.
+ */
+h3_status h3_mod_norm_residual(float* resid, const void* delta, const float* gate,
+                               const float* shift, const float* scale, void* normed,
+                               int S, int L, int D, float eps, h3_stream_t stream);
+
+/*
+ * a2 — per-head Q/K RMSNorm followed by rotary position embedding, in place
+ * (blog section 3.2, #5990; RoPE rows from per-token positions, section 3.1).
+ * For every valid row i, head h and x in {q, k} (gain g_q / g_k):
+ *   y = x[i,h,:] / sqrt(mean(x[i,h,:]^2) + eps) * g
+ *   head_dim is split into sections of axis_dims[0..2] channels for the
+ *   positions pos[i,0..2] = (t, h, w); inside section a the channel pair
+ *   (o_a + 2j, o_a + 2j + 1) is rotated counter-clockwise by
+ *   pos[i,a] * theta^(-2j / axis_dims[a]).
+ *   q, k    [S, H, Dh] bf16 (row stride H*Dh), in/out
+ *   q_gain, k_gain [Dh] float32
+ *   pos     [S, 3] int32
+ *   axis_dims  HOST array of 3 even non-negative ints summing to Dh
+ * Dh == 128. FP32 arithmetic; the angle is formed and reduced in FP64.
+ */
+h3_status h3_qk_norm_rope(void* q, void* k, const float* q_gain, const float* k_gain,
+                          const int32_t* pos, const int* axis_dims, int S, int L, int H,
+                          int Dh, float theta, float eps, h3_stream_t stream);
+
+/*
+ * a3 — dense bidirectional attention over the valid length (blog section 3.1:
+ * the backend takes the valid sequence length; no work on tail padding):
+ *   o[i,h,:] = sum_{j<L} softmax_j(q[i,h,:] . k[j,h,:] * softmax_scale) v[j,h,:]
+ * for i < L. Keys/values of rows >= L are never read; rows >= L of o are not
+ * written.
+ *   q, k, v, o [S, H, Dh] bf16 with row stride H*Dh
+ * Dh == 128. bf16 tensor-core products, FP32 softmax and accumulation, bf16 out.
+ */
+h3_status h3_attention_varlen(const void* q, const void* k, const void* v, void* o, int S,
+                              int L, int H, int Dh, float softmax_scale, h3_stream_t stream);
+
+/*
+ * a5 — SwiGLU (blog section 3.2, #6283): out[i,j] = SiLU(g) * u with
+ * g = gate_up[i,j], u = gate_up[i,F+j], SiLU(g) = g / (1 + exp(-g)), for i < L.
+ *   gate_up [S, 2F] bf16, out [S, F] bf16. F % 8 == 0.
+ */
+h3_status h3_swiglu(const void* gate_up, void* out, int S, int L, int F, h3_stream_t stream);
+
+/*
+ * a4 — one block projection (the matrix multiplies the fused ops of blog
+ * section 3.2 sit around): y[i,:] = bf16( x[i,:] @ w^T ) for i < L, no bias.
+ *   x [S, K] bf16, w [N, K] bf16 (row n = output channel n), y [S, N] bf16.
+ * K % 64 == 0, N % 256 == 0. bf16 tensor-core products, FP32 accumulation.
+ */
+h3_status h3_linear(const void* x, const void* w, void* y, int S, int L, int N, int K,
+                    h3_stream_t stream);
+
+/*
+ * a4 + a5 fused — the FFN gate/up projection with SwiGLU in its epilogue
+ * (blog section 3.2: SwiGLU without separate SiLU and multiply launches):
+ *   out[i,j] = SiLU(bf16(x[i,:] . w_gu[j,:])) * bf16(x[i,:] . w_gu[F+j,:])   for i < L
+ *   x [S, K] bf16, w_gu [2F, K] bf16 (rows [gate | up]), out [S, F] bf16.
+ * F % 128 == 0, K % 64 == 0. The two products are rounded to bf16 before the
+ * SiLU, so the result equals h3_linear followed by h3_swiglu.
+ */
+h3_status h3_linear_swiglu(const void* x, const void* w_gu, void* out, int S, int L, int F,
+                           int K, h3_stream_t stream);
+
+/* Shape and constants of one block. */
+typedef struct h3_block_config {
+  int S;             /* buffer rows                                   */
+  int L;             /* valid rows, 0 <= L <= S                       */
+  int D;             /* hidden width, D == H * Dh                     */
+  int H;             /* heads                                         */
+  int Dh;            /* head dim (128)                                */
+  int F;             /* SwiGLU inner width                            */
+  int axis_dims[3];  /* RoPE sections (t, h, w), sum == Dh            */
+  float theta;       /* RoPE base                                     */
+  float eps_ln;      /* LayerNorm epsilon of the modulation steps     */
+  float eps_qk;      /* Q/K RMSNorm epsilon                           */
+} h3_block_config;
+
+/* Block weights (device pointers, caller-owned). */
+typedef struct h3_block_weights {
+  const void* w_qkv;    /* [3D, D] bf16, rows [q | k | v], each head-major */
+  const void* w_o;      /* [D, D]  bf16                                    */
+  const void* w_gu;     /* [2F, D] bf16, rows [gate | up]                  */
+  const void* w_down;   /* [D, F]  bf16                                    */
+  const float* q_gain;  /* [Dh] float32                                    */
+  const float* k_gain;  /* [Dh] float32                                    */
+} h3_block_weights;
+
+/* Bytes of device workspace h3_block_forward needs for this config
+ * (0 when the config is invalid; h3_last_error() says why). */
+size_t h3_block_workspace_bytes(const h3_block_config* cfg);
+
+/*
+ * a6 — one whole block (blog sections 3.1-3.2), in this order, rows < L:
+ *   (shift1, scale1, gate1, shift2, scale2, gate2) = mod[0..5, :]
+ *   h1 = bf16(LN(r) * (1 + scale1) + shift1)
+ *   [q | k | v] = h1 @ w_qkv^T ; q, k <- RoPE(RMSNorm(.))      (per head)
+ *   a  = attention(q, k, v) over keys < L, scale Dh^-1/2
+ *   r <- r + gate1 * (a @ w_o^T)
+ *   h2 = bf16(LN(r) * (1 + scale2) + shift2)
+ *   [g | u] = h2 @ w_gu^T ; s = SiLU(g) * u
+ *   r <- r + gate2 * (s @ w_down^T)
+ *   resid [S, D] float32 in/out (the residual stream r)
+ *   mod   [6, D] float32
+ *   pos   [S, 3] int32
+ *   workspace: device memory of at least h3_block_workspace_bytes(cfg) bytes,
+ *   256-byte aligned, owned by the caller, overwritten by the call.
+ */
+h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w, float* resid,
+                           const float* mod, const int32_t* pos, void* workspace,
+                           size_t workspace_bytes, h3_stream_t stream);
+
+/* Number of kernel stages h3_block_forward launches, in the order listed
+ * above: 0 modulation+LN, 1 QKV projection, 2 Q/K RMSNorm+RoPE, 3 attention,
+ * 4 output projection, 5 residual+modulation+LN, 6 gate/up projection with
+ * SwiGLU, 7 down projection, 8 residual. */
+#define H3_BLOCK_STAGES 9
+
+/*
+ * h3_block_forward, and records events[i] on `stream` just before stage i is
+ * launched and events[H3_BLOCK_STAGES] after the last stage, so the caller
+ * can time every stage on the launching stream. events: host array of
+ * H3_BLOCK_STAGES + 1 cudaEvent_t handles created by the caller (num_events
+ * must equal that count). The kernels launched are the same as those of
+ * h3_block_forward.
+ */
+h3_status h3_block_forward_events(const h3_block_config* cfg, const h3_block_weights* w,
+                                  float* resid, const float* mod, const int32_t* pos,
+                                  void* workspace, size_t workspace_bytes, h3_stream_t stream,
+                                  void* const* events, int num_events);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier no one arrives at, with a wait limit of timeout_ns. The wait runs
+ * out, the kernel records its code and returns; h3_check_device_error() then
+ * reports H3_ERR_TIMEOUT. Nothing else is touched. */
+h3_status h3_debug_wait_timeout(uint64_t timeout_ns, h3_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3BLOCK_H_ */

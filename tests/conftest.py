@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def h3lib():
+    """Builds (if stale) and loads libh3block.so; GPU tests use this."""
+    from dit_transformer_block_gb300 import build, h3
+    build.build()
+    h3.lib()
+    return h3

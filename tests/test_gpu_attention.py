@@ -1,0 +1,88 @@
+"""GPU parity of the tcgen05 valid-length attention against the oracle,
+called through the C-ABI, plus closed-form cases and pad invariance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.h3_oracle as O
+from dit_transformer_block_gb300 import inputs as I
+from helpers import assert_close_bf16, np64, sample_rows
+
+pytestmark = pytest.mark.gpu
+SENT = -7.25
+dev = "cuda"
+
+
+def run(h3lib, q, k, v, L):
+    S = q.shape[0]
+    o = torch.full_like(q, SENT)
+    h3lib.attention_varlen(q, k, v, o, L)
+    h3lib.check_device_error()
+    assert bool((o[L:] == SENT).all()), "pad rows written"
+    return o
+
+
+@pytest.mark.parametrize("S,L,H", [(256, 250, 4), (128, 1, 2), (128, 127, 2), (128, 128, 2),
+                                   (256, 129, 2), (640, 600, 3)])
+def test_attention_small(h3lib, S, L, H):
+    inp = I.attention_inputs(S, L, H, 128, seed=S + L, device=dev)
+    o = run(h3lib, inp["q"], inp["k"], inp["v"], L)
+    ref = O.attention(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), L, 128 ** -0.5)
+    assert_close_bf16(np64(o[:L]), ref, "attention")
+
+
+def test_attention_large_logits(h3lib):
+    # un-normalised q, k (logit spread ~ 10): exercises the running-max rescale
+    S, L, H = 512, 500, 2
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
+    q = (torch.randn(S, H, 128, generator=g, device=dev) * 3).to(torch.bfloat16)
+    k = (torch.randn(S, H, 128, generator=g, device=dev) * 3).to(torch.bfloat16)
+    v = torch.randn(S, H, 128, generator=g, device=dev).to(torch.bfloat16)
+    o = run(h3lib, q, k, v, L)
+    ref = O.attention(np64(q), np64(k), np64(v), L, 128 ** -0.5)
+    assert_close_bf16(np64(o[:L]), ref, "attention large logits")
+
+
+def test_attention_identical_keys_give_mean_of_v(h3lib):
+    S, L, H = 384, 300, 2
+    inp = I.attention_inputs(S, L, H, 128, seed=5, device=dev)
+    k = inp["k"][:1].expand(S, H, 128).contiguous()
+    o = run(h3lib, inp["q"], k, inp["v"], L)
+    mean = np64(inp["v"][:L]).mean(0)
+    assert_close_bf16(np64(o[:L]), np.broadcast_to(mean, (L, H, 128)), "mean of V")
+
+
+def test_attention_pad_rows_do_not_matter(h3lib):
+    S, L, H = 384, 333, 2
+    inp = I.attention_inputs(S, L, H, 128, seed=6, device=dev)
+    o1 = run(h3lib, inp["q"], inp["k"], inp["v"], L)
+    k2, v2, q2 = inp["k"].clone(), inp["v"].clone(), inp["q"].clone()
+    k2[L:] = 30.0
+    v2[L:] = -1000.0
+    q2[L:] = float("nan")
+    o2 = run(h3lib, q2, k2, v2, L)
+    assert torch.equal(o1[:L], o2[:L])
+    # growing the buffer leaves the valid rows unchanged too
+    S3 = S + 128
+    pad = lambda t: torch.cat([t, torch.randn(128, H, 128, device=dev).to(t.dtype)])
+    o3 = run(h3lib, pad(inp["q"]), pad(inp["k"]), pad(inp["v"]), L)
+    assert torch.equal(o1[:L], o3[:L])
+
+
+def test_attention_deterministic(h3lib):
+    inp = I.attention_inputs(1024, 1000, 2, 128, seed=7, device=dev)
+    o1 = run(h3lib, inp["q"], inp["k"], inp["v"], 1000)
+    o2 = run(h3lib, inp["q"], inp["k"], inp["v"], 1000)
+    assert torch.equal(o1, o2)
+
+
+@pytest.mark.slow
+def test_attention_full_size_sampled(h3lib):
+    S, L, H = 58816, 58758, 42
+    inp = I.attention_inputs(S, L, H, 128, seed=2, device=dev)
+    o = run(h3lib, inp["q"], inp["k"], inp["v"], L)
+    rows = sample_rows(L, 512, 2)
+    ref = O.attention(np64(inp["q"][:L]), np64(inp["k"][:L]), np64(inp["v"][:L]), L, 128 ** -0.5,
+                      rows=rows)
+    assert_close_bf16(np64(o[torch.from_numpy(rows).to(dev)]), ref, "attention full")
