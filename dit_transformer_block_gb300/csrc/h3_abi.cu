@@ -456,4 +456,45 @@ h3_status h3_block_forward_events(const h3_block_config* cfg, const h3_block_wei
                             num_events);
 }
 
+// Scratch of h3_block_forward_noalloc: a fixed array in the library's device
+// data, so that entry point never allocates. Host code only sees a stand-in
+// for this symbol; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[H3_NOALLOC_SCRATCH_BYTES];
+static void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.
+static h3_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev >= kMaxDevices) return fail(H3_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return H3_OK;
+}
+
+h3_status h3_block_forward_noalloc(const h3_block_config* cfg, const h3_block_weights* w,
+                                   float* resid, const float* mod, const int32_t* pos,
+                                   h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_block_config(cfg);
+  if (st != H3_OK) return st;
+  const size_t need = block_ws(cfg).total;
+  H3_REQUIRE(need <= H3_NOALLOC_SCRATCH_BYTES, H3_ERR_WORKSPACE,
+             "this block needs %zu bytes of scratch; the no-alloc entry point has %u bytes "
+             "(use h3_block_forward with a workspace)",
+             need, static_cast<unsigned>(H3_NOALLOC_SCRATCH_BYTES));
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != H3_OK) return st;
+  return block_forward_impl(cfg, w, resid, mod, pos, scratch, H3_NOALLOC_SCRATCH_BYTES, stream,
+                            nullptr, 0);
+}
+
 }  // extern "C"

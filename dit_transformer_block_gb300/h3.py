@@ -60,6 +60,8 @@ _SIGS = {
                               _P, _P, _SZ, _P]),
     "h3_block_forward_events": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights),
                                      _P, _P, _P, _P, _SZ, _P, ctypes.POINTER(_P), _I]),
+    "h3_block_forward_noalloc": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights),
+                                      _P, _P, _P, _P]),
     "h3_debug_wait_timeout": (_I, [_U64, _P]),
 }
 
@@ -200,6 +202,18 @@ def linear_swiglu(x, w_gu, out, L=None, stream=None):
 
 def block_config(S, L, D, H, Dh, F, axis_dims, theta=1e4, eps_ln=1e-6, eps_qk=1e-6) -> BlockConfig:
     return BlockConfig(S, L, D, H, Dh, F, (ctypes.c_int * 3)(*axis_dims), theta, eps_ln, eps_qk)
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def block_forward_noalloc(cfg: BlockConfig, weights, resid, mod, pos, stream=None):
+    """h3_block_forward_noalloc: the block forward with the library's own
+    fixed scratch array instead of a caller workspace, for callers that cannot
+    allocate device memory (blocks up to NOALLOC_SCRATCH_BYTES of workspace)."""
+    w = weights if isinstance(weights, BlockWeights) else block_weights(weights)
+    _check("block_forward_noalloc", lib().h3_block_forward_noalloc(
+        ctypes.byref(cfg), ctypes.byref(w), _p(resid), _p(mod), _p(pos), _s(stream)))
 
 
 def block_workspace_bytes(cfg: BlockConfig) -> int:

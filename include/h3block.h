@@ -216,6 +216,41 @@ h3_status h3_block_forward_events(const h3_block_config* cfg, const h3_block_wei
                                   void* workspace, size_t workspace_bytes, h3_stream_t stream,
                                   void* const* events, int num_events);
 
+/* Bytes of the fixed device scratch array h3_block_forward_noalloc uses. */
+#define H3_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * h3_block_forward for callers that cannot allocate device memory. The source
+ * pages have no counterpart: this entry point exists for callers, not for the
+ * method.
+ *
+ * Some callers cannot give the library a workspace: a host program or
+ * plug-in whose device memory all belongs to a framework's pool and which may
+ * not call cudaMalloc itself, or code that runs where an allocation is not
+ * allowed. This variant takes its scratch from one array of
+ * H3_NOALLOC_SCRATCH_BYTES (32 MiB) in the library's own device memory
+ * instead; that array is reserved on every GPU that loads the library and
+ * stays reserved until the process exits.
+ *  - It allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *    routine is called.
+ *  - A block whose h3_block_workspace_bytes(cfg) exceeds
+ *    H3_NOALLOC_SCRATCH_BYTES is rejected with H3_ERR_WORKSPACE before
+ *    anything is launched (the full 58,816-row block needs 5.5 GB; this entry
+ *    point serves short sequences such as 256 rows of a 512-wide block).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current. Make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last
+ *    call's contents. The block writes every scratch element before it reads
+ *    it, so nothing has to start at zero. Calls whose work overlaps on the
+ *    GPU (different streams, or different host threads) race on the array:
+ *    order them on one stream.
+ * Arguments, results and errors are otherwise those of h3_block_forward.
+ */
+h3_status h3_block_forward_noalloc(const h3_block_config* cfg, const h3_block_weights* w,
+                                   float* resid, const float* mod, const int32_t* pos,
+                                   h3_stream_t stream);
+
 /* Test hook for the bounded-wait machinery: launches one CTA that waits on an
  * mbarrier no one arrives at, with a wait limit of timeout_ns. The wait runs
  * out, the kernel records its code and returns; h3_check_device_error() then
