@@ -43,7 +43,7 @@ def args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -136,7 +136,10 @@ def gpu_uuid(torch, dev):
 
 
 # ----------------------------------------------------------- CPU baseline leg
-def oracle_sample(shape, n_kv=512, n_q=8, seed=3):
+_KV_CACHE = {}
+
+
+def oracle_sample(shape, n_kv=8192, n_q=96, seed=3):
     """Times the oracle on a bounded sample of one block and extrapolates.
 
     Sample: the key/value stage (LayerNorm + K and V projections + K
@@ -144,6 +147,8 @@ def oracle_sample(shape, n_kv=512, n_q=8, seed=3):
     projection, Q RMSNorm/RoPE, attention over all L keys, output projection,
     residual + LayerNorm, gate/up projection, SwiGLU, down projection,
     residual) for n_q rows. One block = L x (t_kv / n_kv + t_q / n_q).
+    The full-length keys/values the query rows attend to are drawn once per
+    process (untimed); their cost is what the timed K/V stage measures.
     """
     import numpy as np
     import torch
@@ -163,16 +168,20 @@ def oracle_sample(shape, n_kv=512, n_q=8, seed=3):
     pos = I.positions_3d(shape.S, L).numpy()
     x_kv = bf(n_kv, D)
     x_q = bf(n_q, D)
-    # keys/values of the full sequence for the query rows to attend to
-    # (drawn, not computed: their cost is the K/V stage timed above)
-    k_all = bf(L, H, Dh)
-    v_all = bf(L, H, Dh)
+    key = (L, H, Dh)
+    if key not in _KV_CACHE:
+        gk = torch.Generator().manual_seed(12345)
+        kv = lambda: torch.randn(L, H, Dh, generator=gk).to(torch.bfloat16).double().numpy()
+        _KV_CACHE[key] = (kv(), kv())
+    k_all, v_all = _KV_CACHE[key]
 
     t0 = time.perf_counter()
-    _, h = O.mod_norm_residual(x_kv, shift=mod[0], scale=mod[1])
-    k = O.linear(h, w_qkv[D:2 * D]).reshape(n_kv, H, Dh)
-    O.qk_norm_rope(k, gain, pos[:n_kv], shape.axis_dims, shape.theta, shape.eps_qk)
-    O.linear(h, w_qkv[2 * D:])
+    for c0 in range(0, n_kv, 2048):
+        c1 = min(n_kv, c0 + 2048)
+        _, h = O.mod_norm_residual(x_kv[c0:c1], shift=mod[0], scale=mod[1])
+        k = O.linear(h, w_qkv[D:2 * D]).reshape(c1 - c0, H, Dh)
+        O.qk_norm_rope(k, gain, pos[c0:c1], shape.axis_dims, shape.theta, shape.eps_qk)
+        O.linear(h, w_qkv[2 * D:])
     t_kv = time.perf_counter() - t0
 
     t0 = time.perf_counter()
@@ -191,8 +200,8 @@ def oracle_sample(shape, n_kv=512, n_q=8, seed=3):
     O.mod_norm_residual(r, f, mod[5])
     t_q = time.perf_counter() - t0
     ms = L * (t_kv / n_kv + t_q / n_q) * 1e3
-    desc = (f"oracle (NumPy FP64) on {n_kv} key/value rows + {n_q} full query rows of the "
-            f"L={L} block, extrapolated linearly to all rows")
+    desc = (f"oracle (NumPy FP64) on the key/value stage of {n_kv} rows and the full query path "
+            f"of {n_q} rows of the L={L} block, extrapolated linearly to all rows")
     return ms, desc, t_kv + t_q
 
 
@@ -214,7 +223,7 @@ def run_reference(a):
     times = []
     desc = ""
     for i in range(a.warmup + a.steps):
-        ms, desc, _ = oracle_sample(shape, n_kv=256, n_q=4, seed=100 + i)
+        ms, desc, _ = oracle_sample(shape, n_kv=2048, n_q=24, seed=100 + i)
         if i >= a.warmup:
             times.append(ms)
     value = statistics.mean(times)
@@ -318,30 +327,42 @@ def run_ours(a):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         step_ms, stage_ms = t[0].item(), t[1:].tolist()
 
-    # ---- end to end through the C-ABI with host buffers
+    # ---- end to end through the C-ABI with host buffers: every step copies
+    # its residual, modulation and positions host -> device from pinned
+    # memory and the updated residual back. Two device buffer sets and a copy
+    # stream let step k+1's upload and step k's download overlap step k's
+    # compute; the timed region spans the first upload to the last download.
     pin = lambda t: t.detach().to("cpu").pin_memory()
-    h_resid, h_mod, h_pos = pin(inp["resid"]), pin(inp["mod"]), pin(inp["pos"])
-    h_out = torch.empty_like(h_resid).pin_memory()
-    d_resid = torch.empty_like(inp["resid"])
-    d_mod = torch.empty_like(inp["mod"])
-    d_pos = torch.empty_like(inp["pos"])
-    h2d = h_resid.numel() * 4 + h_mod.numel() * 4 + h_pos.numel() * 4
-    d2h = h_out.numel() * 4
+    h_in = [(pin(inp["resid"]), pin(inp["mod"]), pin(inp["pos"])) for _ in range(2)]
+    h_out = [torch.empty_like(h_in[0][0]).pin_memory() for _ in range(2)]
+    d_buf = [(torch.empty_like(inp["resid"]), torch.empty_like(inp["mod"]),
+              torch.empty_like(inp["pos"])) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in[0])
+    d2h = h_out[0].numel() * 4
+    copy = torch.cuda.Stream()
 
-    def e2e_step():
-        d_resid.copy_(h_resid, non_blocking=True)
-        d_mod.copy_(h_mod, non_blocking=True)
-        d_pos.copy_(h_pos, non_blocking=True)
-        h3.block_forward(cfg, weights, d_resid, d_mod, d_pos, ws)
-        h_out.copy_(d_resid, non_blocking=True)
+    def e2e_run(n):
+        up = [torch.cuda.Event() for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
+        for k in range(n):
+            b = k % 2
+            with torch.cuda.stream(copy):
+                for d, h in zip(d_buf[b], h_in[b]):
+                    d.copy_(h, non_blocking=True)
+                up[k].record(copy)
+            stream.wait_event(up[k])
+            h3.block_forward(cfg, weights, d_buf[b][0], d_buf[b][1], d_buf[b][2], ws,
+                             stream=stream)
+            done[k].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done[k])
+                h_out[b].copy_(d_buf[b][0], non_blocking=True)
+        torch.cuda.synchronize()
 
-    e2e_step()
-    torch.cuda.synchronize()
+    e2e_run(2)
     barrier()
     t0 = time.perf_counter()
-    for _ in range(a.e2e_steps):
-        e2e_step()
-    torch.cuda.synchronize()
+    e2e_run(a.e2e_steps)
     e2e_ms = (time.perf_counter() - t0) * 1e3 / a.e2e_steps
     barrier()
     if world > 1:
@@ -393,6 +414,7 @@ def run_ours(a):
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": h3.BLOCK_STAGES * a.steps,
+        "e2e_note": "double-buffered: uploads/downloads on a copy stream overlap compute",
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)

@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "h3_internal.cuh"
 
@@ -49,10 +50,112 @@ struct AttnArgs {
   DevErr err;
 };
 
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+// One KV tile of the online softmax for the calling thread's query row (TMEM
+// lane). S_j is read from tS; P_j (bf16 pairs) is written over its first 64
+// columns. valid = keys of this tile that are < L (>= BKV: none masked).
+// o_live: O already holds earlier tiles (so raising the max rescales it).
+// m, l: running max (times scale_log2) and row sum. Warp-collective.
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int valid, bool o_live,
+                                             float scale_log2, float& m, float& l) {
+  uint32_t sr[128];
+  {
+    uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+    uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+    uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+    uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+    tmem_ld32(tS + 0, c0);
+    tmem_ld32(tS + 32, c1);
+    tmem_ld32(tS + 64, c2);
+    tmem_ld32(tS + 96, c3);
+    tmem_ld_wait();
+    tmem_reg_fence(sr);
+  }
+  // Only the last tile holds keys >= L; mask them to -inf.
+  if (valid < BKV) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c >= valid) sr[c] = 0xff800000u;
+  }
+  // Row max of the raw products (the scale is positive, so it commutes with
+  // max), four independent 3-input max chains.
+  float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 128; c += 8) {
+    ma = max3f(ma, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+    mb = max3f(mb, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+    mc = max3f(mc, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+    md = max3f(md, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+  }
+  const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
+  // Raise the running max only when it is exceeded by more than the
+  // threshold; the decision is warp-uniform because the O rescale uses
+  // warp-collective TMEM loads and stores.
+  const bool need = mx > m + RESCALE_THRESHOLD;
+  if (__any_sync(0xffffffffu, need)) {
+    const float m_new = fmaxf(m, mx);
+    const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
+    l *= alpha;
+    if (o_live) {
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {  // 16 columns at a time: the S row is live
+        uint32_t ov[16];
+        tmem_ld16(tO + c * 16, ov);
+        tmem_ld_wait();
+        tmem_reg_fence(ov);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+        tmem_st16(tO + c * 16, ov);
+      }
+    }
+    m = m_new;
+  }
+  // p = exp2(s * scale_log2 - m): one packed FMA per pair, two exp2, one
+  // packed add into the row sum, one bf16x2 pack written over S.
+  const float neg_m = -m;
+  float la = 0.f, lb = 0.f, lc = 0.f, ld = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float x0, x1;
+      ffma2_bc(x0, x1, __uint_as_float(sr[c * 32 + 2 * i]), __uint_as_float(sr[c * 32 + 2 * i + 1]),
+               scale_log2, neg_m);
+      const float p0 = ex2_approx(x0);
+      const float p1 = ex2_approx(x1);
+      if (i & 1)
+        fadd2(lc, ld, p0, p1);
+      else
+        fadd2(la, lb, p0, p1);
+      pk[i] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(tS + c * 16, pk);
+  }
+  l += (la + lb) + (lc + ld);
+  tmem_st_wait();
+}
+
+// Normalises the thread's O row by 1/l and stores it (bf16) when row_ok.
+__device__ __forceinline__ void store_o_row(uint32_t tO, float l, __nv_bfloat16* orow,
+                                            bool row_ok) {
+  const float inv_l = 1.0f / l;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t ov[32];
+    tmem_ld32(tO + c * 32, ov);
+    tmem_ld_wait();
+    tmem_reg_fence(ov);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+    if (row_ok) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+  }
 }
 
 enum Bar { Q_FULL = 0, K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL, P_FULL, O_DONE, NUM_BARS };
@@ -122,8 +225,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         for (int j = 0; j < a.num_kv; ++j) {
           const uint32_t par = static_cast<uint32_t>(j) & 1u;
           if (!mbar_wait(bar(K_FULL), par, a.err, ERR_WAIT_ATTN_MMA)) break;
-          // S/P is free once the previous P V product has completed.
-          if (j > 0 && !mbar_wait(bar(O_DONE), par ^ 1u, a.err, ERR_WAIT_ATTN_MMA)) break;
+          // S_j overwrites P_{j-1}, which the previous P V product reads. MMAs
+          // issued by one thread execute in issue order, so QK_j is queued
+          // right behind PV_{j-1} without waiting for it; S_FULL's commit
+          // still covers PV_{j-1}, so the softmax sees O complete.
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
@@ -163,64 +268,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         break;
       }
       tc_fence_after();
-      uint32_t sr[128];
-      {
-        uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-        uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-        uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
-        uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
-        tmem_ld32(tS + 0, c0);
-        tmem_ld32(tS + 32, c1);
-        tmem_ld32(tS + 64, c2);
-        tmem_ld32(tS + 96, c3);
-        tmem_ld_wait();
-        tmem_reg_fence(sr);
-      }
-      float s[128];
-      const int valid = a.L - j * BKV;  // keys of this tile that are < L
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = __uint_as_float(sr[c]) * a.scale_log2;
-        if (c >= valid) s[c] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      // Raise the running max only when it is exceeded by more than the
-      // threshold; the decision is warp-uniform because the O rescale uses
-      // warp-collective TMEM loads and stores.
-      const bool need = mx > m + RESCALE_THRESHOLD;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = fmaxf(m, mx);
-        const float alpha = fast_exp2(m - m_new);  // 0 on the first tile
-        l *= alpha;
-        if (j > 0) {
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c * 32, ov);
-            tmem_ld_wait();
-            tmem_reg_fence(ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(tO + c * 32, ov);
-          }
-        }
-        m = m_new;
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(s[c * 32 + 2 * i] - m);
-          const float p1 = fast_exp2(s[c * 32 + 2 * i + 1] - m);
-          l += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + c * 16, pk);
-      }
-      tmem_st_wait();
+      softmax_tile(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l);
       tc_fence_before();
       mbar_arrive(bar(P_FULL));
     }
@@ -228,27 +276,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (ok && mbar_wait(bar(O_DONE), static_cast<uint32_t>(a.num_kv - 1) & 1u, a.err,
                         ERR_WAIT_ATTN_SOFTMAX)) {
       tc_fence_after();
-      const float inv_l = 1.0f / l;
       const int row = q0 + row_in_tile;
-      __nv_bfloat16* orow = a.o + static_cast<int64_t>(row) * a.ld_out + col0;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tO + c * 32, ov);
-        tmem_ld_wait();
-        tmem_reg_fence(ov);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
-                              __uint_as_float(ov[2 * i + 1]) * inv_l);
-        if (row < a.L) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
-      }
+      store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L);
     }
   }
 
@@ -260,17 +289,198 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Two query tiles per CTA (256 rows of one head) sharing every K/V tile.
+//   * warps 0-3 / 4-7: softmax of query tile 0 / 1 (thread = row = TMEM lane);
+//   * warp 8: TMA producer (Q0, Q1 once; K_j and V_j through a 4-slot ring);
+//   * warp 9: TMEM allocator (512 columns: S0, S1, O0, O1) and MMA issuer in
+//     the order PV0(j), QK0(j+1), PV1(j), QK1(j+1), so each tile's softmax has
+//     the other tile's two MMAs (1024 tensor clocks) to finish in;
+//   * P_i is written over S_i; QK_i(j+1) is issued right behind PV_i(j) (MMAs
+//     of one thread execute in issue order).
+// Each K/V tile is read from shared memory by two Q tiles, which halves the
+// shared-memory traffic per FLOP of the one-tile design.
+constexpr int Q2_THREADS = 320;
+constexpr int KV_SLOTS = 4;
+constexpr size_t Q2_SMEM_BYTES = 1024 + (2 + KV_SLOTS) * TILE_BYTES + 256;
+
+enum Bar2 {
+  B2_Q = 0,
+  B2_KV_FULL = 1,
+  B2_KV_EMPTY = B2_KV_FULL + KV_SLOTS,
+  B2_S = B2_KV_EMPTY + KV_SLOTS,
+  B2_P = B2_S + 2,
+  B2_O = B2_P + 2,
+  B2_NUM = B2_O + 2
+};
+
+__global__ void __launch_bounds__(Q2_THREADS, 1)
+    attention_2q_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sKV = smem;                              // KV_SLOTS x 32 KB
+  uint8_t* sQ = smem + KV_SLOTS * TILE_BYTES;       // 2 x 32 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * TILE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B2_NUM);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q0 = blockIdx.x * 2 * BQ;
+  const int col0 = blockIdx.y * DH;
+  const int n = a.num_kv;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B2_NUM; ++i) mbar_init(bar(i), (i == B2_P || i == B2_P + 1) ? 128 : 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(bar(B2_Q), 2 * TILE_BYTES);
+      for (int i = 0; i < 2; ++i) {
+        tma_load_2d(smem_u32(sQ + i * TILE_BYTES), &tmQ, bar(B2_Q), col0, q0 + i * BQ);
+        tma_load_2d(smem_u32(sQ + i * TILE_BYTES + BOX_BYTES), &tmQ, bar(B2_Q), col0 + 64,
+                    q0 + i * BQ);
+      }
+      for (int t = 0; t < 2 * n; ++t) {  // even t: K_{t/2}, odd t: V_{t/2}
+        const int slot = t % KV_SLOTS;
+        const uint32_t use = static_cast<uint32_t>(t / KV_SLOTS);
+        if (!mbar_wait(bar(B2_KV_EMPTY + slot), (use & 1u) ^ 1u, a.err, ERR_WAIT_ATTN_PRODUCER))
+          break;
+        const uint32_t full = bar(B2_KV_FULL + slot);
+        mbar_arrive_expect_tx(full, TILE_BYTES);
+        const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
+        uint8_t* dst = sKV + slot * TILE_BYTES;
+        tma_load_2d(smem_u32(dst), m, full, col0, (t >> 1) * BKV);
+        tma_load_2d(smem_u32(dst + BOX_BYTES), m, full, col0 + 64, (t >> 1) * BKV);
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(BQ, BKV, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BQ, DH, true);
+      const uint32_t kv_addr = smem_u32(sKV), q_addr = smem_u32(sQ);
+      auto slot_of = [](int t) { return t % KV_SLOTS; };
+      auto wait_full = [&](int t) {
+        return mbar_wait(bar(B2_KV_FULL + slot_of(t)),
+                         static_cast<uint32_t>(t / KV_SLOTS) & 1u, a.err, ERR_WAIT_ATTN_MMA);
+      };
+      auto qk = [&](int i, int j) {  // S_i = Q_i K_j^T
+        const uint32_t k_addr = kv_addr + slot_of(2 * j) * TILE_BYTES;
+        const uint32_t qa = q_addr + i * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + i * 128, sdesc_sw128(qa + off, 16, 1024),
+                 sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B2_S + i));
+      };
+      auto pv = [&](int i, int j) {  // O_i += P_i V_j
+        const uint32_t v_addr = kv_addr + slot_of(2 * j + 1) * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
+                 sdesc_sw128(v_addr + kk * 2048, BOX_BYTES, 1024), idesc_pv,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B2_O + i));
+      };
+      bool ok = mbar_wait(bar(B2_Q), 0, a.err, ERR_WAIT_ATTN_MMA) && wait_full(0);
+      if (ok) {
+        tc_fence_after();
+        qk(0, 0);
+        qk(1, 0);
+        mma_commit(bar(B2_KV_EMPTY + slot_of(0)));
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const uint32_t par = static_cast<uint32_t>(j) & 1u;
+        if (!wait_full(2 * j + 1) || !mbar_wait(bar(B2_P), par, a.err, ERR_WAIT_ATTN_MMA)) break;
+        tc_fence_after();
+        pv(0, j);
+        const bool more = j + 1 < n;
+        if (more) {
+          if (!wait_full(2 * j + 2)) break;
+          tc_fence_after();
+          qk(0, j + 1);
+        }
+        if (!mbar_wait(bar(B2_P + 1), par, a.err, ERR_WAIT_ATTN_MMA)) break;
+        tc_fence_after();
+        pv(1, j);
+        mma_commit(bar(B2_KV_EMPTY + slot_of(2 * j + 1)));
+        if (more) {
+          qk(1, j + 1);
+          mma_commit(bar(B2_KV_EMPTY + slot_of(2 * j + 2)));
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax
+    const int tile = warp >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + tile * 128;
+    const uint32_t tO = tmem + lane_base + 256 + tile * 128;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait(bar(B2_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
+                     ERR_WAIT_ATTN_SOFTMAX)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      softmax_tile(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l);
+      tc_fence_before();
+      mbar_arrive(bar(B2_P + tile));
+    }
+    if (ok && mbar_wait(bar(B2_O + tile), static_cast<uint32_t>(n - 1) & 1u, a.err,
+                        ERR_WAIT_ATTN_SOFTMAX)) {
+      tc_fence_after();
+      const int row = q0 + tile * BQ + quarter * 32 + lane;
+      store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
                            void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s) {
   static bool attr_done[64] = {};
+  static const bool one_tile = getenv("H3_ATTENTION_TWO_TILE") == nullptr;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attention_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attention_2q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Q2_SMEM_BYTES));
     if (e != cudaSuccess) return cuda_fail(e, "attention: set shared memory size");
     attr_done[dev] = true;
   }
@@ -288,8 +498,13 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   if ((st = make_tmap_bf16_2d(&tq, q, width, L, stride, 64, BQ)) != H3_OK) return st;
   if ((st = make_tmap_bf16_2d(&tk, k, width, L, stride, 64, BKV)) != H3_OK) return st;
   if ((st = make_tmap_bf16_2d(&tv, v, width, L, stride, 64, BKV)) != H3_OK) return st;
-  dim3 grid((L + BQ - 1) / BQ, H);
-  attention_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a);
+  if (one_tile) {
+    dim3 grid((L + BQ - 1) / BQ, H);
+    attention_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a);
+  } else {
+    dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
+    attention_2q_kernel<<<grid, Q2_THREADS, Q2_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  }
   return cuda_fail(cudaGetLastError(), "attention launch");
 }
 

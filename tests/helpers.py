@@ -40,3 +40,31 @@ def sample_rows(L: int, n: int, seed: int) -> np.ndarray:
     rows = g.choice(L, size=min(n, L), replace=False)
     rows[0], rows[-1] = 0, L - 1
     return np.unique(rows)
+
+
+def bf16_ulp(x) -> np.ndarray:
+    """Spacing of bf16 values at |x| (2^(e - 7) for |x| in [2^e, 2^(e+1)))."""
+    x = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+def assert_close_block(x, ref, f_ref, o_ref, gate1, gate2, r_in, what="block"):
+    """Whole-block FP32 output: the last two steps add gate * y for bf16
+    hand-offs y = o, f, where a one-ulp rounding disagreement between two
+    correct evaluations is expected; the elementwise bound is therefore
+    2e-2 * max(1, |ref|) + |gate2| * ulp(f) + |gate1| * ulp(o), and the
+    relative-L2 bound 1e-2 is unchanged. The same bounds apply to the
+    residual increment out - r_in (gate1 * o + gate2 * f), which is small
+    next to the residual and would hide a wrong gate."""
+    x = np.asarray(x, np.float64).reshape(np.shape(ref))
+    ref = np.asarray(ref, np.float64)
+    r_in = np.asarray(r_in, np.float64).reshape(np.shape(ref))
+    assert np.all(np.isfinite(x)), f"{what}: non-finite output"
+    slack = np.abs(gate2)[None, :] * bf16_ulp(f_ref) + np.abs(gate1)[None, :] * bf16_ulp(o_ref)
+    for name, a, b in (("output", x, ref), ("increment", x - r_in, ref - r_in)):
+        bound = BF16_ELEM * np.maximum(1.0, np.abs(b)) + slack
+        ratio = np.max(np.abs(a - b) / bound)
+        r = rel_l2(a, b)
+        assert ratio <= 1.0 and r <= BF16_REL_L2, \
+            f"{what} {name}: max err/bound {ratio:.3g}, rel-L2 {r:.3g}"

@@ -7,7 +7,7 @@ import torch
 
 import oracle.h3_oracle as O
 from dit_transformer_block_gb300 import inputs as I
-from helpers import assert_close_bf16, np64, sample_rows
+from helpers import assert_close_block, np64, sample_rows
 
 pytestmark = pytest.mark.gpu
 dev = "cuda"
@@ -23,12 +23,17 @@ def gpu_block(h3lib, shape, inp):
     return resid
 
 
-def oracle_block(shape, inp, rows=None):
+def check_block(out_rows, shape, inp, rows=None, what="block"):
+    """Compares GPU output rows with the oracle's, with the block tolerance."""
     n = {k: np64(v) if v.is_floating_point() else v.cpu().numpy() for k, v in inp.items()}
-    return O.block_forward(n["resid"], n["mod"], n["w_qkv"], n["w_o"], n["w_gu"], n["w_down"],
-                           n["q_gain"], n["k_gain"], n["pos"], L=shape.L, heads=shape.H,
-                           head_dim=shape.Dh, axis_dims=shape.axis_dims, theta=shape.theta,
-                           eps_ln=shape.eps_ln, eps_qk=shape.eps_qk, rows=rows)
+    ref, mids = O.block_forward(n["resid"], n["mod"], n["w_qkv"], n["w_o"], n["w_gu"],
+                                n["w_down"], n["q_gain"], n["k_gain"], n["pos"], L=shape.L,
+                                heads=shape.H, head_dim=shape.Dh, axis_dims=shape.axis_dims,
+                                theta=shape.theta, eps_ln=shape.eps_ln, eps_qk=shape.eps_qk,
+                                rows=rows, return_intermediates=True)
+    r_in = n["resid"][:shape.L] if rows is None else n["resid"][rows]
+    assert_close_block(np64(out_rows), ref, mids["f"], mids["o"], n["mod"][2], n["mod"][5], r_in,
+                       what)
 
 
 SMALL = [I.TINY,
@@ -41,8 +46,7 @@ SMALL = [I.TINY,
 def test_block_small(h3lib, shape):
     inp = {k: v.to(dev) for k, v in I.block_inputs(shape, seed=0).items()}
     out = gpu_block(h3lib, shape, inp)
-    ref = oracle_block(shape, inp)
-    assert_close_bf16(np64(out[:shape.L]), ref, "block")
+    check_block(out[:shape.L], shape, inp)
     assert torch.equal(out[shape.L:], inp["resid"][shape.L:]), "pad rows written"
 
 
@@ -68,6 +72,28 @@ def test_block_full_size_sampled(h3lib):
     inp = I.block_inputs(shape, seed=3, device=dev)
     out = gpu_block(h3lib, shape, inp)
     rows = sample_rows(shape.L, 512, 3)
-    ref = oracle_block(shape, inp, rows=rows)
-    assert_close_bf16(np64(out[torch.from_numpy(rows).to(dev)]), ref, "block full")
+    check_block(out[torch.from_numpy(rows).to(dev)], shape, inp, rows, "block full")
     assert torch.equal(out[shape.L:], inp["resid"][shape.L:])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("L", [29034, 87846])
+def test_block_stack_length_sweep(h3lib, L):
+    """A stack of blocks with independent seeded weights at the short and long
+    packed lengths (buffers padded to a multiple of 64): each block is checked
+    on sampled rows against the oracle given the GPU's own input to that
+    block; the 29,034-row case runs four blocks, the 87,846-row case one."""
+    S = (L + 63) // 64 * 64
+    shape = I.BlockShape(S=S, L=L, D=5376, H=42, Dh=128, F=14336, axis_dims=(32, 48, 48),
+                         pos_kind="3d", grid=(47, 24, 79) if L > 60000 else (16, 24, 79))
+    blocks = 4 if L < 60000 else 1
+    x = None
+    for b in range(blocks):
+        inp = I.block_inputs(shape, seed=4 + b + (0 if L < 60000 else 10), device=dev)
+        if x is not None:
+            inp["resid"] = x
+        out = gpu_block(h3lib, shape, inp)
+        rows = sample_rows(L, 128, 40 + b)
+        check_block(out[torch.from_numpy(rows).to(dev)], shape, inp, rows, f"block {b} L={L}")
+        assert torch.equal(out[L:], inp["resid"][L:])
+        x = out

@@ -325,6 +325,10 @@ def check_block(o):
     for key in ("h1", "q", "k", "v", "a", "o", "h2", "gu", "u", "f"):
         assert close_bf16(mids[key], ref[key]), key
     assert close_bf16(out, ref["r"])
+    # the residual increment (gate1 * o + gate2 * f) is small next to the
+    # residual itself, so compare it on its own
+    r_in = n["resid"][:shape.L]
+    assert close_bf16(out - r_in, ref["r"] - r_in), "residual increment"
     # zero output projections leave the residual untouched
     z = run_block(o, shape, n, w_o=np.zeros_like(n["w_o"]), w_down=np.zeros_like(n["w_down"]))
     assert np.array_equal(z, n["resid"][:shape.L])
@@ -410,6 +414,21 @@ def _softmax_wrong_axis(z, axis=-1):
     return O.softmax(z, axis=0)
 
 
+def _unpack_shift_scale_swapped(mod):
+    sh1, sc1, g1, sh2, sc2, g2 = O.unpack_mod(mod)
+    return sc1, sh1, g1, sc2, sh2, g2
+
+
+def _unpack_gates_swapped(mod):
+    sh1, sc1, g1, sh2, sc2, g2 = O.unpack_mod(mod)
+    return sh1, sc1, g2, sh2, sc2, g1
+
+
+def _rms_no_eps_mean(x, gain, eps):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt((x * x).sum(-1, keepdims=True) + eps) * np.asarray(gain, np.float64)
+
+
 @pytest.mark.parametrize("name,mut,checks", [
     ("rope sign", dict(rope_apply=_rope_wrong_sign), ["check_rope"]),
     ("rope half-split pairing", dict(rope_apply=_rope_half_split), ["check_rope"]),
@@ -421,6 +440,9 @@ def _softmax_wrong_axis(z, axis=-1):
     ("softmax over queries", dict(softmax=_softmax_wrong_axis), ["check_attention"]),
     ("block with swapped rope", dict(rope_apply=_rope_wrong_sign), ["check_block"]),
     ("block with swapped swiglu", dict(swiglu=_swiglu_swapped), ["check_block"]),
+    ("modulation shift/scale order", dict(unpack_mod=_unpack_shift_scale_swapped), ["check_block"]),
+    ("modulation gates swapped", dict(unpack_mod=_unpack_gates_swapped), ["check_block"]),
+    ("rmsnorm sum instead of mean", dict(rms_norm=_rms_no_eps_mean), ["check_rms_norm"]),
 ])
 def test_planted_mistake_is_caught(name, mut, checks):
     m = _mutant(**mut)
