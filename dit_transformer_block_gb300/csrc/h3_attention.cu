@@ -6,26 +6,28 @@
 // takes part and no query row >= L is produced; section 3.3 / 4.3 name dense
 // BF16 attention as the reference behaviour.
 //
-// Design (per CTA: one head, one tile of 128 query rows; two CTAs per SM):
-//   * warps 0-3 run the softmax: thread t owns query row t, which is TMEM
-//     lane t of the S/P and O tiles;
-//   * warp 4 is the TMA producer: Q once, then K_j and V_j (128 keys each,
-//     single-buffered, zero-filled past L);
-//   * warp 5 allocates 256 TMEM columns and one lane issues the MMAs:
-//       S   = Q K_j^T   (SS form, both operands K-major, 8 x K=16)
-//       O  += P V_j     (TS form: P read from TMEM, V MN-major in smem)
-//   * P (bf16) overwrites the first 64 columns of S in place, so S/P take
-//     128 columns and O 128;
-//   * online softmax in base 2 with the scale folded in; the running max is
-//     raised only when a row's new max exceeds it by more than 8 (then O and
-//     the row sum are rescaled), so most tiles skip the O round trip;
-//   * only the last KV tile needs a key mask.
-// The chain QK_j -> softmax_j -> PV_j is serial inside a CTA; the second CTA
-// on the SM fills the tensor pipe while this one runs its softmax.
+// Design (per CTA: one head, two tiles of 128 query rows, one CTA per SM):
+//   * warps 0-3 and 4-7 run the softmax of query tile 0 and 1: thread t of
+//     a group owns query row t of its tile, which is TMEM lane t of that
+//     tile's S/P and O;
+//   * warp 8 is the TMA producer: Q0 and Q1 once, then K_j and V_j (128 keys
+//     each, zero-filled past L) through a ring of four 32 KB slots;
+//   * warp 9 allocates all 512 TMEM columns (S0, S1, O0, O1) and one lane
+//     issues the MMAs:
+//       S_i  = Q_i K_j^T   (SS form, both operands K-major, 8 x K=16)
+//       O_i += P_i V_j     (TS form: P read from TMEM, V MN-major in smem)
+//     in the order PV0(j), QK0(j+1), PV1(j), QK1(j+1), so each tile's
+//     softmax overlaps the other tile's two products;
+//   * P (bf16) overwrites the first 64 columns of S in place;
+//   * online softmax in base 2 with the scale folded in (packed FP32 FMA and
+//     add, 3-input max); the running max is raised only when a row's new max
+//     exceeds it by more than 8 (then O and the row sum are rescaled), so
+//     most tiles skip the O round trip; only the last KV tile is masked.
+// Both query tiles read every K/V tile from shared memory, which halves the
+// shared-memory operand traffic per FLOP of a one-tile-per-CTA design.
 #include <cuda_bf16.h>
 
 #include <algorithm>
-#include <cstdlib>
 
 #include "h3_internal.cuh"
 
@@ -33,13 +35,9 @@ namespace h3 {
 namespace {
 
 constexpr int BQ = 128, BKV = 128, DH = 128;
-constexpr int THREADS = 192;
 constexpr int TILE_BYTES = BQ * DH * 2;        // 32 KB (two 64-column boxes)
 constexpr int BOX_BYTES = TILE_BYTES / 2;      // 16 KB
-constexpr int TMEM_COLS = 256;
-constexpr uint32_t S_COL = 0, O_COL = 128;
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units (factor 256)
-constexpr size_t SMEM_BYTES = 1024 + 3 * TILE_BYTES + 256;
 
 struct AttnArgs {
   __nv_bfloat16* o;
@@ -158,137 +156,6 @@ __device__ __forceinline__ void store_o_row(uint32_t tO, float l, __nv_bfloat16*
   }
 }
 
-enum Bar { Q_FULL = 0, K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL, P_FULL, O_DONE, NUM_BARS };
-
-__global__ void __launch_bounds__(THREADS, 2)
-    attention_kernel(const __grid_constant__ CUtensorMap tmQ,
-                     const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sV = smem;
-  uint8_t* sK = smem + TILE_BYTES;
-  uint8_t* sQ = smem + 2 * TILE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 3 * TILE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * BQ;
-  const int head = blockIdx.y;
-  const int col0 = head * DH;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NUM_BARS; ++i) mbar_init(bar(i), i == P_FULL ? 128 : 1);
-    fence_mbar_init();
-  }
-  if (warp == 5) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 4) {
-    // ---------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(bar(Q_FULL), TILE_BYTES);
-      tma_load_2d(smem_u32(sQ), &tmQ, bar(Q_FULL), col0, q0);
-      tma_load_2d(smem_u32(sQ + BOX_BYTES), &tmQ, bar(Q_FULL), col0 + 64, q0);
-      for (int j = 0; j < a.num_kv; ++j) {
-        const uint32_t par = (static_cast<uint32_t>(j) & 1u) ^ 1u;
-        if (!mbar_wait(bar(K_EMPTY), par, a.err, ERR_WAIT_ATTN_PRODUCER)) break;
-        mbar_arrive_expect_tx(bar(K_FULL), TILE_BYTES);
-        tma_load_2d(smem_u32(sK), &tmK, bar(K_FULL), col0, j * BKV);
-        tma_load_2d(smem_u32(sK + BOX_BYTES), &tmK, bar(K_FULL), col0 + 64, j * BKV);
-        if (!mbar_wait(bar(V_EMPTY), par, a.err, ERR_WAIT_ATTN_PRODUCER)) break;
-        mbar_arrive_expect_tx(bar(V_FULL), TILE_BYTES);
-        tma_load_2d(smem_u32(sV), &tmV, bar(V_FULL), col0, j * BKV);
-        tma_load_2d(smem_u32(sV + BOX_BYTES), &tmV, bar(V_FULL), col0 + 64, j * BKV);
-      }
-    }
-  } else if (warp == 5) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(BQ, BKV, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BQ, DH, true);
-      const uint32_t tS = tmem + S_COL, tO = tmem + O_COL;
-      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      if (mbar_wait(bar(Q_FULL), 0, a.err, ERR_WAIT_ATTN_MMA)) {
-        for (int j = 0; j < a.num_kv; ++j) {
-          const uint32_t par = static_cast<uint32_t>(j) & 1u;
-          if (!mbar_wait(bar(K_FULL), par, a.err, ERR_WAIT_ATTN_MMA)) break;
-          // S_j overwrites P_{j-1}, which the previous P V product reads. MMAs
-          // issued by one thread execute in issue order, so QK_j is queued
-          // right behind PV_{j-1} without waiting for it; S_FULL's commit
-          // still covers PV_{j-1}, so the softmax sees O complete.
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-            mma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                   idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(S_FULL));
-          mma_commit(bar(K_EMPTY));
-          if (!mbar_wait(bar(P_FULL), par, a.err, ERR_WAIT_ATTN_MMA)) break;
-          if (!mbar_wait(bar(V_FULL), par, a.err, ERR_WAIT_ATTN_MMA)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk) {
-            // V rows kk*16 .. kk*16+15: 2 KB further per step; the two
-            // 64-wide head_dim halves are one box (16 KB) apart.
-            mma_ts(tO, tS + kk * 8, sdesc_sw128(v_addr + kk * 2048, BOX_BYTES, 1024), idesc_pv,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(O_DONE));
-          mma_commit(bar(V_EMPTY));
-        }
-      }
-    }
-  } else {
-    // ---------------------------------------------------------- softmax
-    const int row_in_tile = warp * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_base + S_COL;
-    const uint32_t tO = tmem + lane_base + O_COL;
-    float m = -INFINITY;  // running max, already multiplied by scale_log2
-    float l = 0.f;        // running sum of exp2(s * scale_log2 - m)
-    bool ok = true;
-    for (int j = 0; j < a.num_kv; ++j) {
-      if (!mbar_wait(bar(S_FULL), static_cast<uint32_t>(j) & 1u, a.err, ERR_WAIT_ATTN_SOFTMAX)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      softmax_tile(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l);
-      tc_fence_before();
-      mbar_arrive(bar(P_FULL));
-    }
-    // ---------------------------------------------------------- epilogue
-    if (ok && mbar_wait(bar(O_DONE), static_cast<uint32_t>(a.num_kv - 1) & 1u, a.err,
-                        ERR_WAIT_ATTN_SOFTMAX)) {
-      tc_fence_after();
-      const int row = q0 + row_in_tile;
-      store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 5) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Two query tiles per CTA (256 rows of one head) sharing every K/V tile.
 //   * warps 0-3 / 4-7: softmax of query tile 0 / 1 (thread = row = TMEM lane);
@@ -315,7 +182,7 @@ enum Bar2 {
 };
 
 __global__ void __launch_bounds__(Q2_THREADS, 1)
-    attention_2q_kernel(const __grid_constant__ CUtensorMap tmQ,
+    attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -471,16 +338,12 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
 h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
                            void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s) {
   static bool attr_done[64] = {};
-  static const bool one_tile = getenv("H3_ATTENTION_TWO_TILE") == nullptr;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attention_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attention_2q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(Q2_SMEM_BYTES));
+                                         static_cast<int>(Q2_SMEM_BYTES));
     if (e != cudaSuccess) return cuda_fail(e, "attention: set shared memory size");
     attr_done[dev] = true;
   }
@@ -498,13 +361,8 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   if ((st = make_tmap_bf16_2d(&tq, q, width, L, stride, 64, BQ)) != H3_OK) return st;
   if ((st = make_tmap_bf16_2d(&tk, k, width, L, stride, 64, BKV)) != H3_OK) return st;
   if ((st = make_tmap_bf16_2d(&tv, v, width, L, stride, 64, BKV)) != H3_OK) return st;
-  if (one_tile) {
-    dim3 grid((L + BQ - 1) / BQ, H);
-    attention_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a);
-  } else {
-    dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
-    attention_2q_kernel<<<grid, Q2_THREADS, Q2_SMEM_BYTES, s>>>(tq, tk, tv, a);
-  }
+  dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
+  attention_kernel<<<grid, Q2_THREADS, Q2_SMEM_BYTES, s>>>(tq, tk, tv, a);
   return cuda_fail(cudaGetLastError(), "attention launch");
 }
 
