@@ -45,6 +45,8 @@ def args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the FP8 block, block-stack and output-prep measurements")
     return ap.parse_args()
 
 
@@ -67,6 +69,23 @@ def block_work(S, L, D, H, Dh, F):
     mnr = L * D * (4 + 2) + L * D * (4 + 2 + 4 + 2) + L * D * (4 + 2 + 4)
     qk = 2 * L * D * 2 * 2
     return dict(attn_flop=attn, gemm_flop=gemm, elementwise_bytes=mnr + qk)
+
+
+def stage_work(S, L, D, H, Dh, F):
+    """Per stage of the block: (bound, algorithmic work, unit of the rate).
+    GEMMs count 2MNK, attention 4 L^2 H Dh, HBM-bound stages their minimum
+    bytes read + written (rows < L only)."""
+    return [
+        ("hbm", L * D * (4 + 2), "GB/s"),                        # r -> h1
+        ("tensor", 2.0 * L * D * 3 * D, "TFLOP/s"),              # QKV
+        ("hbm", 2 * L * D * 2 * 2, "GB/s"),                      # q, k in place
+        ("tensor", 4.0 * L * L * H * Dh, "TFLOP/s"),             # attention
+        ("tensor", 2.0 * L * D * D, "TFLOP/s"),                  # out
+        ("hbm", L * D * (4 + 2 + 4 + 2), "GB/s"),                # r, o -> r, h2
+        ("tensor", 2.0 * L * D * 2 * F, "TFLOP/s"),              # gate/up + SwiGLU
+        ("tensor", 2.0 * L * F * D, "TFLOP/s"),                  # down
+        ("hbm", L * D * (4 + 2 + 4), "GB/s"),                    # r, f -> r
+    ]
 
 
 # -------------------------------------------------------------- clock sampler
@@ -133,6 +152,25 @@ def gpu_uuid(torch, dev):
         return u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         return None
+
+
+# ------------------------------------------------------------ across ranks
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks of the default
+    process group (identity with one rank). Each rank runs its own replica of
+    the block, so the job's time is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_value(step_ms: float, world: int) -> float:
+    """Whole-job ms per block forward: N replicas finish N blocks per step."""
+    return step_ms / world
 
 
 # ----------------------------------------------------------- CPU baseline leg
@@ -211,6 +249,46 @@ def cpu_cores():
         return len(os.sched_getaffinity(0))
     except Exception:
         return os.cpu_count()
+
+
+# ------------------------------------------------------------------ extras
+def measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk):
+    """Rows beyond the BF16 block, timed after the main measurement with CUDA
+    events on the launching stream (3 warm-up launches each):
+      fp8_block     the block with online FP8 projections
+      stack4        4 blocks in one h3_stack_forward call (fused boundaries)
+      frames_to_u8  output preparation of the 10 s, 1344 x 768 clip"""
+    def timeit(fn, n):
+        for _ in range(3):
+            fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(n):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        h3.check_device_error()
+        return s.elapsed_time(e) / n
+
+    out = {}
+    r = inp["resid"].clone()
+    w8 = h3.quantize_block_weights_fp8(inp)
+    ws8 = torch.empty(h3.block_workspace_bytes_fp8(cfg), dtype=torch.uint8, device=r.device)
+    ms = timeit(lambda: h3.block_forward_fp8(cfg, w8, r, inp["mod"], inp["pos"], ws8), 3)
+    out["fp8_block"] = {"ms": round(ms, 3), "note": "four projections in FP8 E4M3 with per-row "
+                        "scales; attention and elementwise steps as in the BF16 block"}
+    del ws8, w8
+    mods = torch.stack([inp["mod"]] * 4).contiguous()
+    ms = timeit(lambda: h3.stack_forward(cfg, [inp] * 4, r, mods, inp["pos"], ws), 1)
+    out["stack4"] = {"ms_per_block": round(ms / 4, 3)}
+    f = torch.randn(1, 3, 243, 768, 1344, device=r.device).clamp_(-1.2, 1.2)
+    o = torch.empty(1, 243, 768, 1344, 3, dtype=torch.uint8, device=r.device)
+    ms = timeit(lambda: h3.frames_to_u8(f, o), 5)
+    gbs = f.numel() * 5 / ms / 1e6
+    out["frames_to_u8"] = {"ms": round(ms, 3), "achieved_gbs": round(gbs, 1),
+                           "frac_hbm": round(gbs / pk["hbm"], 3),
+                           "workload": "243 x 768 x 1344 RGB frames (FP32 in, uint8 out)"}
+    return out
 
 
 # ------------------------------------------------------------ reference arm
@@ -322,10 +400,8 @@ def run_ours(a):
     stage_ms = [statistics.mean(events[k][i].elapsed_time(events[k][i + 1])
                                 for k in range(a.steps)) for i in range(h3.BLOCK_STAGES)]
     step_ms = total_ms / a.steps
-    if world > 1:
-        t = torch.tensor([step_ms] + stage_ms, device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, stage_ms = t[0].item(), t[1:].tolist()
+    red = max_over_ranks([step_ms] + stage_ms, device=dev)
+    step_ms, stage_ms = red[0], red[1:]
 
     # ---- end to end through the C-ABI with host buffers: every step uploads
     # its residual, modulation and positions from pinned memory and downloads
@@ -334,13 +410,16 @@ def run_ours(a):
     # download overlap step k's compute; the timed region spans the first
     # upload to the last download.
     pin = lambda t: t.detach().to("cpu").pin_memory()
-    h_in = [(pin(inp["resid"]), pin(inp["mod"]), pin(inp["pos"])) for _ in range(2)]
-    h_out = [torch.empty_like(h_in[0][0]).pin_memory() for _ in range(2)]
+    h_one = (pin(inp["resid"]), pin(inp["mod"]), pin(inp["pos"]))
+    h_in = [h_one, h_one]  # both buffer sets upload the same host data
+    h_one_out = torch.empty_like(h_one[0]).pin_memory()
+    h_out = [h_one_out, h_one_out]
     d_buf = [(torch.empty_like(inp["resid"]), torch.empty_like(inp["mod"]),
               torch.empty_like(inp["pos"])) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in[0])
     d2h = h_out[0].numel() * 4
     up_s, down_s = torch.cuda.Stream(), torch.cuda.Stream()
+    comp_s = torch.cuda.Stream()  # not the legacy default stream, which would serialise the copies
 
     def e2e_run(n):
         up = [torch.cuda.Event() for _ in range(n)]
@@ -354,10 +433,10 @@ def run_ours(a):
                 for d, h in zip(d_buf[b], h_in[b]):
                     d.copy_(h, non_blocking=True)
                 up[k].record(up_s)
-            stream.wait_event(up[k])
+            comp_s.wait_event(up[k])
             h3.block_forward(cfg, weights, d_buf[b][0], d_buf[b][1], d_buf[b][2], ws,
-                             stream=stream)
-            done[k].record(stream)
+                             stream=comp_s)
+            done[k].record(comp_s)
             with torch.cuda.stream(down_s):
                 down_s.wait_event(done[k])
                 h_out[b].copy_(d_buf[b][0], non_blocking=True)
@@ -370,10 +449,7 @@ def run_ours(a):
     e2e_run(a.e2e_steps)
     e2e_ms = (time.perf_counter() - t0) * 1e3 / a.e2e_steps
     barrier()
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = max_over_ranks([e2e_ms], device=dev)[0]
     h3.check_device_error()
 
     if rank != 0:
@@ -389,12 +465,20 @@ def run_ours(a):
     attn_tf = work["attn_flop"] / attn_ms / 1e9
     gemm_tf = work["gemm_flop"] / gemm_ms / 1e9
     traffic = profile_traffic("h3_attention.cu", "attention_full_size.md")
+    stages_roofline = {}
+    for name, t, (bound, amount, unit) in zip(h3.STAGE_NAMES, stage_ms,
+                                              stage_work(S, L, D, H, Dh, F)):
+        rate = amount / t / (1e9 if unit == "TFLOP/s" else 1e6)
+        peak = pk["bf16_sustained"] if bound == "tensor" else pk["hbm"]
+        stages_roofline[name] = {"bound": bound, "achieved": round(rate, 1), "unit": unit,
+                                 "peak": peak, "frac": round(rate / peak, 3)}
+    extras = None if a.no_extras else measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk)
     cpu = None
     if not a.no_cpu_baseline and world == 1:
         ms, desc, secs = oracle_sample(shape)
         cpu = {"value": round(ms, 1), "unit": "ms", "cores": cpu_cores(), "kind": "oracle",
                "sample": desc + f" ({secs:.1f} s of CPU work)"}
-    value = step_ms / world  # whole-job ms per block forward (replicas)
+    value = job_value(step_ms, world)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "ms", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(step_ms, 3),
@@ -410,6 +494,7 @@ def run_ours(a):
         "elementwise_ms": round(ew_ms, 3),
         "elementwise_gbs": round(work["elementwise_bytes"] / ew_ms / 1e6, 1),
         "stages_ms": {n: round(t, 3) for n, t in zip(h3.STAGE_NAMES, stage_ms)},
+        "stages_roofline": stages_roofline,
         "roofline": {"bound": "tensor", "kernel": "attention_kernel",
                      "achieved": round(attn_tf, 1), "peak": pk["bf16_sustained"],
                      "unit": "TFLOP/s", "frac": round(attn_tf / pk["bf16_sustained"], 3),
@@ -421,6 +506,7 @@ def run_ours(a):
         "gpu_launches": h3.BLOCK_STAGES * a.steps,
         "e2e_note": "uploads and downloads on their own streams, two buffer sets: copies overlap compute",
         "clocks": clocks.summary(),
+        "extras": extras,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -114,8 +115,25 @@ int num_sms() {
   return d->sms;
 }
 
+static h3_status make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
+                              uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                              uint32_t box_inner, uint32_t box_outer);
+
 h3_status make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_stride_bytes,
+                      box_inner, box_outer);
+}
+
+h3_status make_tmap_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, outer, row_stride_bytes,
+                      box_inner, box_outer);
+}
+
+static h3_status make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
+                              uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                              uint32_t box_inner, uint32_t box_outer) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -130,7 +148,7 @@ h3_status make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, ui
   const cuuint64_t strides[1] = {row_stride_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -270,6 +288,26 @@ h3_status h3_attention_varlen(const void* q, const void* k, const void* v, void*
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
+h3_status h3_attention_varlen_skip(const void* q, const void* k, const void* v, void* o, int S,
+                                   int L, int H, int Dh, float softmax_scale, float skip_eps,
+                                   h3_stream_t stream) {
+  clear_error();
+  H3_REQUIRE(skip_eps >= 0.f && skip_eps < 1.f, H3_ERR_INVALID_ARG,
+             "skip_eps=%g must be in [0, 1)", static_cast<double>(skip_eps));
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(q && k && v && o, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  H3_REQUIRE(Dh == 128, H3_ERR_UNSUPPORTED, "head_dim %d unsupported (128 only)", Dh);
+  H3_REQUIRE(H > 0 && H <= 65535, H3_ERR_INVALID_ARG, "H=%d", H);
+  H3_REQUIRE(softmax_scale > 0.f, H3_ERR_INVALID_ARG, "softmax_scale must be > 0");
+  H3_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(o), H3_ERR_MISALIGNED,
+             "q, k, v, o must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  const int64_t ld = static_cast<int64_t>(H) * Dh;
+  return launch_attention(q, k, v, ld, o, ld, L, H, softmax_scale,
+                          reinterpret_cast<cudaStream_t>(stream), skip_eps);
+}
+
 h3_status h3_swiglu(const void* gate_up, void* out, int S, int L, int F, h3_stream_t stream) {
   clear_error();
   h3_status st = check_rows(S, L);
@@ -361,28 +399,48 @@ size_t h3_block_workspace_bytes(const h3_block_config* cfg) {
   return block_ws(cfg).total;
 }
 
-static h3_status block_forward_impl(const h3_block_config* cfg, const h3_block_weights* w,
-                                    float* resid, const float* mod, const int32_t* pos,
-                                    void* workspace, size_t workspace_bytes, h3_stream_t stream,
+static h3_status check_weights(const h3_block_weights* w) {
+  H3_REQUIRE(w != nullptr, H3_ERR_INVALID_ARG, "weights struct is NULL");
+  H3_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_down && w->q_gain && w->k_gain,
+             H3_ERR_INVALID_ARG, "a weight pointer is NULL");
+  H3_REQUIRE(aligned16(w->w_qkv) && aligned16(w->w_o) && aligned16(w->w_gu) &&
+                 aligned16(w->w_down) && aligned16(w->q_gain) && aligned16(w->k_gain),
+             H3_ERR_MISALIGNED, "weights and gains must be 16-byte aligned");
+  return H3_OK;
+}
+
+// Runs num_blocks blocks in order over the residual stream. Block b uses
+// w[b] and the modulation table mod + b * num_seg * 6 * D ([num_seg, 6, D]);
+// with seg given, row i uses group seg[i] of that table. The residual update
+// that ends block b and the modulated LayerNorm that starts block b + 1 run
+// as one pass over the residual. events (one block only): recorded before
+// every stage and after the last.
+static h3_status stack_forward_impl(const h3_block_config* cfg, const h3_block_weights* w,
+                                    int num_blocks, float* resid, const float* mod, int num_seg,
+                                    const int32_t* seg, const int32_t* pos, void* workspace,
+                                    size_t workspace_bytes, h3_stream_t stream,
                                     void* const* events, int num_events) {
   clear_error();
   h3_status st = check_block_config(cfg);
   if (st != H3_OK) return st;
-  H3_REQUIRE(w != nullptr, H3_ERR_INVALID_ARG, "weights struct is NULL");
-  H3_REQUIRE(w->w_qkv && w->w_o && w->w_gu && w->w_down && w->q_gain && w->k_gain,
-             H3_ERR_INVALID_ARG, "a weight pointer is NULL");
+  H3_REQUIRE(num_blocks >= 1, H3_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
+  H3_REQUIRE(num_seg >= 1, H3_ERR_INVALID_ARG, "num_seg=%d", num_seg);
+  H3_REQUIRE(seg != nullptr || num_seg == 1, H3_ERR_INVALID_ARG,
+             "num_seg=%d needs a seg array", num_seg);
+  H3_REQUIRE(w != nullptr, H3_ERR_INVALID_ARG, "weights array is NULL");
+  for (int b = 0; b < num_blocks; ++b)
+    if ((st = check_weights(&w[b])) != H3_OK) return st;
   H3_REQUIRE(resid && mod && pos, H3_ERR_INVALID_ARG, "resid, mod and pos must not be NULL");
   const BlockWs ws = block_ws(cfg);
   H3_REQUIRE(workspace != nullptr && workspace_bytes >= ws.total, H3_ERR_WORKSPACE,
              "workspace of %zu bytes given, %zu needed", workspace_bytes, ws.total);
   H3_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, H3_ERR_MISALIGNED,
              "workspace must be 256-byte aligned");
-  H3_REQUIRE(aligned16(w->w_qkv) && aligned16(w->w_o) && aligned16(w->w_gu) &&
-                 aligned16(w->w_down) && aligned16(w->q_gain) && aligned16(w->k_gain) &&
-                 aligned16(resid) && aligned16(mod),
-             H3_ERR_MISALIGNED, "weights, gains, resid and mod must be 16-byte aligned");
-  H3_REQUIRE(events == nullptr || num_events == H3_BLOCK_STAGES + 1, H3_ERR_INVALID_ARG,
-             "events: %d given, %d expected", num_events, H3_BLOCK_STAGES + 1);
+  H3_REQUIRE(aligned16(resid) && aligned16(mod), H3_ERR_MISALIGNED,
+             "resid and mod must be 16-byte aligned");
+  H3_REQUIRE(events == nullptr || (num_blocks == 1 && num_events == H3_BLOCK_STAGES + 1),
+             H3_ERR_INVALID_ARG, "events: %d given, %d expected (one block)", num_events,
+             H3_BLOCK_STAGES + 1);
   if (events != nullptr)
     for (int i = 0; i <= H3_BLOCK_STAGES; ++i)
       H3_REQUIRE(events[i] != nullptr, H3_ERR_INVALID_ARG, "events[%d] is NULL", i);
@@ -396,16 +454,17 @@ static h3_status block_forward_impl(const h3_block_config* cfg, const h3_block_w
   void* attn = base + ws.attn;
   void* proj = base + ws.proj;
   void* ffn = base + ws.ffn;
-  const float* shift1 = mod;
-  const float* scale1 = mod + D;
-  const float* gate1 = mod + 2 * D;
-  const float* shift2 = mod + 3 * D;
-  const float* scale2 = mod + 4 * D;
-  const float* gate2 = mod + 5 * D;
   const int64_t ld_qkv = 3LL * D;
+  const int64_t seg_stride = 6LL * D;  // floats between groups of one table
+  const int64_t block_stride = static_cast<int64_t>(num_seg) * seg_stride;
   auto mark = [&](int i) -> h3_status {
     if (events == nullptr) return H3_OK;
     return cuda_fail(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s), "event record");
+  };
+  auto mnr = [&](const void* delta, const float* gate, const float* shift, const float* scale,
+                 void* normed) {
+    return launch_mod_norm_residual(resid, delta, gate, shift, scale, normed, L, D, cfg->eps_ln,
+                                    s, seg, num_seg, seg_stride);
   };
 #define H3_STAGE(i, call)                          \
   do {                                             \
@@ -413,31 +472,54 @@ static h3_status block_forward_impl(const h3_block_config* cfg, const h3_block_w
     if ((st = (call)) != H3_OK) return st;         \
   } while (0)
 
-  // 0: h1 = LN(r) * (1 + scale1) + shift1
-  H3_STAGE(0, launch_mod_norm_residual(resid, nullptr, nullptr, shift1, scale1, h, L, D,
-                                       cfg->eps_ln, s));
-  // 1: [q | k | v] = h1 W_qkv^T
-  H3_STAGE(1, launch_gemm(h, D, w->w_qkv, D, qkv, ld_qkv, L, 3 * D, D, GEMM_STORE_BF16, s));
-  // 2: q, k <- RoPE(RMSNorm(q, k)) per head
-  H3_STAGE(2, launch_qk_norm_rope(qkv, qkv + 2LL * D, ld_qkv, w->q_gain, w->k_gain, pos,
-                                  cfg->axis_dims, L, H, cfg->theta, cfg->eps_qk, s));
-  // 3: a = softmax(q k^T / sqrt(Dh)) v over keys < L
-  H3_STAGE(3, launch_attention(qkv, qkv + 2LL * D, qkv + 4LL * D, ld_qkv, attn, D, L, H,
-                               1.0f / sqrtf(static_cast<float>(cfg->Dh)), s));
-  // 4: o = a W_o^T
-  H3_STAGE(4, launch_gemm(attn, D, w->w_o, D, proj, D, L, D, D, GEMM_STORE_BF16, s));
-  // 5: r <- r + gate1 * o ; h2 = LN(r) * (1 + scale2) + shift2
-  H3_STAGE(5, launch_mod_norm_residual(resid, proj, gate1, shift2, scale2, h, L, D, cfg->eps_ln,
-                                       s));
-  // 6: s = SiLU(h2 W_g^T) * (h2 W_u^T), SwiGLU fused in the projection's epilogue
-  H3_STAGE(6, launch_gemm(h, D, w->w_gu, D, ffn, F, L, F, D, GEMM_SWIGLU, s));
-  // 7: f = s W_down^T
-  H3_STAGE(7, launch_gemm(ffn, F, w->w_down, F, proj, D, L, D, F, GEMM_STORE_BF16, s));
-  // 8: r <- r + gate2 * f
-  H3_STAGE(8, launch_mod_norm_residual(resid, proj, gate2, nullptr, nullptr, nullptr, L, D,
-                                       cfg->eps_ln, s));
+  for (int b = 0; b < num_blocks; ++b) {
+    const h3_block_weights& wb = w[b];
+    // (shift1, scale1, gate1, shift2, scale2, gate2) of group 0 of block b
+    const float* m = mod + b * block_stride;
+    const float* shift1 = m;
+    const float* scale1 = m + D;
+    const float* gate1 = m + 2 * D;
+    const float* shift2 = m + 3 * D;
+    const float* scale2 = m + 4 * D;
+    const float* gate2 = m + 5 * D;
+    // 0: h1 = LN(r) * (1 + scale1) + shift1 (fused into the previous block's
+    //    last pass for b > 0)
+    if (b == 0) H3_STAGE(0, mnr(nullptr, nullptr, shift1, scale1, h));
+    // 1: [q | k | v] = h1 W_qkv^T
+    H3_STAGE(1, launch_gemm(h, D, wb.w_qkv, D, qkv, ld_qkv, L, 3 * D, D, GEMM_STORE_BF16, s));
+    // 2: q, k <- RoPE(RMSNorm(q, k)) per head
+    H3_STAGE(2, launch_qk_norm_rope(qkv, qkv + 2LL * D, ld_qkv, wb.q_gain, wb.k_gain, pos,
+                                    cfg->axis_dims, L, H, cfg->theta, cfg->eps_qk, s));
+    // 3: a = softmax(q k^T / sqrt(Dh)) v over keys < L
+    H3_STAGE(3, launch_attention(qkv, qkv + 2LL * D, qkv + 4LL * D, ld_qkv, attn, D, L, H,
+                                 1.0f / sqrtf(static_cast<float>(cfg->Dh)), s));
+    // 4: o = a W_o^T
+    H3_STAGE(4, launch_gemm(attn, D, wb.w_o, D, proj, D, L, D, D, GEMM_STORE_BF16, s));
+    // 5: r <- r + gate1 * o ; h2 = LN(r) * (1 + scale2) + shift2
+    H3_STAGE(5, mnr(proj, gate1, shift2, scale2, h));
+    // 6: s = SiLU(h2 W_g^T) * (h2 W_u^T), SwiGLU fused in the projection's epilogue
+    H3_STAGE(6, launch_gemm(h, D, wb.w_gu, D, ffn, F, L, F, D, GEMM_SWIGLU, s));
+    // 7: f = s W_down^T
+    H3_STAGE(7, launch_gemm(ffn, F, wb.w_down, F, proj, D, L, D, F, GEMM_STORE_BF16, s));
+    // 8: r <- r + gate2 * f, and for b + 1 < num_blocks the next block's
+    //    h1 = LN(r) * (1 + scale1') + shift1' in the same pass
+    if (b + 1 < num_blocks) {
+      const float* mn = mod + (b + 1) * block_stride;
+      H3_STAGE(8, mnr(proj, gate2, mn, mn + D, h));
+    } else {
+      H3_STAGE(8, mnr(proj, gate2, nullptr, nullptr, nullptr));
+    }
+  }
 #undef H3_STAGE
   return mark(H3_BLOCK_STAGES);
+}
+
+static h3_status block_forward_impl(const h3_block_config* cfg, const h3_block_weights* w,
+                                    float* resid, const float* mod, const int32_t* pos,
+                                    void* workspace, size_t workspace_bytes, h3_stream_t stream,
+                                    void* const* events, int num_events) {
+  return stack_forward_impl(cfg, w, 1, resid, mod, 1, nullptr, pos, workspace, workspace_bytes,
+                            stream, events, num_events);
 }
 
 h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w, float* resid,
@@ -454,6 +536,194 @@ h3_status h3_block_forward_events(const h3_block_config* cfg, const h3_block_wei
   H3_REQUIRE(events != nullptr, H3_ERR_INVALID_ARG, "events is NULL");
   return block_forward_impl(cfg, w, resid, mod, pos, workspace, workspace_bytes, stream, events,
                             num_events);
+}
+
+h3_status h3_stack_forward(const h3_block_config* cfg, const h3_block_weights* w,
+                           int num_blocks, float* resid, const float* mod, int num_seg,
+                           const int32_t* seg, const int32_t* pos, void* workspace,
+                           size_t workspace_bytes, h3_stream_t stream) {
+  return stack_forward_impl(cfg, w, num_blocks, resid, mod, num_seg, seg, pos, workspace,
+                            workspace_bytes, stream, nullptr, 0);
+}
+
+h3_status h3_mod_norm_residual_seg(float* resid, const void* delta, const float* gate,
+                                   const float* shift, const float* scale, const int32_t* seg,
+                                   int num_seg, int64_t seg_stride, void* normed, int S, int L,
+                                   int D, float eps, h3_stream_t stream) {
+  clear_error();
+  H3_REQUIRE(seg != nullptr, H3_ERR_INVALID_ARG, "seg is NULL");
+  H3_REQUIRE(num_seg >= 1, H3_ERR_INVALID_ARG, "num_seg=%d", num_seg);
+  H3_REQUIRE(seg_stride >= D || num_seg == 1, H3_ERR_INVALID_ARG,
+             "seg_stride=%lld is shorter than D=%d", static_cast<long long>(seg_stride), D);
+  H3_REQUIRE(seg_stride % 4 == 0, H3_ERR_MISALIGNED,
+             "seg_stride must be a multiple of 4 floats (16 bytes)");
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(resid != nullptr, H3_ERR_INVALID_ARG, "resid is NULL");
+  H3_REQUIRE(delta != nullptr || normed != nullptr, H3_ERR_INVALID_ARG,
+             "neither delta nor normed given: nothing to do");
+  H3_REQUIRE(delta == nullptr || gate != nullptr, H3_ERR_INVALID_ARG, "delta given without gate");
+  H3_REQUIRE(normed == nullptr || (shift != nullptr && scale != nullptr), H3_ERR_INVALID_ARG,
+             "normed given without shift and scale");
+  H3_REQUIRE(D > 0 && D % 8 == 0 && D <= 8192, H3_ERR_UNSUPPORTED,
+             "D=%d must be a positive multiple of 8, at most 8192", D);
+  H3_REQUIRE(eps >= 0.f, H3_ERR_INVALID_ARG, "eps < 0");
+  H3_REQUIRE(aligned16(resid) && aligned16(delta) && aligned16(gate) && aligned16(shift) &&
+                 aligned16(scale) && aligned16(normed),
+             H3_ERR_MISALIGNED, "a pointer is not 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_mod_norm_residual(resid, delta, gate, shift, scale, normed, L, D, eps,
+                                  reinterpret_cast<cudaStream_t>(stream), seg, num_seg,
+                                  seg_stride);
+}
+
+h3_status h3_frames_to_u8(const float* frames, uint8_t* out, int B, int C, int T, int H, int W,
+                          h3_stream_t stream) {
+  clear_error();
+  H3_REQUIRE(frames != nullptr && out != nullptr, H3_ERR_INVALID_ARG, "a pointer is NULL");
+  H3_REQUIRE(B >= 0 && C >= 1 && T >= 0 && H >= 0 && W >= 0, H3_ERR_INVALID_ARG,
+             "bad shape B=%d C=%d T=%d H=%d W=%d", B, C, T, H, W);
+  H3_REQUIRE(C <= 16, H3_ERR_UNSUPPORTED, "C=%d exceeds 16 channels", C);
+  const int64_t N = static_cast<int64_t>(T) * H * W;
+  H3_REQUIRE(N % 4 == 0, H3_ERR_UNSUPPORTED, "T*H*W=%lld must be a multiple of 4",
+             static_cast<long long>(N));
+  H3_REQUIRE(aligned16(frames) && (reinterpret_cast<uintptr_t>(out) & 3u) == 0,
+             H3_ERR_MISALIGNED, "frames must be 16-byte and out 4-byte aligned");
+  if (B == 0 || N == 0) return H3_OK;
+  return launch_frames_to_u8(frames, out, B, C, N, reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_quantize_fp8_rows(const void* x, void* q, float* scale, int R, int K,
+                               h3_stream_t stream) {
+  clear_error();
+  H3_REQUIRE(x && q && scale, H3_ERR_INVALID_ARG, "a pointer is NULL");
+  H3_REQUIRE(R >= 0, H3_ERR_INVALID_ARG, "R=%d", R);
+  H3_REQUIRE(K > 0 && K % 8 == 0 && K <= 16384, H3_ERR_UNSUPPORTED,
+             "K=%d must be a positive multiple of 8, at most 16384", K);
+  H3_REQUIRE(aligned16(x) && aligned16(q), H3_ERR_MISALIGNED, "x and q must be 16-byte aligned");
+  if (R == 0) return H3_OK;
+  return launch_quantize_fp8_rows(x, K, q, K, scale, R, K,
+                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_linear_fp8(const void* qx, const float* sx, const void* qw, const float* sw, void* y,
+                        int S, int L, int N, int K, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(qx && sx && qw && sw && y, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  H3_REQUIRE(N > 0 && N % 256 == 0, H3_ERR_UNSUPPORTED, "N=%d must be a multiple of 256", N);
+  H3_REQUIRE(K > 0 && K % 128 == 0, H3_ERR_UNSUPPORTED, "K=%d must be a multiple of 128", K);
+  H3_REQUIRE(aligned16(qx) && aligned16(qw) && aligned16(y), H3_ERR_MISALIGNED,
+             "qx, qw, y must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_gemm_fp8(qx, K, sx, qw, K, sw, y, N, L, N, K, GEMM_STORE_BF16,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_linear_swiglu_fp8(const void* qx, const float* sx, const void* qw_gu,
+                               const float* sw_gu, void* out, int S, int L, int F, int K,
+                               h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(qx && sx && qw_gu && sw_gu && out, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  H3_REQUIRE(F > 0 && F % 128 == 0, H3_ERR_UNSUPPORTED, "F=%d must be a multiple of 128", F);
+  H3_REQUIRE(K > 0 && K % 128 == 0, H3_ERR_UNSUPPORTED, "K=%d must be a multiple of 128", K);
+  H3_REQUIRE(aligned16(qx) && aligned16(qw_gu) && aligned16(out), H3_ERR_MISALIGNED,
+             "qx, qw_gu, out must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_gemm_fp8(qx, K, sx, qw_gu, K, sw_gu, out, F, L, F, K, GEMM_SWIGLU,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+// FP8 block workspace: the BF16 block's slices, then one FP8 code buffer
+// [S, max(D, F)] and one scale vector [S].
+struct BlockWsFp8 {
+  BlockWs bf;
+  size_t codes, scales, total;
+};
+static BlockWsFp8 block_ws_fp8(const h3_block_config* c) {
+  BlockWsFp8 w;
+  w.bf = block_ws(c);
+  size_t off = w.bf.total;
+  w.codes = off;  off += align256(static_cast<size_t>(c->S) * std::max(c->D, c->F));
+  w.scales = off; off += align256(static_cast<size_t>(c->S) * 4);
+  w.total = off;
+  return w;
+}
+
+size_t h3_block_workspace_bytes_fp8(const h3_block_config* cfg) {
+  clear_error();
+  if (check_block_config(cfg) != H3_OK) return 0;
+  if (cfg->D % 128 != 0) {
+    fail(H3_ERR_UNSUPPORTED, "D=%d must be a multiple of 128 for FP8 projections", cfg->D);
+    return 0;
+  }
+  return block_ws_fp8(cfg).total;
+}
+
+h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weights_fp8* w,
+                               float* resid, const float* mod, const int32_t* pos,
+                               void* workspace, size_t workspace_bytes, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_block_config(cfg);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(cfg->D % 128 == 0, H3_ERR_UNSUPPORTED, "D=%d must be a multiple of 128", cfg->D);
+  H3_REQUIRE(w != nullptr, H3_ERR_INVALID_ARG, "weights struct is NULL");
+  H3_REQUIRE(w->w_qkv && w->s_qkv && w->w_o && w->s_o && w->w_gu && w->s_gu && w->w_down &&
+                 w->s_down && w->q_gain && w->k_gain,
+             H3_ERR_INVALID_ARG, "a weight or scale pointer is NULL");
+  H3_REQUIRE(aligned16(w->w_qkv) && aligned16(w->w_o) && aligned16(w->w_gu) &&
+                 aligned16(w->w_down) && aligned16(w->q_gain) && aligned16(w->k_gain),
+             H3_ERR_MISALIGNED, "weights and gains must be 16-byte aligned");
+  H3_REQUIRE(resid && mod && pos, H3_ERR_INVALID_ARG, "resid, mod and pos must not be NULL");
+  H3_REQUIRE(aligned16(resid) && aligned16(mod), H3_ERR_MISALIGNED,
+             "resid and mod must be 16-byte aligned");
+  const BlockWsFp8 ws = block_ws_fp8(cfg);
+  H3_REQUIRE(workspace != nullptr && workspace_bytes >= ws.total, H3_ERR_WORKSPACE,
+             "workspace of %zu bytes given, %zu needed", workspace_bytes, ws.total);
+  H3_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, H3_ERR_MISALIGNED,
+             "workspace must be 256-byte aligned");
+  if (cfg->L == 0) return H3_OK;
+  const int L = cfg->L, D = cfg->D, H = cfg->H, F = cfg->F;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  void* h = base + ws.bf.h;
+  uint8_t* qkv = base + ws.bf.qkv;
+  void* attn = base + ws.bf.attn;
+  void* proj = base + ws.bf.proj;
+  void* ffn = base + ws.bf.ffn;
+  void* codes = base + ws.codes;
+  float* sc = reinterpret_cast<float*>(base + ws.scales);
+  const int64_t ld_qkv = 3LL * D;
+  const float* m = mod;
+  auto quant = [&](const void* x, int K) {
+    return launch_quantize_fp8_rows(x, K, codes, K, sc, L, K, s);
+  };
+  if ((st = launch_mod_norm_residual(resid, nullptr, nullptr, m, m + D, h, L, D, cfg->eps_ln,
+                                     s)) != H3_OK ||
+      (st = quant(h, D)) != H3_OK ||
+      (st = launch_gemm_fp8(codes, D, sc, w->w_qkv, D, w->s_qkv, qkv, ld_qkv, L, 3 * D, D,
+                            GEMM_STORE_BF16, s)) != H3_OK ||
+      (st = launch_qk_norm_rope(qkv, qkv + 2LL * D, ld_qkv, w->q_gain, w->k_gain, pos,
+                                cfg->axis_dims, L, H, cfg->theta, cfg->eps_qk, s)) != H3_OK ||
+      (st = launch_attention(qkv, qkv + 2LL * D, qkv + 4LL * D, ld_qkv, attn, D, L, H,
+                             1.0f / sqrtf(static_cast<float>(cfg->Dh)), s)) != H3_OK ||
+      (st = quant(attn, D)) != H3_OK ||
+      (st = launch_gemm_fp8(codes, D, sc, w->w_o, D, w->s_o, proj, D, L, D, D, GEMM_STORE_BF16,
+                            s)) != H3_OK ||
+      (st = launch_mod_norm_residual(resid, proj, m + 2 * D, m + 3 * D, m + 4 * D, h, L, D,
+                                     cfg->eps_ln, s)) != H3_OK ||
+      (st = quant(h, D)) != H3_OK ||
+      (st = launch_gemm_fp8(codes, D, sc, w->w_gu, D, w->s_gu, ffn, F, L, F, D, GEMM_SWIGLU,
+                            s)) != H3_OK ||
+      (st = quant(ffn, F)) != H3_OK ||
+      (st = launch_gemm_fp8(codes, F, sc, w->w_down, F, w->s_down, proj, D, L, D, F,
+                            GEMM_STORE_BF16, s)) != H3_OK)
+    return st;
+  return launch_mod_norm_residual(resid, proj, m + 5 * D, nullptr, nullptr, nullptr, L, D,
+                                  cfg->eps_ln, s);
 }
 
 // Scratch of h3_block_forward_noalloc: a fixed array in the library's device

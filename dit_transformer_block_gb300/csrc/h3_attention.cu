@@ -45,16 +45,28 @@ struct AttnArgs {
   int L;
   int num_kv;
   float scale_log2;  // softmax_scale * log2(e)
+  int skip;          // Skip-Softmax on
+  float skip_log2;   // skip a key tile when every row's tile max < m - skip_log2
   DevErr err;
 };
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // One KV tile of the online softmax for the calling thread's query row (TMEM
 // lane). S_j is read from tS; P_j (bf16 pairs) is written over its first 64
 // columns. valid = keys of this tile that are < L (>= BKV: none masked).
 // o_live: O already holds earlier tiles (so raising the max rescales it).
 // m, l: running max (times scale_log2) and row sum. Warp-collective.
-__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int valid, bool o_live,
-                                             float scale_log2, float& m, float& l) {
+// Skip-Softmax (skip != 0): the four warps of a query tile vote; when every
+// row's tile maximum lies more than skip_log2 below its running maximum the
+// tile is skipped (no exp2, no P; flags[quarter] tells the MMA warp to leave
+// out its P V product) and the function returns true.
+__device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid, bool o_live,
+                                             float scale_log2, float& m, float& l, int skip,
+                                             float skip_log2, volatile uint32_t* flags,
+                                             int bar_id) {
   uint32_t sr[128];
   {
     uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
@@ -85,6 +97,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int valid
     md = max3f(md, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
   }
   const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
+  if (skip) {
+    const bool row_skip = mx < m - skip_log2;  // never on the first tile (m = -inf)
+    const uint32_t warp_skip = __all_sync(0xffffffffu, row_skip) ? 1u : 0u;
+    const int quarter = (threadIdx.x >> 5) & 3;
+    if ((threadIdx.x & 31) == 0) flags[quarter] = warp_skip;
+    named_barrier_sync(bar_id, 128);
+    if (flags[0] & flags[1] & flags[2] & flags[3]) return true;
+  }
   // Raise the running max only when it is exceeded by more than the
   // threshold; the decision is warp-uniform because the O rescale uses
   // warp-collective TMEM loads and stores.
@@ -131,6 +151,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int valid
   }
   l += (la + lb) + (lc + ld);
   tmem_st_wait();
+  return false;
 }
 
 // Normalises the thread's O row by 1/l and stores it (bf16) when row_ok.
@@ -180,6 +201,8 @@ enum Bar2 {
   B2_O = B2_P + 2,
   B2_NUM = B2_O + 2
 };
+// barriers, the TMEM address word (padded to 16 bytes) and 16 vote flags
+static_assert(B2_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
 
 __global__ void __launch_bounds__(Q2_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -192,6 +215,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
   uint8_t* sQ = smem + KV_SLOTS * TILE_BYTES;       // 2 x 32 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B2_NUM);
+  // Skip-Softmax votes: [tile][parity of j][quarter]
+  volatile uint32_t* skip_flags = tmem_slot + 4;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
@@ -260,10 +285,13 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         }
         mma_commit(bar(B2_S + i));
       };
-      auto pv = [&](int i, int j) {  // O_i += P_i V_j
+      auto pv = [&](int i, int j) {  // O_i += P_i V_j (left out when the tile was skipped)
         const uint32_t v_addr = kv_addr + slot_of(2 * j + 1) * TILE_BYTES;
+        volatile uint32_t* f = skip_flags + (i * 2 + (j & 1)) * 4;
+        const bool skipped = a.skip && (f[0] & f[1] & f[2] & f[3]);
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
+          if (!skipped)
           mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
                  sdesc_sw128(v_addr + kk * 2048, BOX_BYTES, 1024), idesc_pv,
                  (j > 0 || kk > 0) ? 1u : 0u);
@@ -313,7 +341,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         break;
       }
       tc_fence_after();
-      softmax_tile(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l);
+      softmax_tile(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l, a.skip, a.skip_log2,
+                   skip_flags + (tile * 2 + (j & 1)) * 4, 1 + tile);
       tc_fence_before();
       mbar_arrive(bar(B2_P + tile));
     }
@@ -336,7 +365,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
 }  // namespace
 
 h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
-                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s) {
+                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
+                           float skip_eps) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -353,6 +383,8 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   a.L = L;
   a.num_kv = (L + BKV - 1) / BKV;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.skip = skip_eps > 0.f ? 1 : 0;
+  a.skip_log2 = skip_eps > 0.f ? -log2f(skip_eps) : 0.f;
   h3_status st = dev_err(&a.err);
   if (st != H3_OK) return st;
   CUtensorMap tq, tk, tv;

@@ -3,7 +3,9 @@
 // operands once with 16-byte (or 8-byte) vector loads, reduces with warp
 // shuffles, and writes its result once; only rows < L are touched.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "h3_internal.cuh"
@@ -163,14 +165,25 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
+// seg (optional): token-group index of every row; group g reads its gate,
+// shift and scale at an offset of g * seg_stride floats (a [G, 6, D] table).
+// Indices outside [0, num_seg) are clamped so every read stays in the table.
 template <int VPT>
 __global__ void __launch_bounds__(MNR_THREADS)
     mod_norm_residual_kernel(float* __restrict__ resid, const __nv_bfloat16* __restrict__ delta,
                              const float* __restrict__ gate, const float* __restrict__ shift,
                              const float* __restrict__ scale, __nv_bfloat16* __restrict__ normed,
-                             int D, float eps) {
+                             int D, float eps, const int32_t* __restrict__ seg, int num_seg,
+                             int64_t seg_stride) {
   __shared__ float red[MNR_THREADS / 32];
   const int row = blockIdx.x;
+  if (seg != nullptr) {
+    const int g = min(max(__ldg(seg + row), 0), num_seg - 1);
+    const int64_t off = static_cast<int64_t>(g) * seg_stride;
+    gate = gate ? gate + off : nullptr;
+    shift = shift ? shift + off : nullptr;
+    scale = scale ? scale + off : nullptr;
+  }
   const int D4 = D >> 2;
   float4* rrow = reinterpret_cast<float4*>(resid + static_cast<int64_t>(row) * D);
   float4 x[VPT];
@@ -227,7 +240,158 @@ __global__ void __launch_bounds__(MNR_THREADS)
   }
 }
 
+// --------------------------------------------------- GPU output preparation
+// vLLM-Omni H3 blog, section 3.4: decoded FP32 BCTHW frames become contiguous
+// uint8 BTHWC before they leave the GPU. Value map: round-half-even of
+// clamp(x / 2 + 1/2, 0, 1) * 255, each step rounded in FP32 (no FMA).
+// Each thread converts 4 consecutive pixels: one 16-byte load per channel
+// plane, 4*C contiguous output bytes written as 32-bit words.
+constexpr int U8_THREADS = 256;
+constexpr int U8_MAX_C = 16;
+
+__device__ __forceinline__ uint32_t frame_code(float x) {
+  float t = __fadd_rn(__fmul_rn(x, 0.5f), 0.5f);
+  t = fminf(fmaxf(t, 0.0f), 1.0f);
+  return __float2uint_rn(__fmul_rn(t, 255.0f));
+}
+
+// CC > 0: channel count fixed at compile time (packing stays in registers);
+// CC == 0: any C <= U8_MAX_C given at run time.
+template <int CC>
+__global__ void __launch_bounds__(U8_THREADS)
+    frames_to_u8_kernel(const float* __restrict__ in, uint8_t* __restrict__ out, int C_rt,
+                        int64_t N4 /* pixels per batch entry / 4 */, int64_t total4) {
+  const int C = CC > 0 ? CC : C_rt;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(U8_THREADS) + threadIdx.x; i < total4;
+       i += static_cast<int64_t>(gridDim.x) * U8_THREADS) {
+    const int64_t b = i / N4;
+    const int64_t p4 = i - b * N4;
+    const float4* src = reinterpret_cast<const float4*>(in) + b * C * N4 + p4;
+    uint32_t bytes[CC > 0 ? CC : U8_MAX_C];  // 4 pixels x C channels, little-endian
+#pragma unroll
+    for (int w = 0; w < (CC > 0 ? CC : U8_MAX_C); ++w) bytes[w] = 0;
+#pragma unroll
+    for (int c = 0; c < (CC > 0 ? CC : U8_MAX_C); ++c) {
+      if (c >= C) break;
+      const float4 v = __ldcs(src + static_cast<int64_t>(c) * N4);
+      const float px[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int byte = k * C + c;  // pixel k, channel c
+        bytes[byte >> 2] |= frame_code(px[k]) << (8 * (byte & 3));
+      }
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + (b * N4 + p4) * 4 * C);
+#pragma unroll
+    for (int w = 0; w < (CC > 0 ? CC : U8_MAX_C); ++w)
+      if (w < C) dst[w] = bytes[w];
+  }
+}
+
+// ---------------------------------------------- FP8 per-row quantisation
+// vLLM-Omni H3 blog, section 4.3 (online FP8: weights quantised at load
+// time, activations online). One CTA per row: amax over the row, inv = 448 /
+// amax, code = E4M3(x * inv) with saturation, scale = amax / 448; every step
+// rounded in FP32 (IEEE division and multiply).
+constexpr int Q8_THREADS = 256;
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = (lane < Q8_THREADS / 32) ? red[lane] : 0.f;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, m));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+template <int VPT>  // 8-element chunks per thread
+__global__ void __launch_bounds__(Q8_THREADS)
+    quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
+                             uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scale,
+                             int K) {
+  __shared__ float red[Q8_THREADS / 32];
+  const int row = blockIdx.x;
+  const int K8 = K >> 3;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(row) * ldx);
+  uint4 v[VPT];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = threadIdx.x + i * Q8_THREADS;
+    v[i] = c < K8 ? __ldcs(src + c) : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+  amax = block_max(amax, red);
+  const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+  uint2* dst = reinterpret_cast<uint2*>(q + static_cast<int64_t>(row) * ldq);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = threadIdx.x + i * Q8_THREADS;
+    if (c < K8) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[2 * j] = __fmul_rn(bf16_lo(w[j]), inv);
+        f[2 * j + 1] = __fmul_rn(bf16_hi(w[j]), inv);
+      }
+      dst[c] = make_uint2(e4m3x4(f[0], f[1], f[2], f[3]), e4m3x4(f[4], f[5], f[6], f[7]));
+    }
+  }
+  if (threadIdx.x == 0) scale[row] = __fdiv_rn(amax, 448.0f);
+}
+
 }  // namespace
+
+h3_status launch_quantize_fp8_rows(const void* x, int64_t ldx, void* q, int64_t ldq, float* scale,
+                                   int R, int K, cudaStream_t s) {
+  const int vpt = (K / 8 + Q8_THREADS - 1) / Q8_THREADS;
+  const auto* xx = static_cast<const __nv_bfloat16*>(x);
+  auto* qq = static_cast<uint8_t*>(q);
+#define H3_Q8_CASE(V)                                                                   \
+  case V:                                                                               \
+    quantize_fp8_rows_kernel<V><<<R, Q8_THREADS, 0, s>>>(xx, ldx, qq, ldq, scale, K); \
+    break;
+  switch (vpt) {
+    H3_Q8_CASE(1)
+    H3_Q8_CASE(2)
+    H3_Q8_CASE(3)
+    H3_Q8_CASE(4)
+    H3_Q8_CASE(5)
+    H3_Q8_CASE(6)
+    H3_Q8_CASE(7)
+    H3_Q8_CASE(8)
+    default:
+      return fail(H3_ERR_UNSUPPORTED, "quantize_fp8_rows: K=%d exceeds 16384", K);
+  }
+#undef H3_Q8_CASE
+  return cuda_fail(cudaGetLastError(), "quantize_fp8_rows launch");
+}
+
+h3_status launch_frames_to_u8(const float* in, uint8_t* out, int B, int C, int64_t N,
+                              cudaStream_t s) {
+  const int64_t N4 = N / 4;
+  const int64_t total4 = static_cast<int64_t>(B) * N4;
+  const int64_t want = (total4 + U8_THREADS - 1) / U8_THREADS;
+  const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(num_sms()) * 8));
+  if (C == 3)
+    frames_to_u8_kernel<3><<<grid, U8_THREADS, 0, s>>>(in, out, C, N4, total4);
+  else
+    frames_to_u8_kernel<0><<<grid, U8_THREADS, 0, s>>>(in, out, C, N4, total4);
+  return cuda_fail(cudaGetLastError(), "frames_to_u8 launch");
+}
 
 h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream_t s) {
   const int F8 = F / 8;
@@ -259,14 +423,15 @@ h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float*
 
 h3_status launch_mod_norm_residual(float* resid, const void* delta, const float* gate,
                                    const float* shift, const float* scale, void* normed, int L,
-                                   int D, float eps, cudaStream_t s) {
+                                   int D, float eps, cudaStream_t s, const int32_t* seg,
+                                   int num_seg, int64_t seg_stride) {
   const int vpt = (D / 4 + MNR_THREADS - 1) / MNR_THREADS;
   const auto* d = static_cast<const __nv_bfloat16*>(delta);
   auto* n = static_cast<__nv_bfloat16*>(normed);
 #define H3_MNR_CASE(V)                                                              \
   case V:                                                                           \
     mod_norm_residual_kernel<V><<<L, MNR_THREADS, 0, s>>>(resid, d, gate, shift, scale, n, D, \
-                                                          eps);                     \
+                                                          eps, seg, num_seg, seg_stride); \
     break;
   switch (vpt) {
     H3_MNR_CASE(1)

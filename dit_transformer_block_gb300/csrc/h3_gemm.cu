@@ -26,6 +26,7 @@
 namespace h3 {
 namespace {
 
+// BK counts bf16 elements; an FP8 stage holds 2 * BK codes in the same bytes.
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
 constexpr int B_BYTES = BN * BK * 2;        // 32 KB
@@ -38,6 +39,8 @@ constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 
 struct GemmArgs {
   void* C;
   int64_t ldc;
+  const float* sa;        // FP8: per-row scale of A [M]
+  const float* sb;        // FP8: per-row scale of B [rows of B]
   int M, N, K;            // M = valid rows; N = output columns
   int num_m, num_n, num_k;
   int num_tiles;
@@ -58,9 +61,14 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmArgs& a, int& mb
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// FP8 == true: A and B hold E4M3 codes (kind::f8f6f4, K = 32 per MMA, 128
+// codes per 128-byte row of a stage) and the epilogue multiplies the FP32
+// accumulator by sa[row] * sb[col] before rounding to bf16.
+template <bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs a) {
+  constexpr int KB_ELEMS = FP8 ? 2 * BK : BK;  // elements per K block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -122,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          const int kx = kb * BK;
+          const int kx = kb * KB_ELEMS;
           tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, fb, kx, mb * BM);
           tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB, fb, kx, b_row0);
           tma_load_2d(smem_u32(sB + stage * B_BYTES + B_BYTES / 2), &tmB, fb, kx, b_row1);
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -158,7 +166,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(b0 + k * 32, 16, 1024);
-            mma_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (FP8)
+              mma_ss_f8(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              mma_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           mma_commit(smem_u32(&empty[stage]));
           if (++stage == STAGES) {
@@ -188,6 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                              static_cast<uint32_t>(acc * BN);
       __nv_bfloat16* crow =
           static_cast<__nv_bfloat16*>(a.C) + static_cast<int64_t>(row) * a.ldc;
+      const float sa_row = FP8 ? (row_ok ? __ldg(a.sa + row) : 0.f) : 1.f;
       if (a.ep == GEMM_SWIGLU) {
         const int col0 = nb * (BN / 2);
 #pragma unroll 1
@@ -198,6 +210,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld_wait();
           tmem_reg_fence(g);
           tmem_reg_fence(u);
+          if constexpr (FP8) {
+            const float* sg = a.sb + col0 + c * 32;
+            const float* su = a.sb + a.b_half_rows + col0 + c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              g[j] = __float_as_uint(__uint_as_float(g[j]) * (sa_row * __ldg(sg + j)));
+              u[j] = __float_as_uint(__uint_as_float(u[j]) * (sa_row * __ldg(su + j)));
+            }
+          }
           uint32_t o[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -222,6 +243,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(t_row + c * 32, v);
           tmem_ld_wait();
           tmem_reg_fence(v);
+          if constexpr (FP8) {
+            const float* sc = a.sb + col0 + c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              v[j] = __float_as_uint(__uint_as_float(v[j]) * (sa_row * __ldg(sc + j)));
+          }
           uint32_t o[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
@@ -252,20 +279,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-                      int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s) {
+template <bool FP8>
+static h3_status launch_gemm_impl(const void* A, int64_t lda_bytes, const float* sa, const void* B,
+                                  int64_t ldb_bytes, const float* sb, void* C, int64_t ldc, int L,
+                                  int N, int K, GemmEpilogue ep, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return cuda_fail(e, "gemm: set shared memory size");
     attr_done[dev] = true;
   }
+  constexpr int kb_elems = FP8 ? 2 * BK : BK;
   GemmArgs a{};
   a.C = C;
   a.ldc = ldc;
+  a.sa = sa;
+  a.sb = sb;
   a.M = L;
   a.N = N;
   a.K = K;
@@ -275,21 +308,33 @@ h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, vo
   a.b_half_rows = (ep == GEMM_SWIGLU) ? N : 0;
   a.num_m = (L + BM - 1) / BM;
   a.num_n = N / tile_n;
-  a.num_k = (K + BK - 1) / BK;
+  a.num_k = (K + kb_elems - 1) / kb_elems;
   a.num_tiles = a.num_m * a.num_n;
   h3_status st = dev_err(&a.err);
   if (st != H3_OK) return st;
 
   CUtensorMap tmA, tmB;
-  st = make_tmap_bf16_2d(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(L),
-                         static_cast<uint64_t>(lda) * 2, BK, BM);
+  auto tmap = FP8 ? make_tmap_u8_2d : make_tmap_bf16_2d;
+  st = tmap(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(L),
+            static_cast<uint64_t>(lda_bytes), kb_elems, BM);
   if (st != H3_OK) return st;
-  st = make_tmap_bf16_2d(&tmB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(b_rows),
-                         static_cast<uint64_t>(ldb) * 2, BK, BN / 2);
+  st = tmap(&tmB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(b_rows),
+            static_cast<uint64_t>(ldb_bytes), kb_elems, BN / 2);
   if (st != H3_OK) return st;
   const int grid = std::min(a.num_tiles, num_sms());
-  gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, a);
+  gemm_kernel<FP8><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, a);
   return cuda_fail(cudaGetLastError(), "gemm launch");
+}
+
+h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                      int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s) {
+  return launch_gemm_impl<false>(A, lda * 2, nullptr, B, ldb * 2, nullptr, C, ldc, L, N, K, ep, s);
+}
+
+h3_status launch_gemm_fp8(const void* A, int64_t lda, const float* sa, const void* B, int64_t ldb,
+                          const float* sb, void* C, int64_t ldc, int L, int N, int K,
+                          GemmEpilogue ep, cudaStream_t s) {
+  return launch_gemm_impl<true>(A, lda, sa, B, ldb, sb, C, ldc, L, N, K, ep, s);
 }
 
 }  // namespace h3

@@ -23,15 +23,25 @@ int num_sms();
 // swizzle, zero fill outside the tensor.
 h3_status make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+// Same for a tensor of bytes (FP8 codes).
+h3_status make_tmap_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 // ---- kernel launchers (arguments already validated)
 h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream_t s);
 h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float* q_gain,
                               const float* k_gain, const int32_t* pos, const int* axis_dims,
                               int L, int H, float theta, float eps, cudaStream_t s);
+// seg (optional): per-row token-group index into a table whose groups are
+// seg_stride floats apart (gate/shift/scale point at group 0).
 h3_status launch_mod_norm_residual(float* resid, const void* delta, const float* gate,
                                    const float* shift, const float* scale, void* normed, int L,
-                                   int D, float eps, cudaStream_t s);
+                                   int D, float eps, cudaStream_t s, const int32_t* seg = nullptr,
+                                   int num_seg = 1, int64_t seg_stride = 0);
+
+// frames [B, C, N] float32 (N = T*H*W, N % 4 == 0) -> [B, N, C] uint8.
+h3_status launch_frames_to_u8(const float* in, uint8_t* out, int B, int C, int64_t N,
+                              cudaStream_t s);
 
 enum GemmEpilogue : int {
   GEMM_STORE_BF16 = 0,   // C = bf16(acc)
@@ -43,8 +53,22 @@ enum GemmEpilogue : int {
 h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                       int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s);
 
+// FP8 (E4M3) operands with per-row scales: C[:L] = epilogue(bf16-free
+// (A @ B^T) * sa[row] * sb[col]). A [L, K] codes (row stride lda bytes), B
+// [N or 2N, K] codes (row stride ldb bytes), sa [L], sb [N or 2N].
+h3_status launch_gemm_fp8(const void* A, int64_t lda, const float* sa, const void* B, int64_t ldb,
+                          const float* sb, void* C, int64_t ldc, int L, int N, int K,
+                          GemmEpilogue ep, cudaStream_t s);
+// Per-row absmax quantisation of bf16 x [R, K] (row stride ldx elements) to
+// E4M3 codes q [R, K] (row stride ldq bytes) and float32 scales [R].
+h3_status launch_quantize_fp8_rows(const void* x, int64_t ldx, void* q, int64_t ldq, float* scale,
+                                   int R, int K, cudaStream_t s);
+
 // o[:L] = attention(q, k, v); q/k/v rows of stride ld_in elements, o of ld_out.
+// skip_eps > 0: Skip-Softmax, a key tile is left out for a query tile when
+// every row's tile maximum is below eps times the row's running maximum.
 h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
-                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s);
+                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
+                           float skip_eps = 0.f);
 
 }  // namespace h3

@@ -36,6 +36,14 @@ class BlockConfig(ctypes.Structure):
                 ("theta", ctypes.c_float), ("eps_ln", ctypes.c_float), ("eps_qk", ctypes.c_float)]
 
 
+class BlockWeightsFp8(ctypes.Structure):
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("s_qkv", ctypes.c_void_p),
+                ("w_o", ctypes.c_void_p), ("s_o", ctypes.c_void_p),
+                ("w_gu", ctypes.c_void_p), ("s_gu", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
+                ("q_gain", ctypes.c_void_p), ("k_gain", ctypes.c_void_p)]
+
+
 class BlockWeights(ctypes.Structure):
     _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p), ("w_gu", ctypes.c_void_p),
                 ("w_down", ctypes.c_void_p), ("q_gain", ctypes.c_void_p),
@@ -53,6 +61,7 @@ _SIGS = {
     "h3_qk_norm_rope": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P]),
     "h3_attention_varlen": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
     "h3_swiglu": (_I, [_P, _P, _I, _I, _I, _P]),
+    "h3_attention_varlen_skip": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P]),
     "h3_linear": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_linear_swiglu": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_block_workspace_bytes": (_SZ, [ctypes.POINTER(BlockConfig)]),
@@ -63,6 +72,17 @@ _SIGS = {
     "h3_block_forward_noalloc": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights),
                                       _P, _P, _P, _P]),
     "h3_debug_wait_timeout": (_I, [_U64, _P]),
+    "h3_mod_norm_residual_seg": (_I, [_P, _P, _P, _P, _P, _P, _I, ctypes.c_int64, _P, _I, _I, _I,
+                                      _F, _P]),
+    "h3_frames_to_u8": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
+    "h3_quantize_fp8_rows": (_I, [_P, _P, _P, _I, _I, _P]),
+    "h3_linear_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "h3_linear_swiglu_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "h3_block_workspace_bytes_fp8": (_SZ, [ctypes.POINTER(BlockConfig)]),
+    "h3_block_forward_fp8": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeightsFp8),
+                                  _P, _P, _P, _P, _SZ, _P]),
+    "h3_stack_forward": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), _I, _P,
+                              _P, _I, _P, _P, _P, _SZ, _P]),
 }
 
 _lib = None
@@ -147,6 +167,23 @@ def mod_norm_residual(resid, delta=None, gate=None, shift=None, scale=None, norm
         _p(resid), _p(delta), _p(gate), _p(shift), _p(scale), _p(normed), S, L, D, eps, _s(stream)))
 
 
+def mod_norm_residual_seg(resid, table, seg, delta=None, gate_idx=None, shift_idx=None,
+                          scale_idx=None, normed=None, L=None, eps=1e-6, stream=None):
+    """mod_norm_residual with token-group modulation: table [G, 6, D] f32,
+    seg [S] int32; row i uses table[seg[i], idx] for the gate/shift/scale
+    indices given (0..5), e.g. gate_idx=2, shift_idx=3, scale_idx=4."""
+    _need(resid, torch.float32, "resid")
+    _need(table, torch.float32, "table")
+    _need(seg, torch.int32, "seg")
+    S, D = resid.shape
+    G = table.shape[0]
+    L = S if L is None else L
+    row = lambda i: None if i is None else ctypes.c_void_p(table[0, i].data_ptr())
+    _check("mod_norm_residual_seg", lib().h3_mod_norm_residual_seg(
+        _p(resid), _p(delta), row(gate_idx), row(shift_idx), row(scale_idx), _p(seg), G, 6 * D,
+        _p(normed), S, L, D, eps, _s(stream)))
+
+
 def qk_norm_rope(q, k, q_gain, k_gain, pos, axis_dims, L=None, theta=1e4, eps=1e-6, stream=None):
     """In-place per-head RMSNorm + RoPE of q, k [S,H,Dh] bf16."""
     _need(q, torch.bfloat16, "q")
@@ -169,6 +206,17 @@ def attention_varlen(q, k, v, o, L=None, scale=None, stream=None):
     scale = Dh ** -0.5 if scale is None else scale
     _check("attention_varlen", lib().h3_attention_varlen(
         _p(q), _p(k), _p(v), _p(o), S, L, H, Dh, scale, _s(stream)))
+
+
+def attention_varlen_skip(q, k, v, o, L=None, scale=None, skip_eps=0.0, stream=None):
+    """attention_varlen with Skip-Softmax tile skipping (skip_eps = 0: dense)."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _need(t, torch.bfloat16, n)
+    S, H, Dh = q.shape
+    L = S if L is None else L
+    scale = Dh ** -0.5 if scale is None else scale
+    _check("attention_varlen_skip", lib().h3_attention_varlen_skip(
+        _p(q), _p(k), _p(v), _p(o), S, L, H, Dh, scale, skip_eps, _s(stream)))
 
 
 def swiglu(gate_up, out, L=None, stream=None):
@@ -214,6 +262,90 @@ def block_forward_noalloc(cfg: BlockConfig, weights, resid, mod, pos, stream=Non
     w = weights if isinstance(weights, BlockWeights) else block_weights(weights)
     _check("block_forward_noalloc", lib().h3_block_forward_noalloc(
         ctypes.byref(cfg), ctypes.byref(w), _p(resid), _p(mod), _p(pos), _s(stream)))
+
+
+def stack_forward(cfg: BlockConfig, weights_list, resid, mods, pos, workspace, seg=None,
+                  stream=None):
+    """Blocks applied in order: weights_list[b] (dict or BlockWeights) with
+    mods [num_blocks, G, 6, D] f32 (or [num_blocks, 6, D] when seg is None);
+    seg [S] int32 picks each row's group."""
+    n = len(weights_list)
+    arr = (BlockWeights * n)(*(w if isinstance(w, BlockWeights) else block_weights(w)
+                               for w in weights_list))
+    G = 1 if mods.dim() == 3 else mods.shape[1]
+    _need(mods, torch.float32, "mods")
+    _check("stack_forward", lib().h3_stack_forward(
+        ctypes.byref(cfg), arr, n, _p(resid), _p(mods), G, _p(seg), _p(pos), _p(workspace),
+        workspace.numel() * workspace.element_size(), _s(stream)))
+
+
+def frames_to_u8(frames, out, stream=None):
+    """frames [B, C, T, H, W] f32 -> out [B, T, H, W, C] uint8."""
+    _need(frames, torch.float32, "frames")
+    _need(out, torch.uint8, "out")
+    B, C, T, H, W = frames.shape
+    _check("frames_to_u8", lib().h3_frames_to_u8(_p(frames), _p(out), B, C, T, H, W,
+                                                  _s(stream)))
+
+
+def quantize_fp8_rows(x, q, scale, stream=None):
+    """x [R, K] bf16 -> q [R, K] uint8 (E4M3 codes), scale [R] f32."""
+    _need(x, torch.bfloat16, "x")
+    _need(q, torch.uint8, "q")
+    _need(scale, torch.float32, "scale")
+    R, K = x.shape
+    _check("quantize_fp8_rows", lib().h3_quantize_fp8_rows(_p(x), _p(q), _p(scale), R, K,
+                                                            _s(stream)))
+
+
+def linear_fp8(qx, sx, qw, sw, y, L=None, stream=None):
+    S, K = qx.shape
+    N = qw.shape[0]
+    L = S if L is None else L
+    _check("linear_fp8", lib().h3_linear_fp8(_p(qx), _p(sx), _p(qw), _p(sw), _p(y), S, L, N, K,
+                                              _s(stream)))
+
+
+def linear_swiglu_fp8(qx, sx, qw_gu, sw_gu, out, L=None, stream=None):
+    S, K = qx.shape
+    F = out.shape[1]
+    L = S if L is None else L
+    _check("linear_swiglu_fp8", lib().h3_linear_swiglu_fp8(
+        _p(qx), _p(sx), _p(qw_gu), _p(sw_gu), _p(out), S, L, F, K, _s(stream)))
+
+
+def quantize_block_weights_fp8(weights: dict, stream=None) -> dict:
+    """Load-time FP8 quantisation of a block's four projection weights:
+    returns a dict with codes (uint8) and per-row scales for each, plus the
+    Q/K gains, ready for block_forward_fp8."""
+    out = {"q_gain": weights["q_gain"], "k_gain": weights["k_gain"]}
+    for k in ("w_qkv", "w_o", "w_gu", "w_down"):
+        w = weights[k]
+        q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+        sc = torch.empty(w.shape[0], dtype=torch.float32, device=w.device)
+        quantize_fp8_rows(w, q, sc, stream)
+        out[k] = q
+        out["s_" + k[2:]] = sc
+    return out
+
+
+def block_weights_fp8(w: dict) -> BlockWeightsFp8:
+    return BlockWeightsFp8(*(w[k].data_ptr() for k in (
+        "w_qkv", "s_qkv", "w_o", "s_o", "w_gu", "s_gu", "w_down", "s_down", "q_gain", "k_gain")))
+
+
+def block_workspace_bytes_fp8(cfg: BlockConfig) -> int:
+    n = lib().h3_block_workspace_bytes_fp8(ctypes.byref(cfg))
+    if n == 0:
+        raise H3Error("block_workspace_bytes_fp8", 1, last_error())
+    return n
+
+
+def block_forward_fp8(cfg: BlockConfig, weights_fp8, resid, mod, pos, workspace, stream=None):
+    w = weights_fp8 if isinstance(weights_fp8, BlockWeightsFp8) else block_weights_fp8(weights_fp8)
+    _check("block_forward_fp8", lib().h3_block_forward_fp8(
+        ctypes.byref(cfg), ctypes.byref(w), _p(resid), _p(mod), _p(pos), _p(workspace),
+        workspace.numel() * workspace.element_size(), _s(stream)))
 
 
 def block_workspace_bytes(cfg: BlockConfig) -> int:

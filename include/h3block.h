@@ -123,6 +123,23 @@ h3_status h3_attention_varlen(const void* q, const void* k, const void* v, void*
                               int L, int H, int Dh, float softmax_scale, h3_stream_t stream);
 
 /*
+ * a3 with Skip-Softmax (next step after dense attention; blog section 4.3:
+ * skip the softmax and P x V of tiles the QK scores show to be negligible,
+ * decided per tile). Keys are taken in tiles of 128 from key 0 and queries in
+ * tiles of 128 from row 0. A key tile is left out for a query tile when, for
+ * every row of that query tile, the tile's largest score is below
+ * skip_eps times the row's running maximum weight (base-2 exponent more than
+ * log2(1/skip_eps) below the running maximum over the tiles kept so far; the
+ * running maximum may lag the exact one by up to 2^8, which only makes the
+ * test more conservative). skip_eps == 0 is exactly h3_attention_varlen.
+ * The first key tile is never skipped. Arguments as h3_attention_varlen;
+ * 0 <= skip_eps < 1.
+ */
+h3_status h3_attention_varlen_skip(const void* q, const void* k, const void* v, void* o, int S,
+                                   int L, int H, int Dh, float softmax_scale, float skip_eps,
+                                   h3_stream_t stream);
+
+/*
  * a5 — SwiGLU (blog section 3.2, #6283): out[i,j] = SiLU(g) * u with
  * g = gate_up[i,j], u = gate_up[i,F+j], SiLU(g) = g / (1 + exp(-g)), for i < L.
  *   gate_up [S, 2F] bf16, out [S, F] bf16. F % 8 == 0.
@@ -196,6 +213,106 @@ size_t h3_block_workspace_bytes(const h3_block_config* cfg);
 h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w, float* resid,
                            const float* mod, const int32_t* pos, void* workspace,
                            size_t workspace_bytes, h3_stream_t stream);
+
+/*
+ * a1 with token-group modulation (next step after the per-sample form):
+ * the pages denoise conditioning and noisy tokens and video and audio tokens
+ * (with their own sigma schedules) in one packed sequence (blog section 1,
+ * Fig. 1; H3 blog PR, dual schedules). Row i takes its gate, shift and scale
+ * from group seg[i] of a table: group g's vectors are at gate + g*seg_stride,
+ * shift + g*seg_stride, scale + g*seg_stride (floats). Otherwise as
+ * h3_mod_norm_residual.
+ *   seg  [S] int32 device, values in [0, num_seg) (values outside are clamped
+ *        to that range, so reads stay inside the table)
+ *   seg_stride  floats between groups, >= D, multiple of 4
+ */
+h3_status h3_mod_norm_residual_seg(float* resid, const void* delta, const float* gate,
+                                   const float* shift, const float* scale, const int32_t* seg,
+                                   int num_seg, int64_t seg_stride, void* normed, int S, int L,
+                                   int D, float eps, h3_stream_t stream);
+
+/*
+ * A stack of num_blocks blocks applied in order to the residual stream, the
+ * way the denoiser runs its transformer blocks in every forward (blog
+ * section 5). Block b uses w[b] and the modulation table
+ *   mod + b * num_seg * 6 * D      ([num_seg, 6, D] float32, per block)
+ * and, when seg is not NULL, row i uses group seg[i] of that table (see
+ * h3_mod_norm_residual_seg; seg NULL requires num_seg == 1). The residual
+ * update that ends block b and the modulated LayerNorm that starts block
+ * b + 1 run as one pass over the residual. One workspace of
+ * h3_block_workspace_bytes(cfg) serves the whole stack. With num_blocks == 1,
+ * num_seg == 1 and seg == NULL this is h3_block_forward.
+ *   w    host array of num_blocks weight structs
+ */
+h3_status h3_stack_forward(const h3_block_config* cfg, const h3_block_weights* w,
+                           int num_blocks, float* resid, const float* mod, int num_seg,
+                           const int32_t* seg, const int32_t* pos, void* workspace,
+                           size_t workspace_bytes, h3_stream_t stream);
+
+/*
+ * GPU output preparation (blog section 3.4; a stage next to the block): decoded
+ * video frames [B, C, T, H, W] float32 become contiguous [B, T, H, W, C]
+ * uint8, a quarter of the bytes, before they leave the GPU. Each value maps to
+ *   round_half_even( clamp(x * 0.5 + 0.5, 0, 1) * 255 )
+ * with every step rounded in float32 (no fused multiply-add); NaN maps to 0.
+ *   frames  16-byte aligned; out 4-byte aligned; T*H*W % 4 == 0; 1 <= C <= 16
+ */
+h3_status h3_frames_to_u8(const float* frames, uint8_t* out, int B, int C, int T, int H, int W,
+                          h3_stream_t stream);
+
+/*
+ * Online FP8 projections (next step after the BF16 block; blog section 4.3,
+ * "online FP8": eligible linear layers get FP8 weights and scales once at
+ * load time, their activations are quantised online). Format: E4M3 codes,
+ * one float32 scale per row (per output channel for weights, per token for
+ * activations); value = code * scale.
+ *
+ * h3_quantize_fp8_rows: x [R, K] bf16 -> q [R, K] E4M3 codes (bytes), scale
+ * [R] float32, per row: amax = max|x|, inv = 448 / amax (0 if amax == 0),
+ * q = E4M3_satfinite(x * inv) (round to nearest even), scale = amax / 448,
+ * each step rounded in float32. K % 8 == 0, K <= 16384. Serves both the
+ * load-time weight quantisation and the online activation quantisation.
+ */
+h3_status h3_quantize_fp8_rows(const void* x, void* q, float* scale, int R, int K,
+                               h3_stream_t stream);
+
+/*
+ * y[i, :] = bf16( (qx[i, :] . qw[j, :]) * sx[i] * sw[j] ) for i < L: an FP8
+ * projection on tcgen05 (kind::f8f6f4), FP32 accumulation.
+ *   qx [S, K] codes, sx [S]; qw [N, K] codes, sw [N]; y [S, N] bf16.
+ *   K % 128 == 0, N % 256 == 0.
+ */
+h3_status h3_linear_fp8(const void* qx, const float* sx, const void* qw, const float* sw, void* y,
+                        int S, int L, int N, int K, h3_stream_t stream);
+
+/* FP8 gate/up projection with SwiGLU in the epilogue: as h3_linear_swiglu with
+ * FP8 operands (qw_gu [2F, K] codes with scales sw_gu [2F]); the two products
+ * are scaled and rounded to bf16 before the SiLU. F % 128 == 0, K % 128 == 0. */
+h3_status h3_linear_swiglu_fp8(const void* qx, const float* sx, const void* qw_gu,
+                               const float* sw_gu, void* out, int S, int L, int F, int K,
+                               h3_stream_t stream);
+
+/* Block weights with FP8 projections (codes from h3_quantize_fp8_rows). */
+typedef struct h3_block_weights_fp8 {
+  const void* w_qkv;  const float* s_qkv;   /* [3D, D] codes, [3D] scales */
+  const void* w_o;    const float* s_o;     /* [D, D], [D]                */
+  const void* w_gu;   const float* s_gu;    /* [2F, D], [2F]              */
+  const void* w_down; const float* s_down;  /* [D, F], [D]                */
+  const float* q_gain;                      /* [Dh]                       */
+  const float* k_gain;                      /* [Dh]                       */
+} h3_block_weights_fp8;
+
+/* Workspace for h3_block_forward_fp8 (0 when the config is invalid). */
+size_t h3_block_workspace_bytes_fp8(const h3_block_config* cfg);
+
+/* h3_block_forward with the four projections in FP8: every projection input
+ * (h1, the attention output, h2, the SwiGLU output) is quantised per token
+ * with h3_quantize_fp8_rows before its FP8 GEMM; everything else (modulation,
+ * Q/K RMSNorm + RoPE, attention, SwiGLU) is the BF16/FP32 path. D % 128 == 0,
+ * F % 128 == 0 in addition to h3_block_forward's limits. */
+h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weights_fp8* w,
+                               float* resid, const float* mod, const int32_t* pos,
+                               void* workspace, size_t workspace_bytes, h3_stream_t stream);
 
 /* Number of kernel stages h3_block_forward launches, in the order listed
  * above: 0 modulation+LN, 1 QKV projection, 2 Q/K RMSNorm+RoPE, 3 attention,

@@ -108,13 +108,18 @@ def mod_norm_residual(resid, delta=None, gate=None, shift=None, scale=None,
     """
     r = np.asarray(resid, dtype=np.float64)
     if delta is not None:
-        r = round_f32(r + np.asarray(gate, np.float64)[None, :] * np.asarray(delta, np.float64))
+        r = round_f32(r + _per_row(gate) * np.asarray(delta, np.float64))
     h = None
     if scale is not None:
         n = layer_norm(r, eps)
-        h = round_bf16(n * (1.0 + np.asarray(scale, np.float64)[None, :])
-                       + np.asarray(shift, np.float64)[None, :])
+        h = round_bf16(n * (1.0 + _per_row(scale)) + _per_row(shift))
     return r, h
+
+
+def _per_row(v) -> np.ndarray:
+    """A modulation vector [D] (same for every row) or one per row [rows, D]."""
+    v = np.asarray(v, np.float64)
+    return v[None, :] if v.ndim == 1 else v
 
 
 # ---------------------------------------------------------------------------
@@ -239,15 +244,30 @@ def swiglu(gu) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def unpack_mod(mod):
-    """mod [6, D] -> (shift1, scale1, gate1, shift2, scale2, gate2)."""
+    """mod [6, D] -> (shift1, scale1, gate1, shift2, scale2, gate2).
+    mod [rows, 6, D] (one modulation per row) -> six [rows, D] arrays."""
     mod = np.asarray(mod, np.float64)
-    return tuple(mod[i] for i in range(6))
+    return tuple(mod[..., i, :] for i in range(6))
+
+
+def modulation_rows(mod, seg, rows):
+    """Modulation of the given rows. mod [6, D] applies to every token; with
+    seg [S] (the token-group index of every row, e.g. video vs audio tokens
+    that follow their own sigma schedule, or conditioning vs noisy tokens;
+    vLLM-Omni H3 blog, section 1 Fig. 1, and the H3 blog PR's dual
+    video/audio schedules) mod is a table [G, 6, D] and row i uses
+    mod[seg[i]]. Returns [6, D] or [len(rows), 6, D]."""
+    mod = np.asarray(mod, np.float64)
+    if seg is None:
+        return mod
+    return mod[np.asarray(seg)[np.asarray(rows)]]
 
 
 def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
                   *, L: int, heads: int, head_dim: int, axis_dims, theta: float,
                   eps_ln: float = 1e-6, eps_qk: float = 1e-6, rows=None,
-                  kv_chunk: int = 4096, return_intermediates: bool = False):
+                  kv_chunk: int = 4096, return_intermediates: bool = False, seg=None,
+                  fp8: bool = False):
     """Forward pass of one DiT block for query rows `rows` (default all < L).
 
     resid [S, D] float32 residual stream; mod [6, D]; weights bf16-valued
@@ -256,13 +276,28 @@ def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
     to all of them); everything after attention is row-local, so only the
     asked-for rows are carried through. Returns the updated residual rows
     [len(rows), D] (float32 values) and, optionally, a dict of the
-    intermediates for those rows.
+    intermediates for those rows. seg: optional token-group index per row,
+    with mod a table [G, 6, D] (see modulation_rows). fp8: the four
+    projections run as online FP8 (weights and inputs quantised per row,
+    see quantize_fp8_rows / linear_fp8).
     """
+    qw_cache = {}
+
+    def proj(x, w):
+        if not fp8:
+            return linear(x, w)
+        key = id(w)
+        if key not in qw_cache:
+            qw_cache[key] = quantize_fp8_rows(w)
+        qx, sx = quantize_fp8_rows(x)
+        qw, sw = qw_cache[key]
+        return linear_fp8(qx, sx, qw, sw)
+
     D = heads * head_dim
     if rows is None:
         rows = np.arange(L)
     rows = np.asarray(rows)
-    sh1, sc1, g1, sh2, sc2, g2 = unpack_mod(mod)
+    sh1, sc1, g1, sh2, sc2, g2 = unpack_mod(modulation_rows(mod, seg, rows))
     r_all = np.asarray(resid, np.float64)[:L]
     w_qkv = np.asarray(w_qkv, np.float64)
     scale = 1.0 / np.sqrt(head_dim)
@@ -274,25 +309,224 @@ def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
     w_v = w_qkv[2 * D:3 * D]
     for c0 in range(0, L, kv_chunk):
         c1 = min(L, c0 + kv_chunk)
-        _, h1c = mod_norm_residual(r_all[c0:c1], shift=sh1, scale=sc1, eps=eps_ln)
-        kc = linear(h1c, w_k).reshape(c1 - c0, heads, head_dim)
+        shc, scc = unpack_mod(modulation_rows(mod, seg, np.arange(c0, c1)))[:2]
+        _, h1c = mod_norm_residual(r_all[c0:c1], shift=shc, scale=scc, eps=eps_ln)
+        kc = proj(h1c, w_k).reshape(c1 - c0, heads, head_dim)
         k_all[c0:c1] = qk_norm_rope(kc, k_gain, pos[c0:c1], axis_dims, theta, eps_qk)
-        v_all[c0:c1] = linear(h1c, w_v).reshape(c1 - c0, heads, head_dim)
+        v_all[c0:c1] = proj(h1c, w_v).reshape(c1 - c0, heads, head_dim)
 
     r = r_all[rows]
     _, h1 = mod_norm_residual(r, shift=sh1, scale=sc1, eps=eps_ln)
-    q = linear(h1, w_qkv[0:D]).reshape(len(rows), heads, head_dim)
+    q = proj(h1, w_qkv[0:D]).reshape(len(rows), heads, head_dim)
     q = qk_norm_rope(q, q_gain, np.asarray(pos)[rows], axis_dims, theta, eps_qk)
     q_full = np.zeros((L, heads, head_dim))
     q_full[rows] = q
     a = attention(q_full, k_all, v_all, L, scale, rows=rows).reshape(len(rows), D)
-    o = linear(a, w_o)
+    o = proj(a, w_o)
     r, h2 = mod_norm_residual(r, o, g1, sh2, sc2, eps=eps_ln)
-    gu = linear(h2, w_gu)
+    gu = proj(h2, w_gu)
     u = swiglu(gu)
-    f = linear(u, w_down)
+    f = proj(u, w_down)
     r, _ = mod_norm_residual(r, f, g2, eps=eps_ln)
     if return_intermediates:
         return r, dict(h1=h1, q=q, k=k_all[rows], v=v_all[rows], a=a, o=o,
                        h2=h2, gu=gu, u=u, f=f)
     return r
+
+
+def stack_forward(resid, mods, weights, q_gains, k_gains, pos, *, L: int, heads: int,
+                  head_dim: int, axis_dims, theta: float, eps_ln: float = 1e-6,
+                  eps_qk: float = 1e-6, seg=None):
+    """Blocks applied one after another to the whole residual stream (all
+    rows < L); the denoiser runs its transformer blocks in sequence for every
+    forward (vLLM-Omni H3 blog, section 5: FastH3's forwards). mods[b] and
+    (w_qkv, w_o, w_gu, w_down) = weights[b] belong to block b."""
+    r = np.asarray(resid, np.float64).copy()
+    for b in range(len(mods)):
+        w_qkv, w_o, w_gu, w_down = weights[b]
+        r[:L] = block_forward(r, mods[b], w_qkv, w_o, w_gu, w_down, q_gains[b], k_gains[b], pos,
+                              L=L, heads=heads, head_dim=head_dim, axis_dims=axis_dims,
+                              theta=theta, eps_ln=eps_ln, eps_qk=eps_qk, seg=seg)
+    return r[:L]
+
+
+# ---------------------------------------------------------------------------
+# GPU output preparation ([vLLM-Omni H3 blog] section 3.4: decoded FP32
+# BCTHW frames become contiguous uint8 BTHWC before transfer, a quarter of the
+# bytes). The pages give no formula; the reading here is the usual decoder
+# convention: x in [-1, 1] maps to round(clamp(x / 2 + 1/2, 0, 1) * 255) with
+# round-half-to-even, every step in float32 (the precision both sides use for
+# this integer decision), no fused multiply-add.
+# ---------------------------------------------------------------------------
+
+def frames_to_u8(frames) -> np.ndarray:
+    """frames [B, C, T, H, W] float32 -> [B, T, H, W, C] uint8."""
+    x = np.asarray(frames, dtype=np.float32)
+    t = (x * np.float32(0.5)).astype(np.float32) + np.float32(0.5)
+    t = np.clip(t, np.float32(0.0), np.float32(1.0)).astype(np.float32)
+    v = np.rint((t * np.float32(255.0)).astype(np.float32))
+    return np.ascontiguousarray(np.moveaxis(v.astype(np.uint8), 1, -1))
+
+
+# ---------------------------------------------------------------------------
+# Online FP8 projections ([vLLM-Omni H3 blog] section 4.3, "online FP8": the
+# eligible linear layers' weights are quantised to FP8 once at load time with
+# their scales, and their activations are quantised online). The pages give
+# no scaling granularity; the reading here is per-row absmax scaling to
+# FP8 E4M3 (max 448): each weight row (output channel) and each activation
+# row (token) gets its own float32 scale. Every step that decides a code is
+# taken in float32 on both sides:
+#   amax = max |x|,  inv = 448 / amax (0 when amax == 0),  code = e4m3(x * inv)
+#   scale = amax / 448  (dequantised value = code * scale)
+# and the product is y = bf16( (sum_k qa[i,k] qw[j,k]) * sa[i] * sw[j] ).
+# ---------------------------------------------------------------------------
+
+_E4M3_MAX = 448.0
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Round float64 values to FP8 E4M3 (1 sign, 4 exponent bits with bias 7,
+    3 mantissa bits; no infinities), nearest-even, saturating to +-448.
+    Normal numbers have 4 significant bits; below 2^-6 the step is 2^-9."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros_like(x)
+    nz = x != 0
+    _, e = np.frexp(x[nz])
+    q = np.maximum(e - 4, -9).astype(np.float64)
+    step = np.exp2(q)
+    r = np.rint(x[nz] / step) * step
+    out[nz] = np.clip(r, -_E4M3_MAX, _E4M3_MAX)
+    return out
+
+
+def quantize_fp8_rows(x):
+    """Per-row absmax quantisation of x [rows, K] (bf16 values) to E4M3.
+    Returns (codes as float64 values [rows, K], scales float32 values [rows])."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=1)
+    with np.errstate(divide="ignore"):
+        inv = np.where(amax > 0, np.float32(_E4M3_MAX) / amax, np.float32(0)).astype(np.float32)
+    prod = (x32 * inv[:, None]).astype(np.float32)
+    codes = round_e4m3(prod.astype(np.float64))
+    scale = (amax / np.float32(_E4M3_MAX)).astype(np.float32)
+    return codes, scale.astype(np.float64)
+
+
+def linear_fp8(qx, sx, qw, sw) -> np.ndarray:
+    """bf16( (qx @ qw^T) * sx[:, None] * sw[None, :] ), float64 accumulation."""
+    acc = np.asarray(qx, np.float64) @ np.asarray(qw, np.float64).T
+    return round_bf16(acc * np.asarray(sx, np.float64)[:, None] * np.asarray(sw, np.float64)[None, :])
+
+
+# ---------------------------------------------------------------------------
+# Skip-Softmax ([vLLM-Omni H3 blog] section 4.3: the attention backend can
+# skip the softmax and P x V work of tiles the QK scores show to be
+# negligible, decided per tile). Reading: keys are taken in tiles of 128 from
+# key 0 and queries in tiles of 128 from row 0; a key tile is skipped for a
+# query tile when, for every query row of that tile, the tile's largest
+# scaled score lies more than log2(1/eps) below the row's running maximum
+# (in base-2 units, over the key tiles already kept). eps = 0 never skips and
+# is dense attention.
+# ---------------------------------------------------------------------------
+
+def attention_skip(q, k, v, L: int, scale: float, eps: float, tile: int = 128):
+    """Attention with tile-level skipping; returns (out [L, H, Dh] bf16 values,
+    kept [n_qtiles, H, n_ktiles] bool)."""
+    q = np.asarray(q, np.float64)[:L]
+    k = np.asarray(k, np.float64)[:L]
+    v = np.asarray(v, np.float64)[:L]
+    H = q.shape[1]
+    nq = (L + tile - 1) // tile
+    nk = (L + tile - 1) // tile
+    out = np.empty_like(q)
+    kept = np.ones((nq, H, nk), bool)
+    thresh = np.inf if eps <= 0 else np.log2(1.0 / eps)
+    for h in range(H):
+        s = (q[:, h, :] @ k[:, h, :].T) * scale / np.log(2.0)  # base-2 logits
+        for qi in range(nq):
+            r0, r1 = qi * tile, min(L, (qi + 1) * tile)
+            m = np.full(r1 - r0, -np.inf)
+            keep_cols = []
+            for kj in range(nk):
+                c0, c1 = kj * tile, min(L, (kj + 1) * tile)
+                tmax = s[r0:r1, c0:c1].max(axis=1)
+                if np.all(tmax < m - thresh):
+                    kept[qi, h, kj] = False
+                    continue
+                m = np.maximum(m, tmax)
+                keep_cols.append(np.arange(c0, c1))
+            cols = np.concatenate(keep_cols)
+            z = s[r0:r1][:, cols]
+            p = np.exp2(z - z.max(axis=1, keepdims=True))
+            out[r0:r1, h, :] = (p / p.sum(axis=1, keepdims=True)) @ v[cols, h, :]
+    return round_bf16(out), kept
+
+
+# ---------------------------------------------------------------------------
+# FP8 ("SAGE") attention ([vLLM-Omni H3 blog] section 4.3: the attention
+# backend can quantise Q, K, P and V to FP8 for the QK and PV products). The
+# pages give no scaling scheme; the reading here:
+#   * K is first smoothed by subtracting its per-(head, channel) mean over the
+#     L valid keys, rounded to bf16 (softmax is unchanged: each row's scores
+#     move by one constant);
+#   * Q and the smoothed K are quantised to E4M3 per (128-row tile, head)
+#     block, V per (head, channel) over the valid keys, each with absmax
+#     scaling (inv = 448 / amax, code = e4m3(x * inv), scale = amax / 448,
+#     every step in float32);
+#   * scores = (Q codes . K codes) * sq * sk; softmax in base 2 against the
+#     row maximum; P is rounded to E4M3 for the PV product, the row sum uses
+#     the unrounded P; O = (P codes . V codes) * sv / sum.
+# ---------------------------------------------------------------------------
+
+def _absmax_codes(x32, axis):
+    """float32 block -> (E4M3 code values, float32 scale), absmax over `axis`."""
+    amax = np.max(np.abs(x32), axis=axis, keepdims=True)
+    with np.errstate(divide="ignore"):
+        inv = np.where(amax > 0, np.float32(_E4M3_MAX) / amax, np.float32(0)).astype(np.float32)
+    codes = round_e4m3((x32 * inv).astype(np.float32).astype(np.float64))
+    scale = (amax / np.float32(_E4M3_MAX)).astype(np.float32)
+    return codes, scale
+
+
+def sage_quantize(q, k, v, L: int, tile: int = 128):
+    """FP8 operands of SAGE attention. q, k, v [S, H, Dh] bf16 values.
+    Returns dict: qc [L,H,Dh], sq [nt,H], kc, sk [nt,H], vc, sv [H,Dh],
+    k_mean [H,Dh] (bf16 values)."""
+    q = np.asarray(q, np.float32)[:L]
+    k = np.asarray(k, np.float32)[:L]
+    v = np.asarray(v, np.float32)[:L]
+    H, Dh = q.shape[1], q.shape[2]
+    k_mean = round_bf16(np.asarray(k, np.float64).mean(axis=0))
+    ks = (k - k_mean.astype(np.float32)[None]).astype(np.float32)
+    nt = (L + tile - 1) // tile
+    qc = np.empty((L, H, Dh)); kc = np.empty((L, H, Dh))
+    sq = np.empty((nt, H), np.float32); sk = np.empty((nt, H), np.float32)
+    for t in range(nt):
+        r0, r1 = t * tile, min(L, (t + 1) * tile)
+        c, s = _absmax_codes(q[r0:r1], axis=(0, 2))
+        qc[r0:r1], sq[t] = c, s[0, :, 0]
+        c, s = _absmax_codes(ks[r0:r1], axis=(0, 2))
+        kc[r0:r1], sk[t] = c, s[0, :, 0]
+    vc, sv = _absmax_codes(v, axis=0)
+    return dict(qc=qc, sq=sq, kc=kc, sk=sk, vc=vc, sv=sv[0], k_mean=k_mean)
+
+
+def attention_sage(ops, L: int, scale: float, rows=None, tile: int = 128):
+    """FP8 attention from sage_quantize's operands, for query rows `rows`."""
+    if rows is None:
+        rows = np.arange(L)
+    rows = np.asarray(rows)
+    qc, kc, vc = ops["qc"], ops["kc"], ops["vc"]
+    sq = ops["sq"].astype(np.float64)
+    sk = ops["sk"].astype(np.float64)
+    sv = ops["sv"].astype(np.float64)
+    H, Dh = qc.shape[1], qc.shape[2]
+    key_tile = np.arange(L) // tile
+    out = np.empty((len(rows), H, Dh))
+    for h in range(H):
+        s = (qc[rows, h, :] @ kc[:, h, :].T) * sq[rows // tile, h][:, None] * sk[key_tile, h][None, :]
+        z = s * scale / np.log(2.0)
+        p = np.exp2(z - z.max(axis=1, keepdims=True))
+        pc = round_e4m3(p)
+        out[:, h, :] = (pc @ vc[:, h, :]) * sv[h][None, :] / p.sum(axis=1, keepdims=True)
+    return round_bf16(out)

@@ -61,7 +61,11 @@ def assert_close_block(x, ref, f_ref, o_ref, gate1, gate2, r_in, what="block"):
     ref = np.asarray(ref, np.float64)
     r_in = np.asarray(r_in, np.float64).reshape(np.shape(ref))
     assert np.all(np.isfinite(x)), f"{what}: non-finite output"
-    slack = np.abs(gate2)[None, :] * bf16_ulp(f_ref) + np.abs(gate1)[None, :] * bf16_ulp(o_ref)
+    g1 = np.abs(np.asarray(gate1, np.float64))
+    g2 = np.abs(np.asarray(gate2, np.float64))
+    g1 = g1[None, :] if g1.ndim == 1 else g1
+    g2 = g2[None, :] if g2.ndim == 1 else g2
+    slack = g2 * bf16_ulp(f_ref) + g1 * bf16_ulp(o_ref)
     for name, a, b in (("output", x, ref), ("increment", x - r_in, ref - r_in)):
         bound = BF16_ELEM * np.maximum(1.0, np.abs(b)) + slack
         ratio = np.max(np.abs(a - b) / bound)

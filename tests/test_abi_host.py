@@ -108,3 +108,22 @@ def test_product_path_does_not_import_the_oracle():
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                        cwd=str(__import__('pathlib').Path(__file__).resolve().parents[1]))
     assert r.returncode == 0, r.stderr
+
+
+def test_stack_and_segmented_argument_errors(lib):
+    cfg = h3.block_config(256, 250, 512, 4, 128, 1536, (128, 0, 0))
+    n = lib.h3_block_workspace_bytes(ctypes.byref(cfg))
+    w = (h3.BlockWeights * 2)(h3.BlockWeights(4096, 4096, 4096, 4096, 4096, 4096),
+                              h3.BlockWeights(4096, 4096, 4096, 4096, 4096, 4096))
+    f = lib.h3_stack_forward
+    assert f(ctypes.byref(cfg), w, 0, P, P, 1, NULL, P, P, n, NULL) == 1      # no blocks
+    assert f(ctypes.byref(cfg), w, 2, P, P, 2, NULL, P, P, n, NULL) == 1      # groups w/o seg
+    assert f(ctypes.byref(cfg), w, 2, P, P, 0, P, P, P, n, NULL) == 1         # zero groups
+    assert f(ctypes.byref(cfg), w, 2, P, P, 1, NULL, P, P, n - 1, NULL) == 4  # workspace
+    w[1].w_o = None
+    assert f(ctypes.byref(cfg), w, 2, P, P, 1, NULL, P, P, n, NULL) == 1      # NULL weight
+    g = lib.h3_mod_norm_residual_seg
+    assert g(P, P, P, NULL, NULL, NULL, 2, 512, NULL, 8, 8, 64, 1e-6, NULL) == 1  # no seg
+    assert g(P, P, P, NULL, NULL, P, 2, 32, NULL, 8, 8, 64, 1e-6, NULL) == 1    # stride < D
+    assert g(P, P, P, NULL, NULL, P, 2, 66, NULL, 8, 8, 64, 1e-6, NULL) == 3    # stride % 4
+    assert g(P, P, P, NULL, NULL, P, 0, 512, NULL, 8, 8, 64, 1e-6, NULL) == 1   # no groups

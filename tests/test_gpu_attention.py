@@ -86,3 +86,53 @@ def test_attention_full_size_sampled(h3lib):
     ref = O.attention(np64(inp["q"][:L]), np64(inp["k"][:L]), np64(inp["v"][:L]), L, 128 ** -0.5,
                       rows=rows)
     assert_close_bf16(np64(o[torch.from_numpy(rows).to(dev)]), ref, "attention full")
+
+
+def test_skip_softmax_eps_zero_is_dense_bitwise(h3lib):
+    S, L, H = 640, 600, 3
+    inp = I.attention_inputs(S, L, H, 128, seed=8, device=dev)
+    o1 = run(h3lib, inp["q"], inp["k"], inp["v"], L)
+    o2 = torch.full_like(o1, SENT)
+    h3lib.attention_varlen_skip(inp["q"], inp["k"], inp["v"], o2, L, skip_eps=0.0)
+    h3lib.check_device_error()
+    assert torch.equal(o1, o2)
+
+
+def test_skip_softmax_skips_the_tile_the_rule_names(h3lib):
+    # scores in base-2 units (softmax scale ln 2): key tile 0 scores 20, tile 1
+    # scores 18.5 (1.5 below the running max: skipped at eps = 1/2), tile 2
+    # scores 19.5 (kept); every query row is the same, so the decision is the
+    # same for every row and tile 1's keys would carry real weight if kept
+    S = L = 384
+    H = 1
+    q = torch.zeros(S, H, 128)
+    q[:, 0, 0] = 1.0
+    k = torch.zeros(S, H, 128)
+    k[:128, 0, 0] = 20.0
+    k[128:256, 0, 0] = 18.5
+    k[256:, 0, 0] = 19.5
+    g = torch.Generator().manual_seed(9)
+    v = torch.randn(S, H, 128, generator=g)
+    v[128:256] += 1.0  # makes the skipped tile's weight visible in the output
+    q, k, v = (t.to(torch.bfloat16).to(dev) for t in (q, k, v))
+    scale = float(np.log(2.0))
+    o_skip = torch.full_like(q, SENT)
+    h3lib.attention_varlen_skip(q, k, v, o_skip, L, scale=scale, skip_eps=0.5)
+    h3lib.check_device_error()
+    ref, kept = O.attention_skip(np64(q), np64(k), np64(v), L, scale, 0.5)
+    assert kept[:, 0].tolist() == [[True, False, True]] * 3
+    assert_close_bf16(np64(o_skip[:L]), ref, "skip-softmax")
+    o_dense = torch.full_like(q, SENT)
+    h3lib.attention_varlen(q, k, v, o_dense, L, scale=scale)
+    h3lib.check_device_error()
+    assert (o_skip.float() - o_dense.float()).abs().max().item() > 0.05
+
+
+def test_skip_softmax_random_data_matches_dense_within_eps(h3lib):
+    S, L, H = 2048, 2000, 2
+    inp = I.attention_inputs(S, L, H, 128, seed=10, device=dev)
+    o = torch.full_like(inp["q"], SENT)
+    h3lib.attention_varlen_skip(inp["q"], inp["k"], inp["v"], o, L, skip_eps=2.0 ** -20)
+    h3lib.check_device_error()
+    ref = O.attention(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), L, 128 ** -0.5)
+    assert_close_bf16(np64(o[:L]), ref, "skip-softmax random")

@@ -7,7 +7,7 @@ import torch
 
 import oracle.h3_oracle as O
 from dit_transformer_block_gb300 import inputs as I
-from helpers import assert_close_block, np64, sample_rows
+from helpers import assert_close_bf16, assert_close_block, np64, sample_rows
 
 pytestmark = pytest.mark.gpu
 dev = "cuda"
@@ -97,3 +97,84 @@ def test_block_stack_length_sweep(h3lib, L):
         check_block(out[torch.from_numpy(rows).to(dev)], shape, inp, rows, f"block {b} L={L}")
         assert torch.equal(out[L:], inp["resid"][L:])
         x = out
+
+
+def _stack_inputs(shape, nblocks, G=None, seed=20):
+    blocks = [{k: v.to(dev) for k, v in I.block_inputs(shape, seed=seed + b).items()}
+              for b in range(nblocks)]
+    resid = blocks[0]["resid"].clone()
+    if G is None:
+        mods = torch.stack([b["mod"] for b in blocks]).contiguous()
+        seg = None
+    else:
+        g = torch.Generator(device="cpu")
+        g.manual_seed(seed)
+        mods = (torch.randn(nblocks, G, 6, shape.D, generator=g) * 0.1).to(dev).contiguous()
+        seg = torch.randint(0, G, (shape.S,), generator=g, dtype=torch.int32).to(dev)
+    return blocks, resid, mods, seg
+
+
+def _oracle_stack(shape, blocks, resid, mods, seg):
+    W = [tuple(np64(b[k]) for k in ("w_qkv", "w_o", "w_gu", "w_down")) for b in blocks]
+    return O.stack_forward(np64(resid), list(np64(mods)), W, [np64(b["q_gain"]) for b in blocks],
+                           [np64(b["k_gain"]) for b in blocks], blocks[0]["pos"].cpu().numpy(),
+                           L=shape.L, heads=shape.H,
+                           head_dim=shape.Dh, axis_dims=shape.axis_dims, theta=shape.theta,
+                           seg=None if seg is None else seg.cpu().numpy())
+
+
+def _cfg(h3lib, shape):
+    return h3lib.block_config(shape.S, shape.L, shape.D, shape.H, shape.Dh, shape.F,
+                              shape.axis_dims, shape.theta, shape.eps_ln, shape.eps_qk)
+
+
+@pytest.mark.parametrize("G", [None, 3])
+def test_stack_of_four_tiny_blocks(h3lib, G):
+    shape = I.TINY
+    blocks, resid0, mods, seg = _stack_inputs(shape, 4, G)
+    cfg = _cfg(h3lib, shape)
+    ws = torch.empty(h3lib.block_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    out = resid0.clone()
+    h3lib.stack_forward(cfg, blocks, out, mods, blocks[0]["pos"], ws, seg=seg)
+    h3lib.check_device_error()
+    ref = _oracle_stack(shape, blocks, resid0, mods, seg)
+    assert_close_bf16(np64(out[:shape.L]), ref, "stack")
+    r_in = np64(resid0[:shape.L])
+    assert_close_bf16(np64(out[:shape.L]) - r_in, ref - r_in, "stack increment")
+    assert torch.equal(out[shape.L:], resid0[shape.L:])
+    if G is None:
+        # the fused block boundary gives the same bits as separate block calls
+        seq = resid0.clone()
+        for b in range(4):
+            h3lib.block_forward(cfg, blocks[b], seq, mods[b], blocks[0]["pos"], ws)
+        h3lib.check_device_error()
+        assert torch.equal(seq, out)
+
+
+@pytest.mark.slow
+def test_segmented_block_full_size_sampled(h3lib):
+    shape = I.FULL
+    inp = I.block_inputs(shape, seed=7, device=dev)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(7)
+    mods = (torch.randn(1, 2, 6, shape.D, generator=g) * 0.1).to(dev).contiguous()
+    # video tokens in group 0, the trailing audio/text tokens in group 1
+    seg = torch.zeros(shape.S, dtype=torch.int32, device=dev)
+    seg[shape.L - shape.n_tail:] = 1
+    cfg = _cfg(h3lib, shape)
+    ws = torch.empty(h3lib.block_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    out = inp["resid"].clone()
+    h3lib.stack_forward(cfg, [inp], out, mods, inp["pos"], ws, seg=seg)
+    h3lib.check_device_error()
+    rows = np.unique(np.concatenate([sample_rows(shape.L, 256, 8),
+                                     np.arange(shape.L - shape.n_tail, shape.L)]))
+    n = {k: np64(v) if v.is_floating_point() else v.cpu().numpy() for k, v in inp.items()}
+    ref, mids = O.block_forward(n["resid"], np64(mods[0]), n["w_qkv"], n["w_o"], n["w_gu"],
+                                n["w_down"], n["q_gain"], n["k_gain"], n["pos"], L=shape.L,
+                                heads=shape.H, head_dim=shape.Dh, axis_dims=shape.axis_dims,
+                                theta=shape.theta, rows=rows, return_intermediates=True,
+                                seg=seg.cpu().numpy())
+    m = O.modulation_rows(np64(mods[0]), seg.cpu().numpy(), rows)
+    from helpers import assert_close_block as acb
+    acb(np64(out[torch.from_numpy(rows).to(dev)]), ref, mids["f"], mids["o"], m[:, 2], m[:, 5],
+        n["resid"][rows], "segmented block full")

@@ -118,3 +118,26 @@ def test_gate_zero_leaves_residual_bitwise(h3lib):
     h3lib.mod_norm_residual(inp["resid"], inp["delta"], torch.zeros(D, device=dev), L=L)
     h3lib.check_device_error()
     assert torch.equal(inp["resid"], r0)
+
+
+@pytest.mark.parametrize("S,L,D,G", [(256, 250, 512, 3), (64, 61, 5376, 2),
+                                     (58816, 58758, 5376, 2)])
+def test_mod_norm_residual_segmented(h3lib, S, L, D, G):
+    inp = I.mod_inputs(S, D, seed=34, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(35)
+    table = (torch.randn(G, 6, D, generator=g, device=dev) * 0.1).contiguous()
+    seg = torch.randint(0, G, (S,), generator=g, device=dev, dtype=torch.int32)
+    resid, delta = inp["resid"], inp["delta"]
+    r0 = resid.clone()
+    normed = torch.full((S, D), SENT, dtype=torch.bfloat16, device=dev)
+    h3lib.mod_norm_residual_seg(resid, table, seg, delta=delta, gate_idx=2, shift_idx=3,
+                                scale_idx=4, normed=normed, L=L)
+    h3lib.check_device_error()
+    rows = np.arange(L) if L < 1000 else sample_rows(L, 512, 36)
+    tr = torch.from_numpy(rows).to(dev)
+    m = O.modulation_rows(np64(table), seg.cpu().numpy(), rows)
+    r_ref, h_ref = O.mod_norm_residual(np64(r0[tr]), np64(delta[tr]), m[:, 2], m[:, 3], m[:, 4])
+    assert_close_f32(np64(resid[tr]), r_ref, "resid (segmented)")
+    assert_close_bf16(np64(normed[tr]), h_ref, "normed (segmented)")
+    assert torch.equal(resid[L:], r0[L:]) and bool((normed[L:] == SENT).all())

@@ -261,25 +261,27 @@ def tiny_block(shape=None, seed=0):
     return shape, n
 
 
-def run_block(o, shape, n, rows=None, inter=False, **over):
+def run_block(o, shape, n, rows=None, inter=False, seg=None, **over):
     args = dict(n)
     args.update(over)
     return o.block_forward(args["resid"], args["mod"], args["w_qkv"], args["w_o"], args["w_gu"],
                            args["w_down"], args["q_gain"], args["k_gain"], args["pos"],
                            L=shape.L, heads=shape.H, head_dim=shape.Dh,
                            axis_dims=shape.axis_dims, theta=shape.theta, rows=rows,
-                           return_intermediates=inter)
+                           return_intermediates=inter, seg=seg)
 
 
-def torch_block(shape, n):
+def torch_block(shape, n, mod_rows=None):
     """The block written with torch float64 library routines (layer_norm,
     rms_norm, scaled_dot_product_attention, silu) and a complex-number RoPE,
-    with bf16 rounding at the same hand-off points. Returns every hand-off."""
+    with bf16 rounding at the same hand-off points. Returns every hand-off.
+    mod_rows: optional per-row modulation [L, 6, D] instead of n["mod"]."""
     T = lambda a: torch.from_numpy(np.asarray(a, np.float64))
     rb = lambda t: t.float().to(torch.bfloat16).double()
     L, D, H, Dh = shape.L, shape.D, shape.H, shape.Dh
     r = T(n["resid"])[:L]
-    mod = T(n["mod"])
+    m6 = T(n["mod"] if mod_rows is None else mod_rows)
+    mod = [m6[..., i, :] for i in range(6)]
     ln = lambda x: torch.nn.functional.layer_norm(x, (D,), eps=1e-6)
     h1 = rb(ln(r) * (1 + mod[1]) + mod[0])
     qkv = rb(h1 @ T(n["w_qkv"]).T)
@@ -346,6 +348,51 @@ def check_block(o):
 
 def test_block():
     check_block(O)
+
+
+def check_segmented_block(o):
+    shape, n = tiny_block()
+    out = run_block(o, shape, n)
+    # one table and every token in group 0 is the per-sample case, bit for bit
+    assert np.array_equal(run_block(o, shape, n, mod=n["mod"][None], seg=np.zeros(shape.S, int)),
+                          out)
+    g = rng(41)
+    seg = g.integers(0, 2, shape.S)
+    # two identical tables: the grouping does not matter
+    assert np.array_equal(run_block(o, shape, n, mod=np.stack([n["mod"], n["mod"]]), seg=seg),
+                          out)
+    # two different tables against the torch composition with per-row modulation
+    mod2 = np.stack([n["mod"], 0.3 * g.standard_normal(n["mod"].shape)])
+    out2, mids = run_block(o, shape, n, mod=mod2, seg=seg, inter=True)
+    ref = torch_block(shape, n, mod_rows=mod2[seg[:shape.L]])
+    for key in ("h1", "q", "k", "a", "o", "h2", "u", "f"):
+        assert close_bf16(mids[key], ref[key]), key
+    r_in = n["resid"][:shape.L]
+    assert close_bf16(out2 - r_in, ref["r"] - r_in), "segmented increment"
+    # relabelling the groups (tables swapped, ids flipped) changes nothing
+    assert np.array_equal(run_block(o, shape, n, mod=mod2[::-1].copy(), seg=1 - seg), out2)
+
+
+def test_segmented_block():
+    check_segmented_block(O)
+
+
+def test_stack_is_two_torch_blocks():
+    shape, n = tiny_block()
+    _, n2 = tiny_block(seed=9)
+    out = O.stack_forward(n["resid"], [n["mod"], n2["mod"]],
+                          [(n[k] for k in ("w_qkv", "w_o", "w_gu", "w_down")),
+                           (n2[k] for k in ("w_qkv", "w_o", "w_gu", "w_down"))],
+                          [n["q_gain"], n2["q_gain"]], [n["k_gain"], n2["k_gain"]], n["pos"],
+                          L=shape.L, heads=shape.H, head_dim=shape.Dh, axis_dims=shape.axis_dims,
+                          theta=shape.theta)
+    r1 = torch_block(shape, n)["r"]
+    nb = dict(n2)
+    nb["resid"] = np.concatenate([r1, n["resid"][shape.L:]])
+    nb["pos"] = n["pos"]
+    r2 = torch_block(shape, nb)["r"]
+    assert close_bf16(out, r2)
+    assert close_bf16(out - r1, r2 - r1), "second block's increment"
 
 
 # --------------------------------------------- planted mistakes are caught
@@ -424,6 +471,13 @@ def _unpack_gates_swapped(mod):
     return sh1, sc1, g2, sh2, sc2, g1
 
 
+def _modulation_rows_shifted(mod, seg, rows):
+    mod = np.asarray(mod, np.float64)
+    if seg is None:
+        return mod
+    return mod[np.roll(np.asarray(seg), 1)[np.asarray(rows)]]
+
+
 def _rms_no_eps_mean(x, gain, eps):
     x = np.asarray(x, np.float64)
     return x / np.sqrt((x * x).sum(-1, keepdims=True) + eps) * np.asarray(gain, np.float64)
@@ -443,9 +497,239 @@ def _rms_no_eps_mean(x, gain, eps):
     ("modulation shift/scale order", dict(unpack_mod=_unpack_shift_scale_swapped), ["check_block"]),
     ("modulation gates swapped", dict(unpack_mod=_unpack_gates_swapped), ["check_block"]),
     ("rmsnorm sum instead of mean", dict(rms_norm=_rms_no_eps_mean), ["check_rms_norm"]),
+    ("segment of the wrong row", dict(modulation_rows=_modulation_rows_shifted),
+     ["check_segmented_block"]),
 ])
 def test_planted_mistake_is_caught(name, mut, checks):
     m = _mutant(**mut)
     for c in checks:
         with pytest.raises(AssertionError):
             globals()[c](m)
+
+
+# ------------------------------------------------- GPU output preparation
+def check_frames_to_u8(o):
+    # closed-form points: -1 -> 0, 1 -> 255, 0 -> round(127.5) = 128 (half to
+    # even), out-of-range values clamp, NaN-free inputs only
+    x = np.array([-1.0, 1.0, 0.0, -3.0, 2.5, 0.5, -0.5], np.float32).reshape(1, 1, 1, 1, 7)
+    assert o.frames_to_u8(x).reshape(-1).tolist() == [0, 255, 128, 0, 255, 191, 64]
+    # layout: channel moves last, every other axis keeps its order
+    g = rng(50)
+    f = g.uniform(-1, 1, size=(2, 3, 4, 5, 6)).astype(np.float32)
+    u = o.frames_to_u8(f)
+    assert u.shape == (2, 4, 5, 6, 3) and u.dtype == np.uint8
+    b, c, t, h, w = 1, 2, 3, 4, 5
+    one = o.frames_to_u8(f[b:b + 1, c:c + 1, t:t + 1, h:h + 1, w:w + 1]).reshape(())
+    assert u[b, t, h, w, c] == one
+    # library pin: torch float32 arithmetic on the same steps
+    tt = torch.from_numpy(f)
+    ref = ((tt * 0.5 + 0.5).clamp(0, 1) * 255).round().to(torch.uint8).permute(0, 2, 3, 4, 1)
+    assert np.array_equal(u, ref.contiguous().numpy())
+    # monotone in x
+    ramp = np.linspace(-1.2, 1.2, 10001, dtype=np.float32).reshape(1, 1, 1, 1, -1)
+    assert np.all(np.diff(o.frames_to_u8(ramp).reshape(-1).astype(int)) >= 0)
+
+
+def test_frames_to_u8():
+    check_frames_to_u8(O)
+
+
+def _frames_wrong_axis(frames):
+    x = np.asarray(frames, np.float32)
+    v = np.rint(np.clip(x * np.float32(0.5) + np.float32(0.5), 0, 1) * np.float32(255))
+    return np.ascontiguousarray(np.moveaxis(v.astype(np.uint8), 2, -1))
+
+
+def _frames_truncating(frames):
+    x = np.asarray(frames, np.float32)
+    v = np.floor(np.clip(x * np.float32(0.5) + np.float32(0.5), 0, 1) * np.float32(255))
+    return np.ascontiguousarray(np.moveaxis(v.astype(np.uint8), 1, -1))
+
+
+@pytest.mark.parametrize("mut", [_frames_wrong_axis, _frames_truncating])
+def test_planted_output_prep_mistake_is_caught(mut):
+    with pytest.raises(AssertionError):
+        check_frames_to_u8(_mutant(frames_to_u8=mut))
+
+
+# ------------------------------------------------------ online FP8 projections
+def check_fp8(o):
+    # hand-derived E4M3 points: 1 + 1/16 ties to 1 (even), 1 + 3/16 ties to
+    # 1.25 (even), 2^-10 ties to 0, 3 * 2^-10 ties to 2^-8, 500 saturates to 448
+    pts = np.array([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 500.0, -500.0, 2.0 ** -9, 240.0])
+    assert o.round_e4m3(pts).tolist() == [1.0, 1.25, 0.0, 2.0 ** -8, 448.0, -448.0, 2.0 ** -9,
+                                          240.0]
+    # library pin: torch's float32 -> float8_e4m3fn cast inside the finite range
+    x = (rng(60).standard_normal(20000) * 50).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(o.round_e4m3(x.astype(np.float64)), ref)
+    # per-row absmax: the row maximum maps to +-448 exactly, a zero row to 0
+    xs = bf16_values(rng(61).standard_normal((5, 64)) * 3)
+    xs[3] = 0
+    q, s = o.quantize_fp8_rows(xs)
+    am = np.abs(xs).max(1)
+    for i in (0, 1, 2, 4):
+        assert np.max(np.abs(q[i])) == 448.0
+        assert s[i] == np.float32(np.float32(am[i]) / np.float32(448))
+    assert np.all(q[3] == 0) and s[3] == 0
+    # dequantisation error is at most half an E4M3 step (relative 2^-4) per value
+    err = np.abs(q * s[:, None] - xs)
+    assert np.all(err <= np.abs(xs) * 2.0 ** -4 + s[:, None] * 2.0 ** -9 + 1e-12)
+    # the product: integer codes with unit scales give the exact integer product
+    qa = rng(62).integers(-4, 5, size=(4, 32)).astype(np.float64)
+    qb = rng(63).integers(-4, 5, size=(6, 32)).astype(np.float64)
+    exact = np.array([[sum(qa[i, k] * qb[j, k] for k in range(32)) for j in range(6)]
+                      for i in range(4)])
+    assert np.array_equal(o.linear_fp8(qa, np.ones(4), qb, np.ones(6)), exact)
+    # the row and column scales multiply the product
+    sa, sb = np.array([1, 2, 4, 0.5]), np.array([1, 1, 2, 2, 8, 0.25])
+    assert np.array_equal(o.linear_fp8(qa, sa, qb, sb),
+                          o.round_bf16(exact * sa[:, None] * sb[None, :]))
+
+
+def test_fp8():
+    check_fp8(O)
+
+
+def _e4m3_truncating(x):
+    x = np.asarray(x, np.float64)
+    out = np.zeros_like(x)
+    nz = x != 0
+    _, e = np.frexp(x[nz])
+    step = np.exp2(np.maximum(e - 4, -9).astype(np.float64))
+    out[nz] = np.clip(np.trunc(x[nz] / step) * step, -448, 448)
+    return out
+
+
+def _linear_fp8_no_row_scale(qx, sx, qw, sw):
+    acc = np.asarray(qx, np.float64) @ np.asarray(qw, np.float64).T
+    return O.round_bf16(acc * np.asarray(sw, np.float64)[None, :])
+
+
+@pytest.mark.parametrize("mut", [dict(round_e4m3=_e4m3_truncating),
+                                 dict(linear_fp8=_linear_fp8_no_row_scale)])
+def test_planted_fp8_mistake_is_caught(mut):
+    with pytest.raises(AssertionError):
+        check_fp8(_mutant(**mut))
+
+
+def test_fp8_block_close_to_bf16_block():
+    # the FP8 block differs from the BF16 block only by the E4M3 rounding of the
+    # four projection operands (relative step 2^-4): its hand-offs stay within
+    # a few percent of the BF16 ones, and integer-valued weights and inputs that
+    # E4M3 holds exactly give the same projections
+    shape, n = tiny_block()
+    out, mids = run_block(O, shape, n, inter=True)
+    out8, mids8 = O.block_forward(n["resid"], n["mod"], n["w_qkv"], n["w_o"], n["w_gu"],
+                                  n["w_down"], n["q_gain"], n["k_gain"], n["pos"], L=shape.L,
+                                  heads=shape.H, head_dim=shape.Dh, axis_dims=shape.axis_dims,
+                                  theta=shape.theta, return_intermediates=True, fp8=True)
+    for key in ("q", "a", "o", "u", "f"):
+        assert rel_l2_(mids8[key], mids[key]) < 0.08, key
+    assert 0 < rel_l2_(mids8["f"], mids["f"])  # the FP8 path is really taken
+    r_in = n["resid"][:shape.L]
+    assert rel_l2_(out8 - r_in, out - r_in) < 0.08
+
+
+def rel_l2_(x, ref):
+    return float(np.linalg.norm(np.asarray(x) - np.asarray(ref)) / np.linalg.norm(ref))
+
+
+def check_attention_skip(o):
+    r = rng(70)
+    S = L = 384
+    H = 2
+    q = bf16_values(r.standard_normal((S, H, 16)))
+    k = bf16_values(r.standard_normal((S, H, 16)))
+    v = bf16_values(r.standard_normal((S, H, 16)))
+    dense = o.attention(q, k, v, L, 0.25)
+    # eps = 0 keeps every tile and is dense attention
+    out0, kept0 = o.attention_skip(q, k, v, L, 0.25, 0.0)
+    assert kept0.all() and np.allclose(out0, dense, rtol=2 ** -8, atol=1e-12)
+    # a key tile pushed far below every score is skipped for every query tile,
+    # and the result is attention over the other keys
+    k2 = k.copy()
+    q2 = np.abs(q) + 0.5
+    k2[128:256] = -np.abs(k2[128:256]) - 8.0
+    out, kept = o.attention_skip(q2, k2, v, L, 0.25, 2.0 ** -20)
+    assert (~kept[:, :, 1]).all() and kept[:, :, [0, 2]].all()
+    keep = np.r_[0:128, 256:384]
+    sub = np.empty((L, H, 16))
+    for h in range(H):
+        z = (q2[:, h] @ k2[keep, h].T) * 0.25
+        sub[:, h] = torch.softmax(torch.from_numpy(z), dim=1).numpy() @ v[keep, h]
+    assert np.allclose(out, sub, rtol=2 ** -7, atol=1e-12)
+    # the first key tile is never skipped (no running maximum yet)
+    k3 = k.copy()
+    k3[:128] = -np.abs(k3[:128]) - 8.0
+    _, kept3 = o.attention_skip(q2, k3, v, L, 0.25, 2.0 ** -20)
+    assert kept3[:, :, 0].all()
+
+
+def test_attention_skip():
+    check_attention_skip(O)
+
+
+def check_sage(o):
+    r = rng(80)
+    S = L = 300
+    H, Dh = 2, 32
+    q = bf16_values(r.standard_normal((S, H, Dh)))
+    k = bf16_values(r.standard_normal((S, H, Dh)) + 3.0)  # a large common offset
+    v = bf16_values(r.standard_normal((S, H, Dh)))
+    ops = o.sage_quantize(q, k, v, L)
+    # smoothing removes the per-channel mean (up to its bf16 rounding)
+    assert np.allclose(ops["k_mean"], k.mean(0), atol=2 ** -6 * 4)
+    # dequantised operands are within half an E4M3 step of the originals
+    for c, s, x, kind in ((ops["qc"], ops["sq"], q, "q"), (ops["kc"], ops["sk"],
+                          k - ops["k_mean"][None], "k")):
+        deq = c * np.repeat(s.astype(np.float64), 128, axis=0)[:L][:, :, None]
+        assert np.all(np.abs(deq - x) <= np.abs(x) * 2.0 ** -4 + 2.0 ** -9 * np.max(np.abs(x)) + 1e-12), kind
+    deq_v = ops["vc"] * ops["sv"][None].astype(np.float64)
+    assert np.all(np.abs(deq_v - v) <= np.abs(v) * 2.0 ** -4 + 2.0 ** -9 * np.abs(v).max(0) + 1e-12)
+    # the FP8 result stays close to dense attention: per-element E4M3 noise on
+    # P and V is about 2^-4 / sqrt(3) each, ~5 % of the output for random V
+    scale = Dh ** -0.5
+    dense = o.attention(q, k, v, L, scale)
+    out = o.attention_sage(ops, L, scale)
+    assert np.linalg.norm(out - dense) / np.linalg.norm(dense) < 0.1
+    # identical keys: every p is exactly 1 (an E4M3 value), so the output is
+    # the mean of the dequantised V rows
+    kk = np.broadcast_to(k[:1], k.shape).copy()
+    opu = o.sage_quantize(q, kk, v, L)
+    deq_v = opu["vc"] * opu["sv"][None].astype(np.float64)
+    assert np.allclose(o.attention_sage(opu, L, scale), o.round_bf16(deq_v.mean(0))[None].repeat(L, 0),
+                       rtol=2 ** -8, atol=1e-12)
+    # one key far above the others: its p is 1, every other p underflows the
+    # E4M3 range (< 2^-10) and the row sum is 1 up to 2^-20, so the output is
+    # that key's dequantised V row
+    kd = np.zeros_like(k)
+    kd[7] = 8.0
+    qd = np.ones_like(q)
+    opd = o.sage_quantize(qd, kd, v, L)
+    deq_vd = opd["vc"] * opd["sv"][None].astype(np.float64)
+    assert np.allclose(o.attention_sage(opd, L, 1.0), np.broadcast_to(o.round_bf16(deq_vd[7]), (L, H, Dh)),
+                       rtol=2 ** -7, atol=1e-12)
+    # smoothing is exact in the score: with exactly representable operands and
+    # unit-like scales the smoothed scores differ from q.k by one row constant
+    s_full = q[:, 0] @ k[:, 0].T
+    s_smooth = q[:, 0] @ (k[:, 0] - ops["k_mean"][0]).T
+    d = s_full - s_smooth
+    assert np.allclose(d, d[:, :1], atol=1e-9)
+
+
+def test_sage():
+    check_sage(O)
+
+
+def _sage_no_smoothing(q, k, v, L, tile=128):
+    ops = O.sage_quantize(q, k, v, L, tile)
+    ops2 = O.sage_quantize(q, k, v, L, tile)
+    ops2["k_mean"] = np.zeros_like(ops["k_mean"])
+    return ops2
+
+
+def test_planted_sage_mistake_is_caught():
+    with pytest.raises(AssertionError):
+        check_sage(_mutant(sage_quantize=_sage_no_smoothing))
