@@ -277,10 +277,34 @@ def measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk):
     ms = timeit(lambda: h3.block_forward_fp8(cfg, w8, r, inp["mod"], inp["pos"], ws8), 3)
     out["fp8_block"] = {"ms": round(ms, 3), "note": "four projections in FP8 E4M3 with per-row "
                         "scales; attention and elementwise steps as in the BF16 block"}
+    ms = timeit(lambda: h3.block_forward_fp8(cfg, w8, r, inp["mod"], inp["pos"], ws8,
+                                             fp8_attention=True), 3)
+    out["fp8_block_fp8_attention"] = {"ms": round(ms, 3), "note": "FP8 projections and FP8 "
+                                      "(SAGE-style) attention"}
     del ws8, w8
     mods = torch.stack([inp["mod"]] * 4).contiguous()
     ms = timeit(lambda: h3.stack_forward(cfg, [inp] * 4, r, mods, inp["pos"], ws), 1)
     out["stack4"] = {"ms_per_block": round(ms / 4, 3)}
+    # length sweep of a 4-block stack (independent seeded weights per block),
+    # buffers padded to a multiple of 64: ms per block and TFLOP/s vs length
+    del ws
+    sweep = []
+    from dit_transformer_block_gb300 import inputs as I
+    for L_s, grid in ((29034, (16, 24, 79)), (58758, (31, 24, 79)), (87846, (47, 24, 79))):
+        S_s = (L_s + 63) // 64 * 64
+        sh = I.BlockShape(S=S_s, L=L_s, D=shape.D, H=shape.H, Dh=shape.Dh, F=shape.F,
+                          axis_dims=shape.axis_dims, pos_kind="3d", grid=grid)
+        blocks = [I.block_inputs(sh, seed=4 + b, device=r.device) for b in range(4)]
+        cfg_s = h3.block_config(sh.S, sh.L, sh.D, sh.H, sh.Dh, sh.F, sh.axis_dims)
+        ws_s = torch.empty(h3.block_workspace_bytes(cfg_s), dtype=torch.uint8, device=r.device)
+        mods = torch.stack([b["mod"] for b in blocks]).contiguous()
+        rs = blocks[0]["resid"].clone()
+        ms = timeit(lambda: h3.stack_forward(cfg_s, blocks, rs, mods, blocks[0]["pos"], ws_s), 1)
+        w = block_work(sh.S, sh.L, sh.D, sh.H, sh.Dh, sh.F)
+        sweep.append({"L": L_s, "S": S_s, "ms_per_block": round(ms / 4, 3),
+                      "tflops": round((w["attn_flop"] + w["gemm_flop"]) / (ms / 4) / 1e9, 1)})
+        del blocks, ws_s, rs, mods
+    out["length_sweep_stack4"] = sweep
     f = torch.randn(1, 3, 243, 768, 1344, device=r.device).clamp_(-1.2, 1.2)
     o = torch.empty(1, 243, 768, 1344, 3, dtype=torch.uint8, device=r.device)
     ms = timeit(lambda: h3.frames_to_u8(f, o), 5)

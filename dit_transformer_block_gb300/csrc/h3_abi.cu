@@ -308,6 +308,54 @@ h3_status h3_attention_varlen_skip(const void* q, const void* k, const void* v, 
                           reinterpret_cast<cudaStream_t>(stream), skip_eps);
 }
 
+size_t h3_sage_scratch_bytes(int L, int H) {
+  clear_error();
+  if (L < 0 || H <= 0) return 0;
+  return sage_scratch_bytes(L, H);
+}
+
+h3_status h3_sage_quantize(const void* q, const void* k, const void* v, int S, int L, int H,
+                           int Dh, void* qc, void* kc, void* vc, float* sq, float* sk, float* sv,
+                           float* k_mean, void* scratch, size_t scratch_bytes,
+                           h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(q && k && v && qc && kc && vc && sq && sk && sv && k_mean, H3_ERR_INVALID_ARG,
+             "a required pointer is NULL");
+  H3_REQUIRE(Dh == 128, H3_ERR_UNSUPPORTED, "head_dim %d unsupported (128 only)", Dh);
+  H3_REQUIRE(H > 0 && H <= 65535, H3_ERR_INVALID_ARG, "H=%d", H);
+  H3_REQUIRE(scratch != nullptr && scratch_bytes >= sage_scratch_bytes(L, H), H3_ERR_WORKSPACE,
+             "scratch of %zu bytes given, %zu needed", scratch_bytes, sage_scratch_bytes(L, H));
+  H3_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(qc) && aligned16(kc) &&
+                 aligned16(vc) && aligned16(sv) && aligned16(scratch),
+             H3_ERR_MISALIGNED, "operands, codes, sv and scratch must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  const int64_t ld = static_cast<int64_t>(H) * Dh;
+  return launch_sage_quantize(q, k, v, ld, L, H, static_cast<uint8_t*>(qc),
+                              static_cast<uint8_t*>(kc), static_cast<uint8_t*>(vc), ld, sq, sk, sv,
+                              k_mean, scratch, reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_attention_fp8(const void* qc, const void* kc, const void* vc, const float* sq,
+                           const float* sk, const float* sv, void* o, int S, int L, int H,
+                           int Dh, float softmax_scale, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(qc && kc && vc && sq && sk && sv && o, H3_ERR_INVALID_ARG,
+             "a required pointer is NULL");
+  H3_REQUIRE(Dh == 128, H3_ERR_UNSUPPORTED, "head_dim %d unsupported (128 only)", Dh);
+  H3_REQUIRE(H > 0 && H <= 65535, H3_ERR_INVALID_ARG, "H=%d", H);
+  H3_REQUIRE(softmax_scale > 0.f, H3_ERR_INVALID_ARG, "softmax_scale must be > 0");
+  H3_REQUIRE(aligned16(qc) && aligned16(kc) && aligned16(vc) && aligned16(o), H3_ERR_MISALIGNED,
+             "codes and o must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  const int64_t ld = static_cast<int64_t>(H) * Dh;
+  return launch_attention_fp8(qc, kc, vc, ld, sq, sk, sv, o, ld, L, H, softmax_scale,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
 h3_status h3_swiglu(const void* gate_up, void* out, int S, int L, int F, h3_stream_t stream) {
   clear_error();
   h3_status st = check_rows(S, L);
@@ -637,18 +685,30 @@ h3_status h3_linear_swiglu_fp8(const void* qx, const float* sx, const void* qw_g
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
-// FP8 block workspace: the BF16 block's slices, then one FP8 code buffer
-// [S, max(D, F)] and one scale vector [S].
+// FP8 block workspace: the BF16 block's slices, one FP8 code buffer
+// [S, max(D, F)] and one scale vector [S] for the projections, then the FP8
+// attention operands (codes of q, k, v [S, D] each, tile scales sq, sk
+// [ceil(L/128), H], channel scales sv and the K mean [H, 128], scratch).
 struct BlockWsFp8 {
   BlockWs bf;
-  size_t codes, scales, total;
+  size_t codes, scales, aq, ak, av, sq, sk, sv, kmean, scratch, total;
 };
 static BlockWsFp8 block_ws_fp8(const h3_block_config* c) {
   BlockWsFp8 w;
   w.bf = block_ws(c);
+  const size_t S = static_cast<size_t>(c->S), D = static_cast<size_t>(c->D);
+  const size_t tiles = (static_cast<size_t>(c->L) + 127) / 128 + 1;
   size_t off = w.bf.total;
-  w.codes = off;  off += align256(static_cast<size_t>(c->S) * std::max(c->D, c->F));
-  w.scales = off; off += align256(static_cast<size_t>(c->S) * 4);
+  w.codes = off;   off += align256(S * std::max(c->D, c->F));
+  w.scales = off;  off += align256(S * 4);
+  w.aq = off;      off += align256(S * D);
+  w.ak = off;      off += align256(S * D);
+  w.av = off;      off += align256(S * D);
+  w.sq = off;      off += align256(tiles * c->H * 4);
+  w.sk = off;      off += align256(tiles * c->H * 4);
+  w.sv = off;      off += align256(D * 4);
+  w.kmean = off;   off += align256(D * 4);
+  w.scratch = off; off += align256(sage_scratch_bytes(c->L, c->H));
   w.total = off;
   return w;
 }
@@ -665,7 +725,8 @@ size_t h3_block_workspace_bytes_fp8(const h3_block_config* cfg) {
 
 h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weights_fp8* w,
                                float* resid, const float* mod, const int32_t* pos,
-                               void* workspace, size_t workspace_bytes, h3_stream_t stream) {
+                               int fp8_attention, void* workspace, size_t workspace_bytes,
+                               h3_stream_t stream) {
   clear_error();
   h3_status st = check_block_config(cfg);
   if (st != H3_OK) return st;
@@ -701,6 +762,23 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
   auto quant = [&](const void* x, int K) {
     return launch_quantize_fp8_rows(x, K, codes, K, sc, L, K, s);
   };
+  const float sm_scale = 1.0f / sqrtf(static_cast<float>(cfg->Dh));
+  auto attention = [&](uint8_t* qkv_, void* out) -> h3_status {
+    if (!fp8_attention)
+      return launch_attention(qkv_, qkv_ + 2LL * D, qkv_ + 4LL * D, ld_qkv, out, D, L, H,
+                              sm_scale, s);
+    uint8_t* aq = base + ws.aq;
+    uint8_t* ak = base + ws.ak;
+    uint8_t* av = base + ws.av;
+    float* sq = reinterpret_cast<float*>(base + ws.sq);
+    float* sk = reinterpret_cast<float*>(base + ws.sk);
+    float* sv = reinterpret_cast<float*>(base + ws.sv);
+    float* km = reinterpret_cast<float*>(base + ws.kmean);
+    h3_status r = launch_sage_quantize(qkv_, qkv_ + 2LL * D, qkv_ + 4LL * D, ld_qkv, L, H, aq, ak,
+                                       av, D, sq, sk, sv, km, base + ws.scratch, s);
+    if (r != H3_OK) return r;
+    return launch_attention_fp8(aq, ak, av, D, sq, sk, sv, out, D, L, H, sm_scale, s);
+  };
   if ((st = launch_mod_norm_residual(resid, nullptr, nullptr, m, m + D, h, L, D, cfg->eps_ln,
                                      s)) != H3_OK ||
       (st = quant(h, D)) != H3_OK ||
@@ -708,8 +786,7 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
                             GEMM_STORE_BF16, s)) != H3_OK ||
       (st = launch_qk_norm_rope(qkv, qkv + 2LL * D, ld_qkv, w->q_gain, w->k_gain, pos,
                                 cfg->axis_dims, L, H, cfg->theta, cfg->eps_qk, s)) != H3_OK ||
-      (st = launch_attention(qkv, qkv + 2LL * D, qkv + 4LL * D, ld_qkv, attn, D, L, H,
-                             1.0f / sqrtf(static_cast<float>(cfg->Dh)), s)) != H3_OK ||
+      (st = attention(qkv, attn)) != H3_OK ||
       (st = quant(attn, D)) != H3_OK ||
       (st = launch_gemm_fp8(codes, D, sc, w->w_o, D, w->s_o, proj, D, L, D, D, GEMM_STORE_BF16,
                             s)) != H3_OK ||

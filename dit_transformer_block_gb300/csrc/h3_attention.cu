@@ -26,6 +26,7 @@
 // Both query tiles read every K/V tile from shared memory, which halves the
 // shared-memory operand traffic per FLOP of a one-tile-per-CTA design.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 
@@ -38,6 +39,7 @@ constexpr int BQ = 128, BKV = 128, DH = 128;
 constexpr int TILE_BYTES = BQ * DH * 2;        // 32 KB (two 64-column boxes)
 constexpr int BOX_BYTES = TILE_BYTES / 2;      // 16 KB
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units (factor 256)
+constexpr float kLog2P8Scale = 7.807354922057604f;  // log2(224): FP8 P scale
 
 struct AttnArgs {
   __nv_bfloat16* o;
@@ -45,8 +47,14 @@ struct AttnArgs {
   int L;
   int num_kv;
   float scale_log2;  // softmax_scale * log2(e)
-  int skip;          // Skip-Softmax on
-  float skip_log2;   // skip a key tile when every row's tile max < m - skip_log2
+  float skip_log2;   // Skip-Softmax: skip a key tile when every row's tile max < m - skip_log2
+  // FP8 operands: score multiplier of (query tile t, key tile j, head h) is
+  // sq[t * H + h] * sk[j * H + h]; output column d of head h is scaled by
+  // sv[h * 128 + d].
+  const float* sq;
+  const float* sk;
+  const float* sv;
+  int H;
   DevErr err;
 };
 
@@ -63,8 +71,12 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
 // row's tile maximum lies more than skip_log2 below its running maximum the
 // tile is skipped (no exp2, no P; flags[quarter] tells the MMA warp to leave
 // out its P V product) and the function returns true.
+// F8: P is written as E4M3 codes (four per column, 32 columns) and the
+// running max is kept an integer, so every P is an exact power-of-two multiple
+// of the P against any other integer reference.
+template <bool F8, bool SKIP>
 __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid, bool o_live,
-                                             float scale_log2, float& m, float& l, int skip,
+                                             float scale_log2, float& m, float& l,
                                              float skip_log2, volatile uint32_t* flags,
                                              int bar_id) {
   uint32_t sr[128];
@@ -97,7 +109,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
     md = max3f(md, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
   }
   const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
-  if (skip) {
+  if constexpr (SKIP) {
     const bool row_skip = mx < m - skip_log2;  // never on the first tile (m = -inf)
     const uint32_t warp_skip = __all_sync(0xffffffffu, row_skip) ? 1u : 0u;
     const int quarter = (threadIdx.x >> 5) & 3;
@@ -108,9 +120,11 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
   // Raise the running max only when it is exceeded by more than the
   // threshold; the decision is warp-uniform because the O rescale uses
   // warp-collective TMEM loads and stores.
-  const bool need = mx > m + RESCALE_THRESHOLD;
+  // FP8: the running max stays within 1 (log2) of the true one, so P <= 2
+  // and 224 * P fits E4M3 (max 448) with small P still in its normal range.
+  const bool need = mx > m + (F8 ? 1.0f : RESCALE_THRESHOLD);
   if (__any_sync(0xffffffffu, need)) {
-    const float m_new = fmaxf(m, mx);
+    const float m_new = F8 ? ceilf(fmaxf(m, mx)) : fmaxf(m, mx);
     const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
     l *= alpha;
     if (o_live) {
@@ -129,25 +143,49 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
   }
   // p = exp2(s * scale_log2 - m): one packed FMA per pair, two exp2, one
   // packed add into the row sum, one bf16x2 pack written over S.
-  const float neg_m = -m;
+  // FP8: P is carried as 224 * P (log2 224 added to the exponent); O and the
+  // row sum carry the same factor, which cancels in O / l.
+  const float neg_m = F8 ? (kLog2P8Scale - m) : -m;
   float la = 0.f, lb = 0.f, lc = 0.f, ld = 0.f;
+  if constexpr (F8) {
+    uint32_t pk[32];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float x0, x1;
-      ffma2_bc(x0, x1, __uint_as_float(sr[c * 32 + 2 * i]), __uint_as_float(sr[c * 32 + 2 * i + 1]),
-               scale_log2, neg_m);
-      const float p0 = ex2_approx(x0);
-      const float p1 = ex2_approx(x1);
-      if (i & 1)
-        fadd2(lc, ld, p0, p1);
-      else
-        fadd2(la, lb, p0, p1);
-      pk[i] = pack_bf16x2(p0, p1);
+    for (int i = 0; i < 32; ++i) {
+      float x0, x1, x2, x3;
+      ffma2_bc(x0, x1, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]), scale_log2,
+               neg_m);
+      ffma2_bc(x2, x3, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]), scale_log2,
+               neg_m);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+      fadd2(la, lb, p0, p1);
+      fadd2(lc, ld, p2, p3);
+      const uint32_t lo =
+          __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi =
+          __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
+      pk[i] = lo | (hi << 16);
     }
-    tmem_st16(tS + c * 16, pk);
+    tmem_st32(tS, pk);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float x0, x1;
+        ffma2_bc(x0, x1, __uint_as_float(sr[c * 32 + 2 * i]),
+                 __uint_as_float(sr[c * 32 + 2 * i + 1]), scale_log2, neg_m);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        if (i & 1)
+          fadd2(lc, ld, p0, p1);
+        else
+          fadd2(la, lb, p0, p1);
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      tmem_st16(tS + c * 16, pk);
+    }
   }
   l += (la + lb) + (lc + ld);
   tmem_st_wait();
@@ -155,8 +193,9 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
 }
 
 // Normalises the thread's O row by 1/l and stores it (bf16) when row_ok.
+// col_scale (FP8 operands): per-column factor of this head's output, or NULL.
 __device__ __forceinline__ void store_o_row(uint32_t tO, float l, __nv_bfloat16* orow,
-                                            bool row_ok) {
+                                            bool row_ok, const float* col_scale) {
   const float inv_l = 1.0f / l;
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
@@ -164,6 +203,11 @@ __device__ __forceinline__ void store_o_row(uint32_t tO, float l, __nv_bfloat16*
     tmem_ld32(tO + c * 32, ov);
     tmem_ld_wait();
     tmem_reg_fence(ov);
+    if (col_scale != nullptr) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * __ldg(col_scale + c * 32 + i));
+    }
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
@@ -204,16 +248,24 @@ enum Bar2 {
 // barriers, the TMEM address word (padded to 16 bytes) and 16 vote flags
 static_assert(B2_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
 
+// F8: Q, K and V are E4M3 codes (one 128-byte TMA box per 128-row tile, 16
+// KB), the MMAs are kind::f8f6f4 (K = 32 per instruction), P is written to
+// TMEM as E4M3 and read back by the PV product, scores are scaled per (query
+// tile, key tile) and the output per channel.
+// SKIP: Skip-Softmax compiled in (a separate kernel, so the dense kernel
+// carries none of its votes or branches).
+template <bool F8, bool SKIP>
 __global__ void __launch_bounds__(Q2_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ,
-                        const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  constexpr int T_BYTES = F8 ? TILE_BYTES / 2 : TILE_BYTES;  // one Q/K/V tile in smem
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sKV = smem;                              // KV_SLOTS x 32 KB
-  uint8_t* sQ = smem + KV_SLOTS * TILE_BYTES;       // 2 x 32 KB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * TILE_BYTES);
+  uint8_t* sKV = smem;                            // KV_SLOTS tiles
+  uint8_t* sQ = smem + KV_SLOTS * T_BYTES;        // 2 tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * T_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B2_NUM);
   // Skip-Softmax votes: [tile][parity of j][quarter]
   volatile uint32_t* skip_flags = tmem_slot + 4;
@@ -244,11 +296,12 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(bar(B2_Q), 2 * TILE_BYTES);
+      mbar_arrive_expect_tx(bar(B2_Q), 2 * T_BYTES);
       for (int i = 0; i < 2; ++i) {
-        tma_load_2d(smem_u32(sQ + i * TILE_BYTES), &tmQ, bar(B2_Q), col0, q0 + i * BQ);
-        tma_load_2d(smem_u32(sQ + i * TILE_BYTES + BOX_BYTES), &tmQ, bar(B2_Q), col0 + 64,
-                    q0 + i * BQ);
+        tma_load_2d(smem_u32(sQ + i * T_BYTES), &tmQ, bar(B2_Q), col0, q0 + i * BQ);
+        if constexpr (!F8)
+          tma_load_2d(smem_u32(sQ + i * T_BYTES + BOX_BYTES), &tmQ, bar(B2_Q), col0 + 64,
+                      q0 + i * BQ);
       }
       for (int t = 0; t < 2 * n; ++t) {  // even t: K_{t/2}, odd t: V_{t/2}
         const int slot = t % KV_SLOTS;
@@ -256,18 +309,20 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         if (!mbar_wait(bar(B2_KV_EMPTY + slot), (use & 1u) ^ 1u, a.err, ERR_WAIT_ATTN_PRODUCER))
           break;
         const uint32_t full = bar(B2_KV_FULL + slot);
-        mbar_arrive_expect_tx(full, TILE_BYTES);
+        mbar_arrive_expect_tx(full, T_BYTES);
         const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
-        uint8_t* dst = sKV + slot * TILE_BYTES;
+        uint8_t* dst = sKV + slot * T_BYTES;
         tma_load_2d(smem_u32(dst), m, full, col0, (t >> 1) * BKV);
-        tma_load_2d(smem_u32(dst + BOX_BYTES), m, full, col0 + 64, (t >> 1) * BKV);
+        if constexpr (!F8)
+          tma_load_2d(smem_u32(dst + BOX_BYTES), m, full, col0 + 64, (t >> 1) * BKV);
       }
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(BQ, BKV, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BQ, DH, true);
+      constexpr uint32_t idesc_qk = F8 ? idesc_e4m3_f32(BQ, BKV) : idesc_bf16_f32(BQ, BKV, false);
+      constexpr uint32_t idesc_pv =
+          F8 ? (idesc_e4m3_f32(BQ, DH) | (1u << 16)) : idesc_bf16_f32(BQ, DH, true);
       const uint32_t kv_addr = smem_u32(sKV), q_addr = smem_u32(sQ);
       auto slot_of = [](int t) { return t % KV_SLOTS; };
       auto wait_full = [&](int t) {
@@ -275,26 +330,44 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
                          static_cast<uint32_t>(t / KV_SLOTS) & 1u, a.err, ERR_WAIT_ATTN_MMA);
       };
       auto qk = [&](int i, int j) {  // S_i = Q_i K_j^T
-        const uint32_t k_addr = kv_addr + slot_of(2 * j) * TILE_BYTES;
-        const uint32_t qa = q_addr + i * TILE_BYTES;
+        const uint32_t k_addr = kv_addr + slot_of(2 * j) * T_BYTES;
+        const uint32_t qa = q_addr + i * T_BYTES;
+        if constexpr (F8) {
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + i * 128, sdesc_sw128(qa + off, 16, 1024),
-                 sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)  // 32 codes = 32 bytes per step
+            mma_ss_f8(tmem + i * 128, sdesc_sw128(qa + kk * 32, 16, 1024),
+                      sdesc_sw128(k_addr + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+            mma_ss(tmem + i * 128, sdesc_sw128(qa + off, 16, 1024),
+                   sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(bar(B2_S + i));
       };
       auto pv = [&](int i, int j) {  // O_i += P_i V_j (left out when the tile was skipped)
-        const uint32_t v_addr = kv_addr + slot_of(2 * j + 1) * TILE_BYTES;
+        const uint32_t v_addr = kv_addr + slot_of(2 * j + 1) * T_BYTES;
         volatile uint32_t* f = skip_flags + (i * 2 + (j & 1)) * 4;
-        const bool skipped = a.skip && (f[0] & f[1] & f[2] & f[3]);
+        const bool skipped = SKIP && (f[0] & f[1] & f[2] & f[3]);
+        if (!skipped) {
+          if constexpr (F8) {
+            // 32 keys per step: 32 rows of 128 bytes = 4 KB further; P codes
+            // take 8 TMEM columns per step
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          if (!skipped)
-          mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
-                 sdesc_sw128(v_addr + kk * 2048, BOX_BYTES, 1024), idesc_pv,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts_f8(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
+                        sdesc_sw128(v_addr + kk * 4096, T_BYTES, 1024), idesc_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk)
+              mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
+                     sdesc_sw128(v_addr + kk * 2048, BOX_BYTES, 1024), idesc_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
         mma_commit(bar(B2_O + i));
       };
       bool ok = mbar_wait(bar(B2_Q), 0, a.err, ERR_WAIT_ATTN_MMA) && wait_full(0);
@@ -334,6 +407,11 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
     const uint32_t tO = tmem + lane_base + 256 + tile * 128;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    float sq_tile = 1.f;
+    if constexpr (F8) {
+      const int qt = blockIdx.x * 2 + tile;  // 128-row query tile index
+      sq_tile = (qt * BQ < a.L) ? __ldg(a.sq + qt * a.H + blockIdx.y) : 0.f;
+    }
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait(bar(B2_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
                      ERR_WAIT_ATTN_SOFTMAX)) {
@@ -341,8 +419,12 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         break;
       }
       tc_fence_after();
-      softmax_tile(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l, a.skip, a.skip_log2,
-                   skip_flags + (tile * 2 + (j & 1)) * 4, 1 + tile);
+      float mul = a.scale_log2;
+      // a zero tile scale would turn masked (-inf) scores into NaN: keep the
+      // multiplier positive
+      if constexpr (F8) mul = fmaxf(mul * sq_tile * __ldg(a.sk + j * a.H + blockIdx.y), 1e-30f);
+      softmax_tile<F8, SKIP>(tS, tO, a.L - j * BKV, j > 0, mul, m, l, a.skip_log2,
+                             skip_flags + (tile * 2 + (j & 1)) * 4, 1 + tile);
       tc_fence_before();
       mbar_arrive(bar(B2_P + tile));
     }
@@ -350,7 +432,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
                         ERR_WAIT_ATTN_SOFTMAX)) {
       tc_fence_after();
       const int row = q0 + tile * BQ + quarter * 32 + lane;
-      store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L);
+      store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L,
+                  F8 ? a.sv + blockIdx.y * DH : nullptr);
     }
   }
 
@@ -364,29 +447,37 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
 
 }  // namespace
 
-h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
-                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
-                           float skip_eps) {
+template <bool F8, bool SKIP>
+static h3_status set_attention_smem() {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel,
+    const size_t bytes = F8 ? 1024 + (2 + KV_SLOTS) * (TILE_BYTES / 2) + 256 : Q2_SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<F8, SKIP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Q2_SMEM_BYTES));
+                                         static_cast<int>(bytes));
     if (e != cudaSuccess) return cuda_fail(e, "attention: set shared memory size");
     attr_done[dev] = true;
   }
+  return H3_OK;
+}
+
+h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
+                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
+                           float skip_eps) {
+  const bool skip = skip_eps > 0.f;
+  h3_status st = skip ? set_attention_smem<false, true>() : set_attention_smem<false, false>();
+  if (st != H3_OK) return st;
   AttnArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
   a.ld_out = ld_out;
   a.L = L;
+  a.H = H;
   a.num_kv = (L + BKV - 1) / BKV;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.skip = skip_eps > 0.f ? 1 : 0;
-  a.skip_log2 = skip_eps > 0.f ? -log2f(skip_eps) : 0.f;
-  h3_status st = dev_err(&a.err);
-  if (st != H3_OK) return st;
+  a.skip_log2 = skip ? -log2f(skip_eps) : 0.f;
+  if ((st = dev_err(&a.err)) != H3_OK) return st;
   CUtensorMap tq, tk, tv;
   const uint64_t width = static_cast<uint64_t>(H) * DH;
   const uint64_t stride = static_cast<uint64_t>(ld_in) * 2;
@@ -394,8 +485,38 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   if ((st = make_tmap_bf16_2d(&tk, k, width, L, stride, 64, BKV)) != H3_OK) return st;
   if ((st = make_tmap_bf16_2d(&tv, v, width, L, stride, 64, BKV)) != H3_OK) return st;
   dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
-  attention_kernel<<<grid, Q2_THREADS, Q2_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  if (skip)
+    attention_kernel<false, true><<<grid, Q2_THREADS, Q2_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  else
+    attention_kernel<false, false><<<grid, Q2_THREADS, Q2_SMEM_BYTES, s>>>(tq, tk, tv, a);
   return cuda_fail(cudaGetLastError(), "attention launch");
+}
+
+h3_status launch_attention_fp8(const void* qc, const void* kc, const void* vc, int64_t ld_codes,
+                               const float* sq, const float* sk, const float* sv, void* o,
+                               int64_t ld_out, int L, int H, float scale, cudaStream_t s) {
+  h3_status st = set_attention_smem<true, false>();
+  if (st != H3_OK) return st;
+  AttnArgs a{};
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.ld_out = ld_out;
+  a.L = L;
+  a.H = H;
+  a.num_kv = (L + BKV - 1) / BKV;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  if ((st = dev_err(&a.err)) != H3_OK) return st;
+  CUtensorMap tq, tk, tv;
+  const uint64_t width = static_cast<uint64_t>(H) * DH;  // bytes per row of codes
+  if ((st = make_tmap_u8_2d(&tq, qc, width, L, ld_codes, 128, BQ)) != H3_OK) return st;
+  if ((st = make_tmap_u8_2d(&tk, kc, width, L, ld_codes, 128, BKV)) != H3_OK) return st;
+  if ((st = make_tmap_u8_2d(&tv, vc, width, L, ld_codes, 128, BKV)) != H3_OK) return st;
+  const size_t smem = 1024 + (2 + KV_SLOTS) * (TILE_BYTES / 2) + 256;
+  dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
+  attention_kernel<true, false><<<grid, Q2_THREADS, smem, s>>>(tq, tk, tv, a);
+  return cuda_fail(cudaGetLastError(), "attention (fp8) launch");
 }
 
 }  // namespace h3

@@ -71,4 +71,16 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
                            void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
                            float skip_eps = 0.f);
 
+// SAGE-style FP8 attention: operands (h3_sage.cu) and the FP8 attention
+// kernel (h3_attention.cu). Codes [L, H*128] bytes with row stride ldc; sq,
+// sk [ceil(L/128), H]; sv, k_mean [H, 128]; scratch of sage_scratch_bytes.
+size_t sage_scratch_bytes(int L, int H);
+h3_status launch_sage_quantize(const void* q, const void* k, const void* v, int64_t ld, int L,
+                               int H, uint8_t* qc, uint8_t* kc, uint8_t* vc, int64_t ldc,
+                               float* sq, float* sk, float* sv, float* k_mean, void* scratch,
+                               cudaStream_t s);
+h3_status launch_attention_fp8(const void* qc, const void* kc, const void* vc, int64_t ld_codes,
+                               const float* sq, const float* sk, const float* sv, void* o,
+                               int64_t ld_out, int L, int H, float scale, cudaStream_t s);
+
 }  // namespace h3

@@ -1,0 +1,188 @@
+// FP8 operands for SAGE-style attention (vLLM-Omni H3 blog, section 4.3: Q, K,
+// P and V quantised to FP8 for the QK and PV products).
+//
+//   1. kv_stats_partial / kv_stats_final: per (head, channel) mean of K and
+//      absmax of V over the L valid rows, in two deterministic passes (chunk
+//      partials with compensated sums, then an in-order combine);
+//   2. qk_tile_quant: Q, and K minus its mean, to E4M3 per (128-row tile,
+//      head) block with absmax scaling;
+//   3. v_quant: V to E4M3 per (head, channel) with the V absmax.
+// Scaling: inv = 448 / amax (0 when amax == 0), code = E4M3_satfinite(x * inv),
+// scale = amax / 448, every step rounded in FP32. Codes keep the [S, H, 128]
+// row layout of the inputs (one byte per element); rows >= L are not written.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "h3_internal.cuh"
+
+namespace h3 {
+namespace {
+
+constexpr int DH = 128;
+constexpr int ST_ROWS = 512;  // rows per statistics chunk
+
+// Compensated (two-float) accumulation: s + c carries the running sum.
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = __fsub_rn(x, c);
+  const float t = __fadd_rn(s, y);
+  c = __fsub_rn(__fsub_rn(t, s), y);
+  s = t;
+}
+
+// grid (chunks, H), 128 threads: thread d owns channel d of head blockIdx.y.
+__global__ void __launch_bounds__(DH)
+    kv_stats_partial_kernel(const __nv_bfloat16* __restrict__ k,
+                            const __nv_bfloat16* __restrict__ v, int64_t ld, int L,
+                            float* __restrict__ psum, float* __restrict__ pmax) {
+  const int chunk = blockIdx.x, h = blockIdx.y, d = threadIdx.x, H = gridDim.y;
+  const int r0 = chunk * ST_ROWS, r1 = min(L, r0 + ST_ROWS);
+  const int64_t col = static_cast<int64_t>(h) * DH + d;
+  float s = 0.f, c = 0.f, mx = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const int64_t off = static_cast<int64_t>(r) * ld + col;
+    kahan_add(s, c, __bfloat162float(k[off]));
+    mx = fmaxf(mx, fabsf(__bfloat162float(v[off])));
+  }
+  const int64_t o = (static_cast<int64_t>(chunk) * H + h) * DH + d;
+  psum[o] = __fadd_rn(s, -c);
+  pmax[o] = mx;
+}
+
+// grid H, 128 threads: combine the chunks in order.
+__global__ void __launch_bounds__(DH)
+    kv_stats_final_kernel(const float* __restrict__ psum, const float* __restrict__ pmax,
+                          int chunks, int L, float* __restrict__ k_mean, float* __restrict__ sv,
+                          float* __restrict__ inv_v) {
+  const int h = blockIdx.x, d = threadIdx.x, H = gridDim.x;
+  float s = 0.f, c = 0.f, mx = 0.f;
+  for (int ch = 0; ch < chunks; ++ch) {
+    const int64_t o = (static_cast<int64_t>(ch) * H + h) * DH + d;
+    kahan_add(s, c, psum[o]);
+    mx = fmaxf(mx, pmax[o]);
+  }
+  const int i = h * DH + d;
+  k_mean[i] = __fdiv_rn(__fadd_rn(s, -c), static_cast<float>(L));
+  sv[i] = __fdiv_rn(mx, 448.0f);
+  inv_v[i] = mx > 0.f ? __fdiv_rn(448.0f, mx) : 0.f;
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+constexpr int QT_THREADS = 256;  // 16 rows x 16 chunks of 8 channels per pass, 8 passes
+
+// grid (tiles, H, 2): z = 0 quantises Q, z = 1 quantises K - mean.
+__global__ void __launch_bounds__(QT_THREADS)
+    qk_tile_quant_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                         int64_t ld, const float* __restrict__ k_mean, int L,
+                         uint8_t* __restrict__ qc, uint8_t* __restrict__ kc, int64_t ldc,
+                         float* __restrict__ sq, float* __restrict__ sk) {
+  __shared__ float red[QT_THREADS / 32];
+  const int tile = blockIdx.x, h = blockIdx.y, which = blockIdx.z, H = gridDim.y;
+  const __nv_bfloat16* src = which ? k : q;
+  uint8_t* dst = which ? kc : qc;
+  const int chunk = threadIdx.x & 15;   // channels 8*chunk .. 8*chunk+7
+  const int rsub = threadIdx.x >> 4;    // row within a 16-row pass
+  float mean[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mean[j] = which ? k_mean[h * DH + chunk * 8 + j] : 0.f;
+  float x[8][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = tile * 128 + i * 16 + rsub;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (row < L)
+      raw = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(row) * ld + h * DH +
+                                            chunk * 8);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[i][2 * j] = row < L ? __fsub_rn(bf16_lo(w[j]), mean[2 * j]) : 0.f;
+      x[i][2 * j + 1] = row < L ? __fsub_rn(bf16_hi(w[j]), mean[2 * j + 1]) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[i][j]));
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < QT_THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = tile * 128 + i * 16 + rsub;
+    if (row < L) {
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(x[i][j], inv);
+      *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(row) * ldc + h * DH + chunk * 8) =
+          make_uint2(e4m3x4(f[0], f[1], f[2], f[3]), e4m3x4(f[4], f[5], f[6], f[7]));
+    }
+  }
+  if (threadIdx.x == 0) (which ? sk : sq)[tile * H + h] = __fdiv_rn(amax, 448.0f);
+}
+
+// One thread per 8 channels of one row.
+__global__ void __launch_bounds__(256)
+    v_quant_kernel(const __nv_bfloat16* __restrict__ v, int64_t ld, const float* __restrict__ inv_v,
+                   int L, int H, uint8_t* __restrict__ vc, int64_t ldc) {
+  const int64_t per_row = static_cast<int64_t>(H) * (DH / 8);
+  const int64_t total = static_cast<int64_t>(L) * per_row;
+  for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
+    const int64_t row = i / per_row;
+    const int64_t cc = i - row * per_row;  // chunk of 8 channels across heads
+    const uint4 raw = *reinterpret_cast<const uint4*>(v + row * ld + cc * 8);
+    const float4 i0 = *reinterpret_cast<const float4*>(inv_v + cc * 8);
+    const float4 i1 = *reinterpret_cast<const float4*>(inv_v + cc * 8 + 4);
+    const float inv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __fmul_rn(bf16_lo(w[j]), inv[2 * j]);
+      f[2 * j + 1] = __fmul_rn(bf16_hi(w[j]), inv[2 * j + 1]);
+    }
+    *reinterpret_cast<uint2*>(vc + row * ldc + cc * 8) =
+        make_uint2(e4m3x4(f[0], f[1], f[2], f[3]), e4m3x4(f[4], f[5], f[6], f[7]));
+  }
+}
+
+}  // namespace
+
+size_t sage_scratch_bytes(int L, int H) {
+  const size_t chunks = (static_cast<size_t>(L) + ST_ROWS - 1) / ST_ROWS;
+  return 2 * chunks * H * DH * sizeof(float) + static_cast<size_t>(H) * DH * sizeof(float);
+}
+
+h3_status launch_sage_quantize(const void* q, const void* k, const void* v, int64_t ld, int L,
+                               int H, uint8_t* qc, uint8_t* kc, uint8_t* vc, int64_t ldc,
+                               float* sq, float* sk, float* sv, float* k_mean, void* scratch,
+                               cudaStream_t s) {
+  const int chunks = (L + ST_ROWS - 1) / ST_ROWS;
+  float* psum = static_cast<float*>(scratch);
+  float* pmax = psum + static_cast<size_t>(chunks) * H * DH;
+  float* inv_v = pmax + static_cast<size_t>(chunks) * H * DH;
+  const auto* qq = static_cast<const __nv_bfloat16*>(q);
+  const auto* kk = static_cast<const __nv_bfloat16*>(k);
+  const auto* vv = static_cast<const __nv_bfloat16*>(v);
+  kv_stats_partial_kernel<<<dim3(chunks, H), DH, 0, s>>>(kk, vv, ld, L, psum, pmax);
+  kv_stats_final_kernel<<<H, DH, 0, s>>>(psum, pmax, chunks, L, k_mean, sv, inv_v);
+  const int tiles = (L + 127) / 128;
+  qk_tile_quant_kernel<<<dim3(tiles, H, 2), QT_THREADS, 0, s>>>(qq, kk, ld, k_mean, L, qc, kc, ldc,
+                                                               sq, sk);
+  const int64_t work = static_cast<int64_t>(L) * H * (DH / 8);
+  const int grid = static_cast<int>(std::min<int64_t>((work + 255) / 256, num_sms() * 8LL));
+  v_quant_kernel<<<grid, 256, 0, s>>>(vv, ld, inv_v, L, H, vc, ldc);
+  return cuda_fail(cudaGetLastError(), "sage quantize launch");
+}
+
+}  // namespace h3

@@ -61,6 +61,10 @@ _SIGS = {
     "h3_qk_norm_rope": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P]),
     "h3_attention_varlen": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
     "h3_swiglu": (_I, [_P, _P, _I, _I, _I, _P]),
+    "h3_sage_scratch_bytes": (_SZ, [_I, _I]),
+    "h3_sage_quantize": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                              _P]),
+    "h3_attention_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
     "h3_attention_varlen_skip": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P]),
     "h3_linear": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_linear_swiglu": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
@@ -80,7 +84,7 @@ _SIGS = {
     "h3_linear_swiglu_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_block_workspace_bytes_fp8": (_SZ, [ctypes.POINTER(BlockConfig)]),
     "h3_block_forward_fp8": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeightsFp8),
-                                  _P, _P, _P, _P, _SZ, _P]),
+                                  _P, _P, _P, _I, _P, _SZ, _P]),
     "h3_stack_forward": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), _I, _P,
                               _P, _I, _P, _P, _P, _SZ, _P]),
 }
@@ -219,6 +223,38 @@ def attention_varlen_skip(q, k, v, o, L=None, scale=None, skip_eps=0.0, stream=N
         _p(q), _p(k), _p(v), _p(o), S, L, H, Dh, scale, skip_eps, _s(stream)))
 
 
+def sage_quantize(q, k, v, L=None, stream=None) -> dict:
+    """FP8 operands for attention_fp8 (allocated here, from torch): codes qc,
+    kc, vc (uint8 [S, H, Dh]), scales sq, sk ([ceil(L/128), H]), sv and
+    k_mean ([H, Dh])."""
+    S, H, Dh = q.shape
+    L = S if L is None else L
+    dev = q.device
+    nt = max(1, (L + 127) // 128)
+    out = dict(qc=torch.zeros(S, H, Dh, dtype=torch.uint8, device=dev),
+               kc=torch.zeros(S, H, Dh, dtype=torch.uint8, device=dev),
+               vc=torch.zeros(S, H, Dh, dtype=torch.uint8, device=dev),
+               sq=torch.zeros(nt, H, device=dev), sk=torch.zeros(nt, H, device=dev),
+               sv=torch.zeros(H, Dh, device=dev), k_mean=torch.zeros(H, Dh, device=dev))
+    nbytes = lib().h3_sage_scratch_bytes(L, H)
+    scratch = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _check("sage_quantize", lib().h3_sage_quantize(
+        _p(q), _p(k), _p(v), S, L, H, Dh, _p(out["qc"]), _p(out["kc"]), _p(out["vc"]),
+        _p(out["sq"]), _p(out["sk"]), _p(out["sv"]), _p(out["k_mean"]), _p(scratch), nbytes,
+        _s(stream)))
+    return out
+
+
+def attention_fp8(ops: dict, o, L=None, scale=None, stream=None):
+    """FP8 attention on sage_quantize's operands into o [S, H, Dh] bf16."""
+    S, H, Dh = o.shape
+    L = S if L is None else L
+    scale = Dh ** -0.5 if scale is None else scale
+    _check("attention_fp8", lib().h3_attention_fp8(
+        _p(ops["qc"]), _p(ops["kc"]), _p(ops["vc"]), _p(ops["sq"]), _p(ops["sk"]),
+        _p(ops["sv"]), _p(o), S, L, H, Dh, scale, _s(stream)))
+
+
 def swiglu(gate_up, out, L=None, stream=None):
     _need(gate_up, torch.bfloat16, "gate_up")
     _need(out, torch.bfloat16, "out")
@@ -341,11 +377,12 @@ def block_workspace_bytes_fp8(cfg: BlockConfig) -> int:
     return n
 
 
-def block_forward_fp8(cfg: BlockConfig, weights_fp8, resid, mod, pos, workspace, stream=None):
+def block_forward_fp8(cfg: BlockConfig, weights_fp8, resid, mod, pos, workspace, stream=None,
+                      fp8_attention=False):
     w = weights_fp8 if isinstance(weights_fp8, BlockWeightsFp8) else block_weights_fp8(weights_fp8)
     _check("block_forward_fp8", lib().h3_block_forward_fp8(
-        ctypes.byref(cfg), ctypes.byref(w), _p(resid), _p(mod), _p(pos), _p(workspace),
-        workspace.numel() * workspace.element_size(), _s(stream)))
+        ctypes.byref(cfg), ctypes.byref(w), _p(resid), _p(mod), _p(pos), int(fp8_attention),
+        _p(workspace), workspace.numel() * workspace.element_size(), _s(stream)))
 
 
 def block_workspace_bytes(cfg: BlockConfig) -> int:

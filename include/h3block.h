@@ -140,6 +140,36 @@ h3_status h3_attention_varlen_skip(const void* q, const void* k, const void* v, 
                                    h3_stream_t stream);
 
 /*
+ * a3 with FP8 ("SAGE") products (next step; blog section 4.3: Q, K, P and V
+ * quantised to FP8 for the QK and PV products). Two steps:
+ *
+ * h3_sage_quantize: K is smoothed by subtracting its per-(head, channel)
+ * mean over the L valid keys (float32; softmax is unchanged), Q and the
+ * smoothed K are quantised to E4M3 per (128-row tile, head) block and V per
+ * (head, channel), all with absmax scaling (inv = 448 / amax, code =
+ * E4M3_satfinite(x * inv), scale = amax / 448, float32 steps).
+ *   q, k, v   [S, H, Dh] bf16 (row stride H*Dh)
+ *   qc, kc, vc [S, H, Dh] E4M3 codes (bytes); rows >= L are not written
+ *   sq, sk    [ceil(L/128), H] float32; sv, k_mean [H, Dh] float32
+ *   scratch   device memory of h3_sage_scratch_bytes(L, H) bytes
+ *
+ * h3_attention_fp8: o[i] = sum_j E4M3(p_ij) * vc[j] * sv / sum_j p_ij with
+ * p_ij = 224 * 2^(z_ij - m_i), z_ij = (qc_i . kc_j) * sq * sk * softmax_scale
+ * * log2(e), m_i an integer running maximum kept within 1 of the exact one
+ * (so P is an exact power-of-two multiple of the P against the exact maximum
+ * and 224 * P <= 448); tcgen05 kind::f8f6f4 for QK and PV, FP32 softmax and
+ * accumulation, bf16 out. Dh == 128.
+ */
+size_t h3_sage_scratch_bytes(int L, int H);
+h3_status h3_sage_quantize(const void* q, const void* k, const void* v, int S, int L, int H,
+                           int Dh, void* qc, void* kc, void* vc, float* sq, float* sk, float* sv,
+                           float* k_mean, void* scratch, size_t scratch_bytes,
+                           h3_stream_t stream);
+h3_status h3_attention_fp8(const void* qc, const void* kc, const void* vc, const float* sq,
+                           const float* sk, const float* sv, void* o, int S, int L, int H,
+                           int Dh, float softmax_scale, h3_stream_t stream);
+
+/*
  * a5 — SwiGLU (blog section 3.2, #6283): out[i,j] = SiLU(g) * u with
  * g = gate_up[i,j], u = gate_up[i,F+j], SiLU(g) = g / (1 + exp(-g)), for i < L.
  *   gate_up [S, 2F] bf16, out [S, F] bf16. F % 8 == 0.
@@ -307,12 +337,15 @@ size_t h3_block_workspace_bytes_fp8(const h3_block_config* cfg);
 
 /* h3_block_forward with the four projections in FP8: every projection input
  * (h1, the attention output, h2, the SwiGLU output) is quantised per token
- * with h3_quantize_fp8_rows before its FP8 GEMM; everything else (modulation,
- * Q/K RMSNorm + RoPE, attention, SwiGLU) is the BF16/FP32 path. D % 128 == 0,
- * F % 128 == 0 in addition to h3_block_forward's limits. */
+ * with h3_quantize_fp8_rows before its FP8 GEMM. fp8_attention != 0 also runs
+ * the attention in FP8 (h3_sage_quantize + h3_attention_fp8); otherwise the
+ * attention and everything else (modulation, Q/K RMSNorm + RoPE, SwiGLU) is
+ * the BF16/FP32 path. D % 128 == 0, F % 128 == 0 in addition to
+ * h3_block_forward's limits. */
 h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weights_fp8* w,
                                float* resid, const float* mod, const int32_t* pos,
-                               void* workspace, size_t workspace_bytes, h3_stream_t stream);
+                               int fp8_attention, void* workspace, size_t workspace_bytes,
+                               h3_stream_t stream);
 
 /* Number of kernel stages h3_block_forward launches, in the order listed
  * above: 0 modulation+LN, 1 QKV projection, 2 Q/K RMSNorm+RoPE, 3 attention,

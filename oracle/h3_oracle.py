@@ -267,7 +267,7 @@ def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
                   *, L: int, heads: int, head_dim: int, axis_dims, theta: float,
                   eps_ln: float = 1e-6, eps_qk: float = 1e-6, rows=None,
                   kv_chunk: int = 4096, return_intermediates: bool = False, seg=None,
-                  fp8: bool = False):
+                  fp8: bool = False, fp8_attention: bool = False):
     """Forward pass of one DiT block for query rows `rows` (default all < L).
 
     resid [S, D] float32 residual stream; mod [6, D]; weights bf16-valued
@@ -307,21 +307,34 @@ def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
     v_all = np.empty((L, heads, head_dim))
     w_k = w_qkv[D:2 * D]
     w_v = w_qkv[2 * D:3 * D]
+    # FP8 attention scales Q per 128-row tile, so every row's q is needed then
+    q_all = np.zeros((L, heads, head_dim)) if fp8_attention else None
+    w_q = w_qkv[0:D]
     for c0 in range(0, L, kv_chunk):
         c1 = min(L, c0 + kv_chunk)
         shc, scc = unpack_mod(modulation_rows(mod, seg, np.arange(c0, c1)))[:2]
         _, h1c = mod_norm_residual(r_all[c0:c1], shift=shc, scale=scc, eps=eps_ln)
+        if fp8_attention:
+            qc = proj(h1c, w_q).reshape(c1 - c0, heads, head_dim)
+            q_all[c0:c1] = qk_norm_rope(qc, q_gain, pos[c0:c1], axis_dims, theta, eps_qk)
         kc = proj(h1c, w_k).reshape(c1 - c0, heads, head_dim)
         k_all[c0:c1] = qk_norm_rope(kc, k_gain, pos[c0:c1], axis_dims, theta, eps_qk)
         v_all[c0:c1] = proj(h1c, w_v).reshape(c1 - c0, heads, head_dim)
 
     r = r_all[rows]
     _, h1 = mod_norm_residual(r, shift=sh1, scale=sc1, eps=eps_ln)
-    q = proj(h1, w_qkv[0:D]).reshape(len(rows), heads, head_dim)
+    q = proj(h1, w_q).reshape(len(rows), heads, head_dim)
     q = qk_norm_rope(q, q_gain, np.asarray(pos)[rows], axis_dims, theta, eps_qk)
-    q_full = np.zeros((L, heads, head_dim))
-    q_full[rows] = q
-    a = attention(q_full, k_all, v_all, L, scale, rows=rows).reshape(len(rows), D)
+    if fp8_attention:
+        q_full = q_all
+    else:
+        q_full = np.zeros((L, heads, head_dim))
+        q_full[rows] = q
+    if fp8_attention:
+        ops = sage_quantize(q_full, k_all, v_all, L)
+        a = attention_sage(ops, L, scale, rows=rows).reshape(len(rows), D)
+    else:
+        a = attention(q_full, k_all, v_all, L, scale, rows=rows).reshape(len(rows), D)
     o = proj(a, w_o)
     r, h2 = mod_norm_residual(r, o, g1, sh2, sc2, eps=eps_ln)
     gu = proj(h2, w_gu)
@@ -467,15 +480,19 @@ def attention_skip(q, k, v, L: int, scale: float, eps: float, tile: int = 128):
 # backend can quantise Q, K, P and V to FP8 for the QK and PV products). The
 # pages give no scaling scheme; the reading here:
 #   * K is first smoothed by subtracting its per-(head, channel) mean over the
-#     L valid keys, rounded to bf16 (softmax is unchanged: each row's scores
+#     L valid keys, taken in float32 (softmax is unchanged: each row's scores
 #     move by one constant);
 #   * Q and the smoothed K are quantised to E4M3 per (128-row tile, head)
 #     block, V per (head, channel) over the valid keys, each with absmax
 #     scaling (inv = 448 / amax, code = e4m3(x * inv), scale = amax / 448,
 #     every step in float32);
-#   * scores = (Q codes . K codes) * sq * sk; softmax in base 2 against the
-#     row maximum; P is rounded to E4M3 for the PV product, the row sum uses
-#     the unrounded P; O = (P codes . V codes) * sv / sum.
+#   * scores = (Q codes . K codes) * sq * sk; softmax in base 2 against an
+#     integer reference at or above the row maximum (the ceiling of the row
+#     maximum: any integer reference gives P values that differ by an exact
+#     power of two, so their E4M3 codes agree in the normal range); 224 * P
+#     (at most 448) is rounded to E4M3 for the PV product, which keeps P down
+#     to 2^-14 of the row maximum in E4M3's normal range; the row sum uses the
+#     unrounded 224 * P; O = (P codes . V codes) * sv / sum.
 # ---------------------------------------------------------------------------
 
 def _absmax_codes(x32, axis):
@@ -488,15 +505,19 @@ def _absmax_codes(x32, axis):
     return codes, scale
 
 
-def sage_quantize(q, k, v, L: int, tile: int = 128):
+def sage_quantize(q, k, v, L: int, tile: int = 128, k_mean=None):
     """FP8 operands of SAGE attention. q, k, v [S, H, Dh] bf16 values.
+    k_mean: the per-(head, channel) mean of K to subtract (float32 values);
+    computed here (float64, rounded to float32) when not given.
     Returns dict: qc [L,H,Dh], sq [nt,H], kc, sk [nt,H], vc, sv [H,Dh],
-    k_mean [H,Dh] (bf16 values)."""
+    k_mean [H,Dh]."""
     q = np.asarray(q, np.float32)[:L]
     k = np.asarray(k, np.float32)[:L]
     v = np.asarray(v, np.float32)[:L]
     H, Dh = q.shape[1], q.shape[2]
-    k_mean = round_bf16(np.asarray(k, np.float64).mean(axis=0))
+    if k_mean is None:
+        k_mean = np.asarray(k, np.float64).mean(axis=0)
+    k_mean = np.asarray(k_mean, np.float32).astype(np.float64)
     ks = (k - k_mean.astype(np.float32)[None]).astype(np.float32)
     nt = (L + tile - 1) // tile
     qc = np.empty((L, H, Dh)); kc = np.empty((L, H, Dh))
@@ -526,7 +547,7 @@ def attention_sage(ops, L: int, scale: float, rows=None, tile: int = 128):
     for h in range(H):
         s = (qc[rows, h, :] @ kc[:, h, :].T) * sq[rows // tile, h][:, None] * sk[key_tile, h][None, :]
         z = s * scale / np.log(2.0)
-        p = np.exp2(z - z.max(axis=1, keepdims=True))
+        p = 224.0 * np.exp2(z - np.ceil(z.max(axis=1, keepdims=True)))
         pc = round_e4m3(p)
         out[:, h, :] = (pc @ vc[:, h, :]) * sv[h][None, :] / p.sum(axis=1, keepdims=True)
     return round_bf16(out)

@@ -151,3 +151,35 @@ def test_fp8_block_full_size_sampled(h3lib):
     out = run_fp8_block(h3lib, shape, inp)
     rows = sample_rows(shape.L, 256, 9)
     check_fp8_block(out[torch.from_numpy(rows).to(dev)], shape, inp, rows, elementwise=False)
+
+
+def run_fp8_block_attn(h3lib, shape, inp):
+    cfg = h3lib.block_config(shape.S, shape.L, shape.D, shape.H, shape.Dh, shape.F,
+                             shape.axis_dims, shape.theta, shape.eps_ln, shape.eps_qk)
+    w8 = h3lib.quantize_block_weights_fp8(inp)
+    ws = torch.empty(h3lib.block_workspace_bytes_fp8(cfg), dtype=torch.uint8, device=dev)
+    out = inp["resid"].clone()
+    h3lib.block_forward_fp8(cfg, w8, out, inp["mod"], inp["pos"], ws, fp8_attention=True)
+    h3lib.check_device_error()
+    return out
+
+
+@pytest.mark.parametrize("full", [False, pytest.param(True, marks=pytest.mark.slow)])
+def test_fp8_block_with_fp8_attention(h3lib, full):
+    """FP8 projections and FP8 (SAGE) attention together, against the oracle's
+    block with the same options; relative L2 on the output and the increment
+    (the same tolerances and reasons as the FP8 full-size block)."""
+    shape = I.FULL if full else I.TINY
+    inp = (I.block_inputs(shape, seed=3, device=dev) if full else
+           {k: v.to(dev) for k, v in I.block_inputs(shape, seed=0).items()})
+    out = run_fp8_block_attn(h3lib, shape, inp)
+    rows = sample_rows(shape.L, 128, 13) if full else np.arange(shape.L)
+    n = {k: np64(v) if v.is_floating_point() else v.cpu().numpy() for k, v in inp.items()}
+    ref = O.block_forward(n["resid"], n["mod"], n["w_qkv"], n["w_o"], n["w_gu"], n["w_down"],
+                          n["q_gain"], n["k_gain"], n["pos"], L=shape.L, heads=shape.H,
+                          head_dim=shape.Dh, axis_dims=shape.axis_dims, theta=shape.theta,
+                          rows=rows, fp8=True, fp8_attention=True)
+    x = np64(out[torch.from_numpy(rows).to(dev)])
+    r_in = n["resid"][rows]
+    assert rel_l2(x, ref) <= 1e-2, rel_l2(x, ref)
+    assert rel_l2(x - r_in, ref - r_in) <= 5e-2, rel_l2(x - r_in, ref - r_in)

@@ -679,8 +679,8 @@ def check_sage(o):
     k = bf16_values(r.standard_normal((S, H, Dh)) + 3.0)  # a large common offset
     v = bf16_values(r.standard_normal((S, H, Dh)))
     ops = o.sage_quantize(q, k, v, L)
-    # smoothing removes the per-channel mean (up to its bf16 rounding)
-    assert np.allclose(ops["k_mean"], k.mean(0), atol=2 ** -6 * 4)
+    # smoothing removes the per-channel mean
+    assert np.allclose(ops["k_mean"], k.mean(0), rtol=1e-6, atol=1e-7)
     # dequantised operands are within half an E4M3 step of the originals
     for c, s, x, kind in ((ops["qc"], ops["sq"], q, "q"), (ops["kc"], ops["sk"],
                           k - ops["k_mean"][None], "k")):
@@ -694,29 +694,25 @@ def check_sage(o):
     dense = o.attention(q, k, v, L, scale)
     out = o.attention_sage(ops, L, scale)
     assert np.linalg.norm(out - dense) / np.linalg.norm(dense) < 0.1
-    # identical keys: every p is exactly 1 (an E4M3 value), so the output is
-    # the mean of the dequantised V rows
-    kk = np.broadcast_to(k[:1], k.shape).copy()
-    opu = o.sage_quantize(q, kk, v, L)
+    # all scores 0 (q = 0): every p is exactly 1, an E4M3 value, so the output
+    # is the mean of the dequantised V rows
+    opu = o.sage_quantize(np.zeros_like(q), k, v, L)
     deq_v = opu["vc"] * opu["sv"][None].astype(np.float64)
-    assert np.allclose(o.attention_sage(opu, L, scale), o.round_bf16(deq_v.mean(0))[None].repeat(L, 0),
-                       rtol=2 ** -8, atol=1e-12)
-    # one key far above the others: its p is 1, every other p underflows the
-    # E4M3 range (< 2^-10) and the row sum is 1 up to 2^-20, so the output is
-    # that key's dequantised V row
+    assert np.allclose(o.attention_sage(opu, L, scale),
+                       o.round_bf16(deq_v.mean(0))[None].repeat(L, 0), rtol=2 ** -8, atol=1e-12)
+    # one key far above the others: every other p underflows E4M3, so the
+    # output is that key's dequantised V row times one factor (its E4M3 code
+    # over its exact p) within half an E4M3 step of 1
     kd = np.zeros_like(k)
     kd[7] = 8.0
-    qd = np.ones_like(q)
-    opd = o.sage_quantize(qd, kd, v, L)
+    opd = o.sage_quantize(np.ones_like(q), kd, v, L)
     deq_vd = opd["vc"] * opd["sv"][None].astype(np.float64)
-    assert np.allclose(o.attention_sage(opd, L, 1.0), np.broadcast_to(o.round_bf16(deq_vd[7]), (L, H, Dh)),
-                       rtol=2 ** -7, atol=1e-12)
-    # smoothing is exact in the score: with exactly representable operands and
-    # unit-like scales the smoothed scores differ from q.k by one row constant
-    s_full = q[:, 0] @ k[:, 0].T
-    s_smooth = q[:, 0] @ (k[:, 0] - ops["k_mean"][0]).T
-    d = s_full - s_smooth
-    assert np.allclose(d, d[:, :1], atol=1e-9)
+    outd = o.attention_sage(opd, L, 1.0)
+    ratio = outd / deq_vd[7][None]
+    big = np.abs(deq_vd[7][None]) > 0.05
+    lam = np.median(ratio[np.broadcast_to(big, ratio.shape)])
+    assert abs(lam - 1) <= 2 ** -4
+    assert np.allclose(outd, lam * deq_vd[7][None], rtol=2 ** -7, atol=2 ** -7 * 0.05)
 
 
 def test_sage():
