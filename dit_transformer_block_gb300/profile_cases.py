@@ -1,6 +1,6 @@
 """Small, fixed cases for ncu captures of the library's kernels.
 
-    python -m dit_transformer_block_gb300.profile_cases [attention] [gemm] [elementwise]
+    python -m dit_transformer_block_gb300.profile_cases [attention] [gemm] [elementwise] [fp8]
 
 Each selected kernel runs twice on inputs larger than L2 (129 MB) but a few
 hundred MB in total, so that an `ncu --set full -k <kernel> -s 1 -c 1`
@@ -9,6 +9,8 @@ capture of the second launch ends within a minute or two:
   gemm        M = 8192, N = 16128, K = 5376 (the QKV projection shape; 520 MB)
   elementwise qk_norm_rope on 16384 x 42 x 128, SwiGLU on 16384 x 2 x 14336,
               modulation/LN/residual on 16384 x 5376
+  fp8         FP8 GEMM (QKV shape, M = 8192), per-row FP8 quantisation of
+              8192 x 5376, SAGE quantisation and FP8 attention at S = L = 16384
 """
 from __future__ import annotations
 
@@ -20,7 +22,7 @@ from dit_transformer_block_gb300 import build, h3
 
 
 def main(argv):
-    which = set(argv) or {"attention", "gemm", "elementwise"}
+    which = set(argv) or {"attention", "gemm", "elementwise", "fp8"}
     build.build()
     h3.lib()
     dev = "cuda"
@@ -52,6 +54,22 @@ def main(argv):
         runs.append(lambda: h3.qk_norm_rope(qq, kk, ones, ones, pos, (32, 48, 48), S))
         runs.append(lambda: h3.swiglu(gu, u, S))
         runs.append(lambda: h3.mod_norm_residual(r, d, mod[2], mod[3], mod[4], hh, S))
+    if "fp8" in which:
+        M, N, K = 8192, 16128, 5376
+        x8, w8 = rnd(M, K), rnd(N, K, std=0.02)
+        qx = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        sx = torch.empty(M, device=dev)
+        qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
+        sw = torch.empty(N, device=dev)
+        h3.quantize_fp8_rows(w8, qw, sw)
+        y8 = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        runs.append(lambda: h3.quantize_fp8_rows(x8, qx, sx))
+        runs.append(lambda: h3.linear_fp8(qx, sx, qw, sw, y8, M))
+        S = 16384
+        qa, ka, va = rnd(S, 42, 128), rnd(S, 42, 128), rnd(S, 42, 128)
+        oa = torch.empty_like(qa)
+        ops = h3.sage_quantize(qa, ka, va, S)
+        runs.append(lambda: h3.attention_fp8(ops, oa, S))
     for _ in range(2):
         for fn in runs:
             fn()
