@@ -65,10 +65,13 @@ def block_work(S, L, D, H, Dh, F):
     """Algorithmic FLOPs and bytes of one block (valid rows only)."""
     attn = 4.0 * L * L * H * Dh
     gemm = 2.0 * L * D * (3 * D) + 2.0 * L * D * D + 2.0 * L * D * (2 * F) + 2.0 * L * F * D
-    # bytes of the HBM-bound stages, as launched (unfused between kernels)
-    mnr = L * D * (4 + 2) + L * D * (4 + 2 + 4 + 2) + L * D * (4 + 2 + 4)
-    qk = 2 * L * D * 2 * 2
-    return dict(attn_flop=attn, gemm_flop=gemm, elementwise_bytes=mnr + qk)
+    # bytes of the HBM-bound stages as launched: the first modulated LayerNorm
+    # (plus the RoPE table: positions in, 64 (cos, sin) pairs out per row) and
+    # the middle residual + LayerNorm; Q/K RMSNorm + RoPE, SwiGLU and the last
+    # residual update run in GEMM epilogues
+    mnr = L * D * (4 + 2) + L * D * (4 + 2 + 4 + 2)
+    rope = L * (12 + 64 * 8)
+    return dict(attn_flop=attn, gemm_flop=gemm, elementwise_bytes=mnr + rope)
 
 
 def stage_work(S, L, D, H, Dh, F):
@@ -76,15 +79,13 @@ def stage_work(S, L, D, H, Dh, F):
     GEMMs count 2MNK, attention 4 L^2 H Dh, HBM-bound stages their minimum
     bytes read + written (rows < L only)."""
     return [
-        ("hbm", L * D * (4 + 2), "GB/s"),                        # r -> h1
-        ("tensor", 2.0 * L * D * 3 * D, "TFLOP/s"),              # QKV
-        ("hbm", 2 * L * D * 2 * 2, "GB/s"),                      # q, k in place
+        ("hbm", L * D * (4 + 2) + L * (12 + 64 * 8), "GB/s"),   # r -> h1; pos -> RoPE table
+        ("tensor", 2.0 * L * D * 3 * D, "TFLOP/s"),              # QKV + Q/K RMSNorm + RoPE
         ("tensor", 4.0 * L * L * H * Dh, "TFLOP/s"),             # attention
         ("tensor", 2.0 * L * D * D, "TFLOP/s"),                  # out
         ("hbm", L * D * (4 + 2 + 4 + 2), "GB/s"),                # r, o -> r, h2
         ("tensor", 2.0 * L * D * 2 * F, "TFLOP/s"),              # gate/up + SwiGLU
-        ("tensor", 2.0 * L * F * D, "TFLOP/s"),                  # down
-        ("hbm", L * D * (4 + 2 + 4), "GB/s"),                    # r, f -> r
+        ("tensor", 2.0 * L * F * D, "TFLOP/s"),                  # down + residual
     ]
 
 
@@ -483,9 +484,9 @@ def run_ours(a):
 
     pk = peaks()
     work = block_work(S, L, D, H, Dh, F)
-    attn_ms = stage_ms[3]
-    gemm_ms = stage_ms[1] + stage_ms[4] + stage_ms[6] + stage_ms[7]
-    ew_ms = stage_ms[0] + stage_ms[2] + stage_ms[5] + stage_ms[8]
+    attn_ms = stage_ms[2]
+    gemm_ms = stage_ms[1] + stage_ms[3] + stage_ms[5] + stage_ms[6]
+    ew_ms = stage_ms[0] + stage_ms[4]
     attn_tf = work["attn_flop"] / attn_ms / 1e9
     gemm_tf = work["gemm_flop"] / gemm_ms / 1e9
     traffic = profile_traffic("h3_attention.cu", "attention_full_size.md")
@@ -527,7 +528,7 @@ def run_ours(a):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": h3.BLOCK_STAGES * a.steps,
+        "gpu_launches": h3.BLOCK_LAUNCHES * a.steps,
         "e2e_note": "uploads and downloads on their own streams, two buffer sets: copies overlap compute",
         "clocks": clocks.summary(),
         "extras": extras,

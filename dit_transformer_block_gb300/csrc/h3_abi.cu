@@ -398,6 +398,76 @@ h3_status h3_linear_swiglu(const void* x, const void* w_gu, void* out, int S, in
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
+static h3_status check_axis_dims(const int* axis_dims, float theta) {
+  H3_REQUIRE(axis_dims != nullptr, H3_ERR_INVALID_ARG, "axis_dims is NULL");
+  int sum = 0;
+  for (int a = 0; a < 3; ++a) {
+    H3_REQUIRE(axis_dims[a] >= 0 && axis_dims[a] % 2 == 0, H3_ERR_INVALID_ARG,
+               "axis_dims[%d]=%d must be even and >= 0", a, axis_dims[a]);
+    sum += axis_dims[a];
+  }
+  H3_REQUIRE(sum == 128, H3_ERR_INVALID_ARG, "axis_dims sum %d != head_dim 128", sum);
+  H3_REQUIRE(theta > 0.f, H3_ERR_INVALID_ARG, "theta must be > 0");
+  return H3_OK;
+}
+
+h3_status h3_rope_table(const int32_t* pos, const int* axis_dims, int S, int L, float theta,
+                        float* table, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(pos && table, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  if ((st = check_axis_dims(axis_dims, theta)) != H3_OK) return st;
+  H3_REQUIRE(aligned16(table), H3_ERR_MISALIGNED, "table must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  return launch_rope_table(pos, axis_dims, L, theta, reinterpret_cast<float2*>(table),
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+h3_status h3_linear_qk_norm_rope(const void* x, const void* w_qkv, void* qkv,
+                                 const float* q_gain, const float* k_gain,
+                                 const float* rope_table, int S, int L, int H, int K, float eps,
+                                 h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(x && w_qkv && qkv && q_gain && k_gain && rope_table, H3_ERR_INVALID_ARG,
+             "a required pointer is NULL");
+  H3_REQUIRE(H > 0 && H % 2 == 0, H3_ERR_UNSUPPORTED, "H=%d must be even", H);
+  H3_REQUIRE(K > 0 && K % 64 == 0, H3_ERR_UNSUPPORTED, "K=%d must be a multiple of 64", K);
+  H3_REQUIRE(eps >= 0.f, H3_ERR_INVALID_ARG, "eps must be >= 0");
+  H3_REQUIRE(aligned16(x) && aligned16(w_qkv) && aligned16(qkv) && aligned16(q_gain) &&
+                 aligned16(k_gain) && aligned16(rope_table),
+             H3_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  const int D = H * 128;
+  GemmExtra ex;
+  ex.q_gain = q_gain;
+  ex.k_gain = k_gain;
+  ex.rope = reinterpret_cast<const float2*>(rope_table);
+  ex.d_model = D;
+  ex.eps = eps;
+  return launch_gemm(x, K, w_qkv, K, qkv, 3LL * D, L, 3 * D, K, GEMM_QK_NORM_ROPE,
+                     reinterpret_cast<cudaStream_t>(stream), &ex);
+}
+
+h3_status h3_linear_residual(const void* x, const void* w, float* resid, const float* gate,
+                             int S, int L, int N, int K, h3_stream_t stream) {
+  clear_error();
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(x && w && resid && gate, H3_ERR_INVALID_ARG, "a required pointer is NULL");
+  H3_REQUIRE(N > 0 && N % 256 == 0, H3_ERR_UNSUPPORTED, "N=%d must be a multiple of 256", N);
+  H3_REQUIRE(K > 0 && K % 64 == 0, H3_ERR_UNSUPPORTED, "K=%d must be a multiple of 64", K);
+  H3_REQUIRE(aligned16(x) && aligned16(w) && aligned16(resid) && aligned16(gate),
+             H3_ERR_MISALIGNED, "x, w, resid, gate must be 16-byte aligned");
+  if (L == 0) return H3_OK;
+  GemmExtra ex;
+  ex.gate = gate;
+  return launch_gemm(x, K, w, K, resid, N, L, N, K, GEMM_RESIDUAL,
+                     reinterpret_cast<cudaStream_t>(stream), &ex);
+}
+
 static h3_status check_block_config(const h3_block_config* c) {
   H3_REQUIRE(c != nullptr, H3_ERR_INVALID_ARG, "config is NULL");
   h3_status st = check_rows(c->S, c->L);
@@ -426,7 +496,7 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // Workspace slices (bf16, S rows each): h [D] (h1, later h2), qkv [3D],
 // attn [D], proj [D] (attention projection, later FFN down), ffn [F].
 struct BlockWs {
-  size_t h, qkv, attn, proj, ffn, total;
+  size_t h, qkv, attn, proj, ffn, rope, total;
 };
 static BlockWs block_ws(const h3_block_config* c) {
   BlockWs w;
@@ -437,6 +507,7 @@ static BlockWs block_ws(const h3_block_config* c) {
   w.attn = off; off += align256(row * c->D);
   w.proj = off; off += align256(row * c->D);
   w.ffn = off;  off += align256(row * c->F);
+  w.rope = off; off += align256(static_cast<size_t>(c->S) * 64 * sizeof(float2));
   w.total = off;
   return w;
 }
@@ -459,10 +530,14 @@ static h3_status check_weights(const h3_block_weights* w) {
 
 // Runs num_blocks blocks in order over the residual stream. Block b uses
 // w[b] and the modulation table mod + b * num_seg * 6 * D ([num_seg, 6, D]);
-// with seg given, row i uses group seg[i] of that table. The residual update
-// that ends block b and the modulated LayerNorm that starts block b + 1 run
-// as one pass over the residual. events (one block only): recorded before
-// every stage and after the last.
+// with seg given, row i uses group seg[i] of that table. Fusions:
+//   * the RoPE (cos, sin) table is built once (positions are shared by all
+//     blocks) and Q/K RMSNorm + RoPE run in the QKV projection's epilogue;
+//   * the residual update that ends block b and the modulated LayerNorm that
+//     starts block b + 1 run as one pass over the residual;
+//   * the last block's residual update runs in the down projection's
+//     epilogue.
+// events (one block only): recorded before every stage and after the last.
 static h3_status stack_forward_impl(const h3_block_config* cfg, const h3_block_weights* w,
                                     int num_blocks, float* resid, const float* mod, int num_seg,
                                     const int32_t* seg, const int32_t* pos, void* workspace,
@@ -502,6 +577,7 @@ static h3_status stack_forward_impl(const h3_block_config* cfg, const h3_block_w
   void* attn = base + ws.attn;
   void* proj = base + ws.proj;
   void* ffn = base + ws.ffn;
+  float2* rope = reinterpret_cast<float2*>(base + ws.rope);
   const int64_t ld_qkv = 3LL * D;
   const int64_t seg_stride = 6LL * D;  // floats between groups of one table
   const int64_t block_stride = static_cast<int64_t>(num_seg) * seg_stride;
@@ -531,31 +607,45 @@ static h3_status stack_forward_impl(const h3_block_config* cfg, const h3_block_w
     const float* scale2 = m + 4 * D;
     const float* gate2 = m + 5 * D;
     // 0: h1 = LN(r) * (1 + scale1) + shift1 (fused into the previous block's
-    //    last pass for b > 0)
-    if (b == 0) H3_STAGE(0, mnr(nullptr, nullptr, shift1, scale1, h));
-    // 1: [q | k | v] = h1 W_qkv^T
-    H3_STAGE(1, launch_gemm(h, D, wb.w_qkv, D, qkv, ld_qkv, L, 3 * D, D, GEMM_STORE_BF16, s));
-    // 2: q, k <- RoPE(RMSNorm(q, k)) per head
-    H3_STAGE(2, launch_qk_norm_rope(qkv, qkv + 2LL * D, ld_qkv, wb.q_gain, wb.k_gain, pos,
-                                    cfg->axis_dims, L, H, cfg->theta, cfg->eps_qk, s));
-    // 3: a = softmax(q k^T / sqrt(Dh)) v over keys < L
-    H3_STAGE(3, launch_attention(qkv, qkv + 2LL * D, qkv + 4LL * D, ld_qkv, attn, D, L, H,
+    //    last pass for b > 0) and, once, the RoPE table of every row
+    if (b == 0) {
+      H3_STAGE(0, mnr(nullptr, nullptr, shift1, scale1, h));
+      if ((st = launch_rope_table(pos, cfg->axis_dims, L, cfg->theta, rope, s)) != H3_OK)
+        return st;
+    }
+    // 1: [q | k | v] = h1 W_qkv^T; q, k <- RoPE(RMSNorm(q, k)) per head in the
+    //    epilogue
+    GemmExtra qk;
+    qk.q_gain = wb.q_gain;
+    qk.k_gain = wb.k_gain;
+    qk.rope = rope;
+    qk.d_model = D;
+    qk.eps = cfg->eps_qk;
+    H3_STAGE(1, launch_gemm(h, D, wb.w_qkv, D, qkv, ld_qkv, L, 3 * D, D, GEMM_QK_NORM_ROPE, s,
+                            &qk));
+    // 2: a = softmax(q k^T / sqrt(Dh)) v over keys < L
+    H3_STAGE(2, launch_attention(qkv, qkv + 2LL * D, qkv + 4LL * D, ld_qkv, attn, D, L, H,
                                  1.0f / sqrtf(static_cast<float>(cfg->Dh)), s));
-    // 4: o = a W_o^T
-    H3_STAGE(4, launch_gemm(attn, D, wb.w_o, D, proj, D, L, D, D, GEMM_STORE_BF16, s));
-    // 5: r <- r + gate1 * o ; h2 = LN(r) * (1 + scale2) + shift2
-    H3_STAGE(5, mnr(proj, gate1, shift2, scale2, h));
-    // 6: s = SiLU(h2 W_g^T) * (h2 W_u^T), SwiGLU fused in the projection's epilogue
-    H3_STAGE(6, launch_gemm(h, D, wb.w_gu, D, ffn, F, L, F, D, GEMM_SWIGLU, s));
-    // 7: f = s W_down^T
-    H3_STAGE(7, launch_gemm(ffn, F, wb.w_down, F, proj, D, L, D, F, GEMM_STORE_BF16, s));
-    // 8: r <- r + gate2 * f, and for b + 1 < num_blocks the next block's
-    //    h1 = LN(r) * (1 + scale1') + shift1' in the same pass
+    // 3: o = a W_o^T
+    H3_STAGE(3, launch_gemm(attn, D, wb.w_o, D, proj, D, L, D, D, GEMM_STORE_BF16, s));
+    // 4: r <- r + gate1 * o ; h2 = LN(r) * (1 + scale2) + shift2
+    H3_STAGE(4, mnr(proj, gate1, shift2, scale2, h));
+    // 5: s = SiLU(h2 W_g^T) * (h2 W_u^T), SwiGLU fused in the projection's epilogue
+    H3_STAGE(5, launch_gemm(h, D, wb.w_gu, D, ffn, F, L, F, D, GEMM_SWIGLU, s));
+    // 6: f = s W_down^T; r <- r + gate2 * f, in the epilogue for the last
+    //    block, else in one pass with the next block's
+    //    h1 = LN(r) * (1 + scale1') + shift1'
     if (b + 1 < num_blocks) {
       const float* mn = mod + (b + 1) * block_stride;
-      H3_STAGE(8, mnr(proj, gate2, mn, mn + D, h));
+      H3_STAGE(6, launch_gemm(ffn, F, wb.w_down, F, proj, D, L, D, F, GEMM_STORE_BF16, s));
+      if ((st = mnr(proj, gate2, mn, mn + D, h)) != H3_OK) return st;
     } else {
-      H3_STAGE(8, mnr(proj, gate2, nullptr, nullptr, nullptr));
+      GemmExtra res;
+      res.gate = gate2;
+      res.seg = seg;
+      res.num_seg = num_seg;
+      res.seg_stride = seg_stride;
+      H3_STAGE(6, launch_gemm(ffn, F, wb.w_down, F, resid, D, L, D, F, GEMM_RESIDUAL, s, &res));
     }
   }
 #undef H3_STAGE
@@ -757,6 +847,15 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
   void* ffn = base + ws.bf.ffn;
   void* codes = base + ws.codes;
   float* sc = reinterpret_cast<float*>(base + ws.scales);
+  float2* rope = reinterpret_cast<float2*>(base + ws.bf.rope);
+  GemmExtra qk;
+  qk.q_gain = w->q_gain;
+  qk.k_gain = w->k_gain;
+  qk.rope = rope;
+  qk.d_model = D;
+  qk.eps = cfg->eps_qk;
+  GemmExtra res;
+  res.gate = mod + 5 * D;
   const int64_t ld_qkv = 3LL * D;
   const float* m = mod;
   auto quant = [&](const void* x, int K) {
@@ -781,11 +880,10 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
   };
   if ((st = launch_mod_norm_residual(resid, nullptr, nullptr, m, m + D, h, L, D, cfg->eps_ln,
                                      s)) != H3_OK ||
+      (st = launch_rope_table(pos, cfg->axis_dims, L, cfg->theta, rope, s)) != H3_OK ||
       (st = quant(h, D)) != H3_OK ||
       (st = launch_gemm_fp8(codes, D, sc, w->w_qkv, D, w->s_qkv, qkv, ld_qkv, L, 3 * D, D,
-                            GEMM_STORE_BF16, s)) != H3_OK ||
-      (st = launch_qk_norm_rope(qkv, qkv + 2LL * D, ld_qkv, w->q_gain, w->k_gain, pos,
-                                cfg->axis_dims, L, H, cfg->theta, cfg->eps_qk, s)) != H3_OK ||
+                            GEMM_QK_NORM_ROPE, s, &qk)) != H3_OK ||
       (st = attention(qkv, attn)) != H3_OK ||
       (st = quant(attn, D)) != H3_OK ||
       (st = launch_gemm_fp8(codes, D, sc, w->w_o, D, w->s_o, proj, D, L, D, D, GEMM_STORE_BF16,
@@ -796,11 +894,10 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
       (st = launch_gemm_fp8(codes, D, sc, w->w_gu, D, w->s_gu, ffn, F, L, F, D, GEMM_SWIGLU,
                             s)) != H3_OK ||
       (st = quant(ffn, F)) != H3_OK ||
-      (st = launch_gemm_fp8(codes, F, sc, w->w_down, F, w->s_down, proj, D, L, D, F,
-                            GEMM_STORE_BF16, s)) != H3_OK)
+      (st = launch_gemm_fp8(codes, F, sc, w->w_down, F, w->s_down, resid, D, L, D, F,
+                            GEMM_RESIDUAL, s, &res)) != H3_OK)
     return st;
-  return launch_mod_norm_residual(resid, proj, m + 5 * D, nullptr, nullptr, nullptr, L, D,
-                                  cfg->eps_ln, s);
+  return H3_OK;
 }
 
 // Scratch of h3_block_forward_noalloc: a fixed array in the library's device

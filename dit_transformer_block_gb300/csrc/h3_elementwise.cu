@@ -73,6 +73,31 @@ struct RopeTable {
   int axis[QK_HEAD_DIM / 2];      // which position (t, h, w) drives the pair
 };
 
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
+
+// Angle of pair pr at position p: formed and reduced modulo 2*pi in FP64,
+// then sin/cos in FP32 on an argument in [-pi, pi].
+__device__ __forceinline__ void rope_angle(int32_t p, double omega, float& sn, float& cs) {
+  const double phi = static_cast<double>(p) * omega;
+  const double turns = rint(phi * kInvTwoPi);
+  const float red = static_cast<float>(fma(-turns, kTwoPi, phi));
+  sincosf(red, &sn, &cs);
+}
+
+// One thread per (row, pair): out[row * 64 + pr] = (cos, sin).
+__global__ void __launch_bounds__(256)
+    rope_table_kernel(const int32_t* __restrict__ pos, int L, const RopeTable tab,
+                      float2* __restrict__ out) {
+  const int64_t i = blockIdx.x * 256LL + threadIdx.x;
+  if (i >= static_cast<int64_t>(L) * (QK_HEAD_DIM / 2)) return;
+  const int64_t row = i / (QK_HEAD_DIM / 2);
+  const int pr = static_cast<int>(i - row * (QK_HEAD_DIM / 2));
+  float sn, cs;
+  rope_angle(__ldg(pos + 3 * row + tab.axis[pr]), tab.omega[pr], sn, cs);
+  out[i] = make_float2(cs, sn);
+}
+
 __global__ void __launch_bounds__(QK_WARPS * 32)
     qk_norm_rope_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
                         int64_t row_stride, const float* __restrict__ q_gain,
@@ -92,19 +117,13 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
   const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp + 4));
   const float gain[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 
-  // Angles of this lane's pairs: formed and reduced modulo 2*pi in FP64,
-  // then sin/cos in FP32 on an argument in [-pi, pi].
+  // Angles of this lane's pairs
   const int32_t p3[3] = {__ldg(pos + 3 * row), __ldg(pos + 3 * row + 1), __ldg(pos + 3 * row + 2)};
   float cs[4], sn[4];
-  constexpr double kTwoPi = 6.283185307179586476925286766559;
-  constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const int pr = sub * 4 + t;
-    const double phi = static_cast<double>(p3[tab.axis[pr]]) * tab.omega[pr];
-    const double turns = rint(phi * kInvTwoPi);
-    const float red = static_cast<float>(fma(-turns, kTwoPi, phi));
-    sincosf(red, &sn[t], &cs[t]);
+    rope_angle(p3[tab.axis[pr]], tab.omega[pr], sn[t], cs[t]);
   }
 
   for (int h0 = 0; h0 < H; h0 += 2 * QK_BATCH) {
@@ -401,9 +420,7 @@ h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream
   return cuda_fail(cudaGetLastError(), "swiglu launch");
 }
 
-h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float* q_gain,
-                              const float* k_gain, const int32_t* pos, const int* axis_dims,
-                              int L, int H, float theta, float eps, cudaStream_t s) {
+static RopeTable rope_table(const int* axis_dims, float theta) {
   RopeTable tab;
   int pr = 0;
   for (int a = 0; a < 3; ++a) {
@@ -413,6 +430,22 @@ h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float*
       tab.axis[pr] = a;
     }
   }
+  return tab;
+}
+
+h3_status launch_rope_table(const int32_t* pos, const int* axis_dims, int L, float theta,
+                            float2* out, cudaStream_t s) {
+  const RopeTable tab = rope_table(axis_dims, theta);
+  const int64_t n = static_cast<int64_t>(L) * (QK_HEAD_DIM / 2);
+  const int grid = static_cast<int>((n + 255) / 256);
+  rope_table_kernel<<<grid, 256, 0, s>>>(pos, L, tab, out);
+  return cuda_fail(cudaGetLastError(), "rope_table launch");
+}
+
+h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float* q_gain,
+                              const float* k_gain, const int32_t* pos, const int* axis_dims,
+                              int L, int H, float theta, float eps, cudaStream_t s) {
+  const RopeTable tab = rope_table(axis_dims, theta);
   const int64_t warps = 2LL * L;
   const int grid = static_cast<int>((warps + QK_WARPS - 1) / QK_WARPS);
   qk_norm_rope_kernel<<<grid, QK_WARPS * 32, 0, s>>>(

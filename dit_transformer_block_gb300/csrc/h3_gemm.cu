@@ -14,9 +14,17 @@
 //   * two 256-column FP32 accumulators in TMEM so the epilogue of one tile
 //     overlaps the main loop of the next;
 //   * rows >= L are zero-filled by TMA on load and never stored.
-// Epilogues: plain bf16 store, or SwiGLU where the B tile's first 128 rows are
-// gate rows and the last 128 the matching up rows, and the 128 output columns
-// are SiLU(g) * u (both rounded to bf16 first, like the unfused path).
+// Epilogues (each rounds the product to bf16 first, like the unfused path):
+//   * plain bf16 store;
+//   * SwiGLU: the B tile's first 128 rows are gate rows and the last 128 the
+//     matching up rows; the 128 output columns are SiLU(g) * u;
+//   * residual: C is the FP32 residual stream and gets gate[col] * bf16(acc)
+//     added with one fma, the arithmetic of the modulation kernel's residual
+//     step, so the block's residual update needs no pass of its own;
+//   * Q/K RMSNorm + RoPE: a 256-column tile is two 128-channel heads; a q or k
+//     head of the thread's row is normalised by its RMS (a first pass over its
+//     TMEM columns), scaled by the gain and rotated pair by pair with the row's
+//     (cos, sin) table, then stored; v columns are stored as they are.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -46,6 +54,7 @@ struct GemmArgs {
   int num_tiles;
   int ep;                 // GemmEpilogue
   int b_half_rows;        // SwiGLU: row offset of the up half inside B
+  GemmExtra x;            // operands of the residual and Q/K-norm epilogues
   DevErr err;
 };
 
@@ -60,6 +69,23 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmArgs& a, int& mb
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// 32 accumulator columns of this thread's row, FP8-scaled when FP8, each
+// rounded to bf16 (returned as floats).
+template <bool FP8>
+__device__ __forceinline__ void load_chunk_bf16(uint32_t taddr, float sa_row, const float* sb,
+                                                float (&x)[32]) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  tmem_ld_wait();
+  tmem_reg_fence(v);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float f = __uint_as_float(v[j]);
+    if constexpr (FP8) f *= sa_row * __ldg(sb + j);
+    x[j] = round_to_bf16(f);
+  }
+}
 
 // FP8 == true: A and B hold E4M3 codes (kind::f8f6f4, K = 32 per MMA, 128
 // codes per 128-byte row of a stage) and the epilogue multiplies the FP32
@@ -235,6 +261,72 @@ __global__ void __launch_bounds__(THREADS, 1)
               dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
           }
         }
+      } else if (a.ep == GEMM_RESIDUAL) {
+        const int col0 = nb * BN;
+        float* rrow = static_cast<float*>(a.C) + static_cast<int64_t>(row) * a.ldc + col0;
+        const float* grow = a.x.gate + col0;
+        if (a.x.seg != nullptr && row_ok)
+          grow += static_cast<int64_t>(min(max(__ldg(a.x.seg + row), 0), a.x.num_seg - 1)) *
+                  a.x.seg_stride;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float f[32];
+          load_chunk_bf16<FP8>(t_row + c * 32, sa_row, a.sb + col0 + c * 32, f);
+          if (row_ok) {
+            float4* rp = reinterpret_cast<float4*>(rrow + c * 32);
+            const float4* gp = reinterpret_cast<const float4*>(grow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float4 r = rp[q];
+              const float4 g = __ldg(gp + q);
+              r.x = fmaf(g.x, f[4 * q + 0], r.x);
+              r.y = fmaf(g.y, f[4 * q + 1], r.y);
+              r.z = fmaf(g.z, f[4 * q + 2], r.z);
+              r.w = fmaf(g.w, f[4 * q + 3], r.w);
+              rp[q] = r;
+            }
+          }
+        }
+      } else if (a.ep == GEMM_QK_NORM_ROPE && nb * BN < 2 * a.x.d_model) {
+        const float2* rope = a.x.rope + static_cast<int64_t>(row_ok ? row : 0) * 64;
+#pragma unroll 1
+        for (int hh = 0; hh < BN / 128; ++hh) {
+          const int hcol = nb * BN + hh * 128;
+          const float* gain = hcol < a.x.d_model ? a.x.q_gain : a.x.k_gain;
+          const uint32_t t_head = t_row + hh * 128;
+          // pass 1: sum of squares of the bf16-rounded head
+          float ss = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float f[32];
+            load_chunk_bf16<FP8>(t_head + c * 32, sa_row, a.sb + hcol + c * 32, f);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ss = fmaf(f[j], f[j], ss);
+          }
+          const float inv = rsqrtf(ss * (1.0f / 128.0f) + a.x.eps);
+          // pass 2: scale, gain, rotate, store
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float f[32];
+            load_chunk_bf16<FP8>(t_head + c * 32, sa_row, a.sb + hcol + c * 32, f);
+            uint32_t o[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              const float2 r = __ldg(rope + c * 16 + t);
+              const float g0 = __ldg(gain + c * 32 + 2 * t);
+              const float g1 = __ldg(gain + c * 32 + 2 * t + 1);
+              const float x0 = f[2 * t] * inv * g0;
+              const float x1 = f[2 * t + 1] * inv * g1;
+              o[t] = pack_bf16x2(x0 * r.x - x1 * r.y, x0 * r.y + x1 * r.x);
+            }
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(crow + hcol + c * 32);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            }
+          }
+        }
       } else {
         const int col0 = nb * BN;
 #pragma unroll 1
@@ -282,7 +374,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <bool FP8>
 static h3_status launch_gemm_impl(const void* A, int64_t lda_bytes, const float* sa, const void* B,
                                   int64_t ldb_bytes, const float* sb, void* C, int64_t ldc, int L,
-                                  int N, int K, GemmEpilogue ep, cudaStream_t s) {
+                                  int N, int K, GemmEpilogue ep, cudaStream_t s,
+                                  const GemmExtra* extra) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -303,6 +396,7 @@ static h3_status launch_gemm_impl(const void* A, int64_t lda_bytes, const float*
   a.N = N;
   a.K = K;
   a.ep = ep;
+  if (extra != nullptr) a.x = *extra;
   const int b_rows = (ep == GEMM_SWIGLU) ? 2 * N : N;
   const int tile_n = (ep == GEMM_SWIGLU) ? BN / 2 : BN;
   a.b_half_rows = (ep == GEMM_SWIGLU) ? N : 0;
@@ -327,14 +421,16 @@ static h3_status launch_gemm_impl(const void* A, int64_t lda_bytes, const float*
 }
 
 h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-                      int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s) {
-  return launch_gemm_impl<false>(A, lda * 2, nullptr, B, ldb * 2, nullptr, C, ldc, L, N, K, ep, s);
+                      int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s,
+                      const GemmExtra* extra) {
+  return launch_gemm_impl<false>(A, lda * 2, nullptr, B, ldb * 2, nullptr, C, ldc, L, N, K, ep, s,
+                                 extra);
 }
 
 h3_status launch_gemm_fp8(const void* A, int64_t lda, const float* sa, const void* B, int64_t ldb,
                           const float* sb, void* C, int64_t ldc, int L, int N, int K,
-                          GemmEpilogue ep, cudaStream_t s) {
-  return launch_gemm_impl<true>(A, lda, sa, B, ldb, sb, C, ldc, L, N, K, ep, s);
+                          GemmEpilogue ep, cudaStream_t s, const GemmExtra* extra) {
+  return launch_gemm_impl<true>(A, lda, sa, B, ldb, sb, C, ldc, L, N, K, ep, s, extra);
 }
 
 }  // namespace h3

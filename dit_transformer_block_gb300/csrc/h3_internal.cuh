@@ -39,26 +39,53 @@ h3_status launch_mod_norm_residual(float* resid, const void* delta, const float*
                                    int D, float eps, cudaStream_t s, const int32_t* seg = nullptr,
                                    int num_seg = 1, int64_t seg_stride = 0);
 
+// (cos, sin) of every RoPE angle of rows [0, L): out[i * 64 + p] for channel
+// pair p of a 128-channel head, the angle formed and reduced exactly as
+// launch_qk_norm_rope does.
+h3_status launch_rope_table(const int32_t* pos, const int* axis_dims, int L, float theta,
+                            float2* out, cudaStream_t s);
+
 // frames [B, C, N] float32 (N = T*H*W, N % 4 == 0) -> [B, N, C] uint8.
 h3_status launch_frames_to_u8(const float* in, uint8_t* out, int B, int C, int64_t N,
                               cudaStream_t s);
 
 enum GemmEpilogue : int {
-  GEMM_STORE_BF16 = 0,   // C = bf16(acc)
-  GEMM_SWIGLU = 1,       // B rows [gate | up] of F each; C[:, j] = SiLU(g) * u, width F
+  GEMM_STORE_BF16 = 0,     // C = bf16(acc)
+  GEMM_SWIGLU = 1,         // B rows [gate | up] of F each; C[:, j] = SiLU(g) * u, width F
+  GEMM_RESIDUAL = 2,       // C is the FP32 residual: C[:, j] += gate[j] * bf16(acc)
+  GEMM_QK_NORM_ROPE = 3,   // C = bf16(acc), then RMSNorm + RoPE on the q and k heads
+};
+// Operands of the fused epilogues (unused fields may stay zero).
+struct GemmExtra {
+  // GEMM_RESIDUAL: per-column gate [N]; with seg, row i reads the gate at
+  // gate + clamp(seg[i], 0, num_seg - 1) * seg_stride.
+  const float* gate = nullptr;
+  const int32_t* seg = nullptr;
+  int num_seg = 1;
+  int64_t seg_stride = 0;
+  // GEMM_QK_NORM_ROPE: columns [0, d_model) are q heads, [d_model, 2 d_model)
+  // k heads (128 channels each), the rest pass through; every head of a row is
+  // rounded to bf16, scaled by 1/rms and its gain, rotated by the row's
+  // (cos, sin) table [L, 64] (h3::launch_rope_table) and rounded again.
+  const float* q_gain = nullptr;
+  const float* k_gain = nullptr;
+  const float2* rope = nullptr;
+  int d_model = 0;
+  float eps = 0.f;
 };
 // C[:L, :] = epilogue(A[:L, :K] @ B^T). A row stride lda, B [N, K] row stride
-// ldb, C row stride ldc (elements). For GEMM_SWIGLU, N is the width of C (= F)
-// and B holds 2N rows.
+// ldb, C row stride ldc (elements of C). For GEMM_SWIGLU, N is the width of C
+// (= F) and B holds 2N rows.
 h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-                      int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s);
+                      int64_t ldc, int L, int N, int K, GemmEpilogue ep, cudaStream_t s,
+                      const GemmExtra* extra = nullptr);
 
 // FP8 (E4M3) operands with per-row scales: C[:L] = epilogue(bf16-free
 // (A @ B^T) * sa[row] * sb[col]). A [L, K] codes (row stride lda bytes), B
 // [N or 2N, K] codes (row stride ldb bytes), sa [L], sb [N or 2N].
 h3_status launch_gemm_fp8(const void* A, int64_t lda, const float* sa, const void* B, int64_t ldb,
                           const float* sb, void* C, int64_t ldc, int L, int N, int K,
-                          GemmEpilogue ep, cudaStream_t s);
+                          GemmEpilogue ep, cudaStream_t s, const GemmExtra* extra = nullptr);
 // Per-row absmax quantisation of bf16 x [R, K] (row stride ldx elements) to
 // E4M3 codes q [R, K] (row stride ldq bytes) and float32 scales [R].
 h3_status launch_quantize_fp8_rows(const void* x, int64_t ldx, void* q, int64_t ldq, float* scale,

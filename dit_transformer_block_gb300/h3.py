@@ -68,6 +68,9 @@ _SIGS = {
     "h3_attention_varlen_skip": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P]),
     "h3_linear": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_linear_swiglu": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "h3_rope_table": (_I, [_P, _P, _I, _I, _F, _P, _P]),
+    "h3_linear_qk_norm_rope": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
+    "h3_linear_residual": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_block_workspace_bytes": (_SZ, [ctypes.POINTER(BlockConfig)]),
     "h3_block_forward": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), _P, _P,
                               _P, _P, _SZ, _P]),
@@ -284,6 +287,42 @@ def linear_swiglu(x, w_gu, out, L=None, stream=None):
                                                     _s(stream)))
 
 
+def rope_table(pos, axis_dims, table, L=None, theta=1e4, stream=None):
+    """table[:L] = (cos, sin) of every RoPE angle; pos [S,3] int32, table [S,64,2] f32."""
+    _need(pos, torch.int32, "pos")
+    _need(table, torch.float32, "table")
+    S = pos.shape[0]
+    L = S if L is None else L
+    ax = (ctypes.c_int * 3)(*axis_dims)
+    _check("rope_table", lib().h3_rope_table(_p(pos), ctypes.cast(ax, ctypes.c_void_p), S, L,
+                                              theta, _p(table), _s(stream)))
+
+
+def linear_qk_norm_rope(x, w_qkv, qkv, q_gain, k_gain, table, L=None, eps=1e-6, stream=None):
+    """qkv[:L] = x @ w_qkv^T with per-head Q/K RMSNorm + RoPE (table from
+    rope_table) in the epilogue; x [S,K], w_qkv [3D,K], qkv [S,3D] bf16."""
+    for n, t in (("x", x), ("w_qkv", w_qkv), ("qkv", qkv)):
+        _need(t, torch.bfloat16, n)
+    S, K = x.shape
+    H = w_qkv.shape[0] // 3 // 128
+    L = S if L is None else L
+    _check("linear_qk_norm_rope", lib().h3_linear_qk_norm_rope(
+        _p(x), _p(w_qkv), _p(qkv), _p(q_gain), _p(k_gain), _p(table), S, L, H, K, eps,
+        _s(stream)))
+
+
+def linear_residual(x, w, resid, gate, L=None, stream=None):
+    """resid[:L] += gate * bf16(x @ w^T) in FP32; x [S,K], w [N,K] bf16, resid [S,N] f32."""
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    _need(resid, torch.float32, "resid")
+    S, K = x.shape
+    N = w.shape[0]
+    L = S if L is None else L
+    _check("linear_residual", lib().h3_linear_residual(_p(x), _p(w), _p(resid), _p(gate), S, L,
+                                                        N, K, _s(stream)))
+
+
 def block_config(S, L, D, H, Dh, F, axis_dims, theta=1e4, eps_ln=1e-6, eps_qk=1e-6) -> BlockConfig:
     return BlockConfig(S, L, D, H, Dh, F, (ctypes.c_int * 3)(*axis_dims), theta, eps_ln, eps_qk)
 
@@ -392,9 +431,11 @@ def block_workspace_bytes(cfg: BlockConfig) -> int:
     return n
 
 
-BLOCK_STAGES = 9
-STAGE_NAMES = ("mod_norm", "qkv_proj", "qk_norm_rope", "attention", "out_proj",
-               "residual_mod_norm", "gate_up_swiglu", "down_proj", "residual")
+BLOCK_STAGES = 7
+STAGE_NAMES = ("mod_norm", "qkv_proj_qk_norm_rope", "attention", "out_proj",
+               "residual_mod_norm", "gate_up_swiglu", "down_proj_residual")
+# kernels one block launches: the stages plus the RoPE table pass
+BLOCK_LAUNCHES = BLOCK_STAGES + 1
 
 
 def block_weights(weights: dict) -> BlockWeights:

@@ -196,6 +196,49 @@ h3_status h3_linear(const void* x, const void* w, void* y, int S, int L, int N, 
 h3_status h3_linear_swiglu(const void* x, const void* w_gu, void* out, int S, int L, int F,
                            int K, h3_stream_t stream);
 
+/*
+ * a2 inputs, precomputed — the (cos, sin) of every RoPE angle of rows < L
+ * (blog section 3.2: Q/K RMSNorm and RoPE fused, here into the QKV
+ * projection's epilogue, which reads this table):
+ *   table[i, p] = (cos phi, sin phi), phi = pos[i, a] * theta^(-2j / axis_dims[a])
+ * for channel pair p of a 128-channel head (section a, pair j within it, as in
+ * h3_qk_norm_rope), angle formed and reduced in FP64, cos/sin in FP32.
+ *   pos   [S, 3] int32; axis_dims HOST [3], even, sum 128
+ *   table [S, 64, 2] float32 (rows >= L not written)
+ */
+h3_status h3_rope_table(const int32_t* pos, const int* axis_dims, int S, int L, float theta,
+                        float* table, h3_stream_t stream);
+
+/*
+ * a4 + a2 fused — the QKV projection with Q/K RMSNorm + RoPE in its epilogue
+ * (blog section 3.2: the small ops around the projections fused):
+ *   qkv[i, :] = bf16(x[i, :] @ w_qkv^T) for i < L, then every q head (columns
+ *   [0, 128H)) and k head (columns [128H, 256H)) of row i is normalised,
+ *   scaled by q_gain / k_gain and rotated with table row i exactly as
+ *   h3_qk_norm_rope would do it; v columns are the plain product.
+ *   x [S, K] bf16, w_qkv [384H, K] bf16, qkv [S, 384H] bf16
+ *   q_gain, k_gain [128] float32; rope_table from h3_rope_table
+ * H even, K % 64 == 0. Equals h3_linear followed by h3_qk_norm_rope up to the
+ * order of the FP32 sum of squares inside the RMS.
+ */
+h3_status h3_linear_qk_norm_rope(const void* x, const void* w_qkv, void* qkv,
+                                 const float* q_gain, const float* k_gain,
+                                 const float* rope_table, int S, int L, int H, int K, float eps,
+                                 h3_stream_t stream);
+
+/*
+ * a4 + a1 fused — a projection whose product goes straight into the FP32
+ * residual stream (blog section 3.2: FP32 residual merged into the
+ * surrounding ops):
+ *   resid[i, n] = fma(gate[n], bf16(x[i, :] . w[n, :]), resid[i, n])   for i < L
+ * which is h3_linear followed by the residual step of h3_mod_norm_residual,
+ * bit for bit.
+ *   x [S, K] bf16, w [N, K] bf16, resid [S, N] float32 in/out, gate [N] float32
+ * N % 256 == 0, K % 64 == 0.
+ */
+h3_status h3_linear_residual(const void* x, const void* w, float* resid, const float* gate,
+                             int S, int L, int N, int K, h3_stream_t stream);
+
 /* Shape and constants of one block. */
 typedef struct h3_block_config {
   int S;             /* buffer rows                                   */
@@ -239,6 +282,10 @@ size_t h3_block_workspace_bytes(const h3_block_config* cfg);
  *   pos   [S, 3] int32
  *   workspace: device memory of at least h3_block_workspace_bytes(cfg) bytes,
  *   256-byte aligned, owned by the caller, overwritten by the call.
+ * Q/K RMSNorm + RoPE run in the QKV projection's epilogue
+ * (h3_linear_qk_norm_rope), SwiGLU in the gate/up projection's
+ * (h3_linear_swiglu) and the last residual update in the down projection's
+ * (h3_linear_residual).
  */
 h3_status h3_block_forward(const h3_block_config* cfg, const h3_block_weights* w, float* resid,
                            const float* mod, const int32_t* pos, void* workspace,
@@ -347,11 +394,12 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
                                int fp8_attention, void* workspace, size_t workspace_bytes,
                                h3_stream_t stream);
 
-/* Number of kernel stages h3_block_forward launches, in the order listed
- * above: 0 modulation+LN, 1 QKV projection, 2 Q/K RMSNorm+RoPE, 3 attention,
- * 4 output projection, 5 residual+modulation+LN, 6 gate/up projection with
- * SwiGLU, 7 down projection, 8 residual. */
-#define H3_BLOCK_STAGES 9
+/* Number of stages h3_block_forward runs, in the order listed above:
+ * 0 modulation+LN (and the RoPE table), 1 QKV projection with Q/K
+ * RMSNorm+RoPE in its epilogue, 2 attention, 3 output projection,
+ * 4 residual+modulation+LN, 5 gate/up projection with SwiGLU in its epilogue,
+ * 6 down projection with the residual update in its epilogue. */
+#define H3_BLOCK_STAGES 7
 
 /*
  * h3_block_forward, and records events[i] on `stream` just before stage i is

@@ -79,13 +79,40 @@ def test_linear_argument_errors(lib):
     assert st(lib, "h3_linear", P, P, PM, 8, 8, 256, 64, NULL) == 3
     assert st(lib, "h3_linear", P, P, P, 8, 9, 256, 64, NULL) == 1
     assert st(lib, "h3_linear_swiglu", P, P, P, 8, 8, 100, 64, NULL) == 2
+    gain = ctypes.c_void_p(4096)
+    f = "h3_linear_qk_norm_rope"
+    assert st(lib, f, P, P, P, gain, gain, P, 8, 8, 3, 64, 1e-6, NULL) == 2     # odd H
+    assert st(lib, f, P, P, P, gain, gain, P, 8, 8, 2, 60, 1e-6, NULL) == 2     # K % 64
+    assert st(lib, f, P, P, P, gain, gain, NULL, 8, 8, 2, 64, 1e-6, NULL) == 1  # no table
+    assert st(lib, f, P, P, PM, gain, gain, P, 8, 8, 2, 64, 1e-6, NULL) == 3
+    assert st(lib, f, P, P, P, gain, gain, P, 8, 8, 2, 64, -1.0, NULL) == 1     # eps < 0
+    f = "h3_linear_residual"
+    assert st(lib, f, P, P, P, P, 8, 8, 200, 64, NULL) == 2
+    assert st(lib, f, P, P, P, NULL, 8, 8, 256, 64, NULL) == 1                 # no gate
+    assert st(lib, f, P, P, PM, P, 8, 8, 256, 64, NULL) == 3
+    assert st(lib, f, P, P, P, P, 8, 9, 256, 64, NULL) == 1                    # L > S
+
+
+def test_rope_table_argument_errors(lib):
+    f = "h3_rope_table"
+    ax = (ctypes.c_int * 3)(32, 48, 48)
+    bad = (ctypes.c_int * 3)(32, 48, 46)
+    odd = (ctypes.c_int * 3)(33, 47, 48)
+    A = lambda a: ctypes.cast(a, ctypes.c_void_p)
+    assert st(lib, f, P, A(bad), 8, 8, 1e4, P, NULL) == 1
+    assert st(lib, f, P, A(odd), 8, 8, 1e4, P, NULL) == 1
+    assert st(lib, f, P, A(ax), 8, 8, 0.0, P, NULL) == 1
+    assert st(lib, f, NULL, A(ax), 8, 8, 1e4, P, NULL) == 1
+    assert st(lib, f, P, A(ax), 8, 8, 1e4, PM, NULL) == 3
+    assert st(lib, f, P, A(ax), 8, 0, 1e4, P, NULL) == 0                      # L == 0: nothing
 
 
 def test_block_config_and_workspace(lib):
     cfg = h3.block_config(256, 250, 512, 4, 128, 1536, (128, 0, 0))
     n = lib.h3_block_workspace_bytes(ctypes.byref(cfg))
-    # h, attn, proj [S, D] + qkv [S, 3D] + ffn [S, F], bf16, 256-byte aligned slices
-    assert n == 256 * 2 * (512 * 6 + 1536)
+    # h, attn, proj [S, D] + qkv [S, 3D] + ffn [S, F], bf16, and the RoPE
+    # table [S, 64] (cos, sin) float32, 256-byte aligned slices
+    assert n == 256 * 2 * (512 * 6 + 1536) + 256 * 64 * 8
     bad = h3.block_config(256, 250, 500, 4, 128, 1536, (128, 0, 0))
     assert lib.h3_block_workspace_bytes(ctypes.byref(bad)) == 0
     assert "D=" in h3.last_error()
