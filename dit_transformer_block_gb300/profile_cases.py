@@ -6,7 +6,10 @@ Each selected kernel runs twice on inputs larger than L2 (129 MB) but a few
 hundred MB in total, so that an `ncu --set full -k <kernel> -s 1 -c 1`
 capture of the second launch ends within a minute or two:
   attention   S = L = 16384, 42 heads x 128 (q, k, v, o: 704 MB)
-  gemm        M = 8192, N = 16128, K = 5376 (the QKV projection shape; 520 MB)
+  gemm        M = 8192, N = 16128, K = 5376 (the QKV projection shape; 520 MB),
+              plain and with Q/K RMSNorm + RoPE in the epilogue (after its RoPE
+              table), then the down projection shape M = 8192, N = 5376,
+              K = 14336 with the residual update in the epilogue (565 MB)
   elementwise qk_norm_rope on 16384 x 42 x 128, SwiGLU on 16384 x 2 x 14336,
               modulation/LN/residual on 16384 x 5376
   fp8         FP8 GEMM (QKV shape, M = 8192), per-row FP8 quantisation of
@@ -40,6 +43,16 @@ def main(argv):
         x, w = rnd(M, K), rnd(N, K, std=0.02)
         y = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
         runs.append(lambda: h3.linear(x, w, y, M))
+        from dit_transformer_block_gb300 import inputs as I
+        pos = I.positions_3d(M, M, grid=(31, 24, 79), n_tail=22).to(dev)
+        tab = torch.empty(M, 64, 2, device=dev)
+        gains = torch.ones(128, device=dev)
+        runs.append(lambda: h3.rope_table(pos, (32, 48, 48), tab, M))
+        runs.append(lambda: h3.linear_qk_norm_rope(x, w, y, gains, gains, tab, M))
+        xd, wd = rnd(M, 14336), rnd(5376, 14336, std=0.02)
+        rd = torch.randn(M, 5376, generator=g, device=dev)
+        gate = torch.randn(5376, generator=g, device=dev) * 0.1
+        runs.append(lambda: h3.linear_residual(xd, wd, rd, gate, M))
     if "elementwise" in which:
         S = 16384
         qq, kk = rnd(S, 42, 128), rnd(S, 42, 128)
