@@ -531,8 +531,9 @@ static h3_status check_weights(const h3_block_weights* w) {
 // Runs num_blocks blocks in order over the residual stream. Block b uses
 // w[b] and the modulation table mod + b * num_seg * 6 * D ([num_seg, 6, D]);
 // with seg given, row i uses group seg[i] of that table. Fusions:
-//   * the RoPE (cos, sin) table is built once (positions are shared by all
-//     blocks) and Q/K RMSNorm + RoPE run in the QKV projection's epilogue;
+//   * the RoPE (cos, sin) table is built once, by the first modulated
+//     LayerNorm pass (positions are shared by all blocks), and Q/K RMSNorm +
+//     RoPE run in the QKV projection's epilogue;
 //   * the residual update that ends block b and the modulated LayerNorm that
 //     starts block b + 1 run as one pass over the residual;
 //   * the last block's residual update runs in the down projection's
@@ -586,9 +587,9 @@ static h3_status stack_forward_impl(const h3_block_config* cfg, const h3_block_w
     return cuda_fail(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s), "event record");
   };
   auto mnr = [&](const void* delta, const float* gate, const float* shift, const float* scale,
-                 void* normed) {
+                 void* normed, const RopeRequest* rope = nullptr) {
     return launch_mod_norm_residual(resid, delta, gate, shift, scale, normed, L, D, cfg->eps_ln,
-                                    s, seg, num_seg, seg_stride);
+                                    s, seg, num_seg, seg_stride, rope);
   };
 #define H3_STAGE(i, call)                          \
   do {                                             \
@@ -607,11 +608,11 @@ static h3_status stack_forward_impl(const h3_block_config* cfg, const h3_block_w
     const float* scale2 = m + 4 * D;
     const float* gate2 = m + 5 * D;
     // 0: h1 = LN(r) * (1 + scale1) + shift1 (fused into the previous block's
-    //    last pass for b > 0) and, once, the RoPE table of every row
+    //    last pass for b > 0); the same pass writes the RoPE table of every
+    //    row, once per call
     if (b == 0) {
-      H3_STAGE(0, mnr(nullptr, nullptr, shift1, scale1, h));
-      if ((st = launch_rope_table(pos, cfg->axis_dims, L, cfg->theta, rope, s)) != H3_OK)
-        return st;
+      const RopeRequest rq{pos, cfg->axis_dims, cfg->theta, rope};
+      H3_STAGE(0, mnr(nullptr, nullptr, shift1, scale1, h, &rq));
     }
     // 1: [q | k | v] = h1 W_qkv^T; q, k <- RoPE(RMSNorm(q, k)) per head in the
     //    epilogue
@@ -878,9 +879,9 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
     if (r != H3_OK) return r;
     return launch_attention_fp8(aq, ak, av, D, sq, sk, sv, out, D, L, H, sm_scale, s);
   };
+  const RopeRequest rq{pos, cfg->axis_dims, cfg->theta, rope};
   if ((st = launch_mod_norm_residual(resid, nullptr, nullptr, m, m + D, h, L, D, cfg->eps_ln,
-                                     s)) != H3_OK ||
-      (st = launch_rope_table(pos, cfg->axis_dims, L, cfg->theta, rope, s)) != H3_OK ||
+                                     s, nullptr, 1, 0, &rq)) != H3_OK ||
       (st = quant(h, D)) != H3_OK ||
       (st = launch_gemm_fp8(codes, D, sc, w->w_qkv, D, w->s_qkv, qkv, ld_qkv, L, 3 * D, D,
                             GEMM_QK_NORM_ROPE, s, &qk)) != H3_OK ||

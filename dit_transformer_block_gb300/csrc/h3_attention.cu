@@ -449,18 +449,10 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
 
 template <bool F8, bool SKIP>
 static h3_status set_attention_smem() {
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    const size_t bytes = F8 ? 1024 + (2 + KV_SLOTS) * (TILE_BYTES / 2) + 256 : Q2_SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel<F8, SKIP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
-    if (e != cudaSuccess) return cuda_fail(e, "attention: set shared memory size");
-    attr_done[dev] = true;
-  }
-  return H3_OK;
+  static std::atomic<bool> done[64];
+  const size_t bytes = F8 ? 1024 + (2 + KV_SLOTS) * (TILE_BYTES / 2) + 256 : Q2_SMEM_BYTES;
+  return set_smem_limit(done, attention_kernel<F8, SKIP>, bytes,
+                        "attention: set shared memory size");
 }
 
 h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,

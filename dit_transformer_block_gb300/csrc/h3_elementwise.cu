@@ -187,13 +187,16 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // seg (optional): token-group index of every row; group g reads its gate,
 // shift and scale at an offset of g * seg_stride floats (a [G, 6, D] table).
 // Indices outside [0, num_seg) are clamped so every read stays in the table.
-template <int VPT>
+// ROPE: the CTA also writes its row of the RoPE (cos, sin) table (threads
+// 0-63, one pair each, while the row's loads are in flight).
+template <int VPT, bool ROPE>
 __global__ void __launch_bounds__(MNR_THREADS)
     mod_norm_residual_kernel(float* __restrict__ resid, const __nv_bfloat16* __restrict__ delta,
                              const float* __restrict__ gate, const float* __restrict__ shift,
                              const float* __restrict__ scale, __nv_bfloat16* __restrict__ normed,
                              int D, float eps, const int32_t* __restrict__ seg, int num_seg,
-                             int64_t seg_stride) {
+                             int64_t seg_stride, const int32_t* __restrict__ pos,
+                             float2* __restrict__ rope_out, const RopeTable tab) {
   __shared__ float red[MNR_THREADS / 32];
   const int row = blockIdx.x;
   if (seg != nullptr) {
@@ -210,6 +213,14 @@ __global__ void __launch_bounds__(MNR_THREADS)
   for (int v = 0; v < VPT; ++v) {
     const int c = threadIdx.x + v * MNR_THREADS;
     x[v] = c < D4 ? rrow[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if constexpr (ROPE) {
+    const int t = threadIdx.x;
+    if (t < QK_HEAD_DIM / 2) {
+      float sn, cs;
+      rope_angle(__ldg(pos + 3LL * row + tab.axis[t]), tab.omega[t], sn, cs);
+      rope_out[static_cast<int64_t>(row) * (QK_HEAD_DIM / 2) + t] = make_float2(cs, sn);
+    }
   }
   if (delta != nullptr) {
     const uint2* drow = reinterpret_cast<const uint2*>(delta + static_cast<int64_t>(row) * D);
@@ -457,14 +468,24 @@ h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float*
 h3_status launch_mod_norm_residual(float* resid, const void* delta, const float* gate,
                                    const float* shift, const float* scale, void* normed, int L,
                                    int D, float eps, cudaStream_t s, const int32_t* seg,
-                                   int num_seg, int64_t seg_stride) {
+                                   int num_seg, int64_t seg_stride, const RopeRequest* rope) {
   const int vpt = (D / 4 + MNR_THREADS - 1) / MNR_THREADS;
   const auto* d = static_cast<const __nv_bfloat16*>(delta);
   auto* n = static_cast<__nv_bfloat16*>(normed);
-#define H3_MNR_CASE(V)                                                              \
-  case V:                                                                           \
-    mod_norm_residual_kernel<V><<<L, MNR_THREADS, 0, s>>>(resid, d, gate, shift, scale, n, D, \
-                                                          eps, seg, num_seg, seg_stride); \
+  RopeTable tab{};
+  if (rope != nullptr) tab = rope_table(rope->axis_dims, rope->theta);
+  const int32_t* pos = rope ? rope->pos : nullptr;
+  float2* out = rope ? rope->out : nullptr;
+#define H3_MNR_LAUNCH(V, R)                                                              \
+  mod_norm_residual_kernel<V, R><<<L, MNR_THREADS, 0, s>>>(resid, d, gate, shift, scale, n, D, \
+                                                           eps, seg, num_seg, seg_stride, pos, \
+                                                           out, tab)
+#define H3_MNR_CASE(V)                  \
+  case V:                               \
+    if (rope != nullptr)                \
+      H3_MNR_LAUNCH(V, true);           \
+    else                                \
+      H3_MNR_LAUNCH(V, false);          \
     break;
   switch (vpt) {
     H3_MNR_CASE(1)
@@ -479,6 +500,7 @@ h3_status launch_mod_norm_residual(float* resid, const void* delta, const float*
       return fail(H3_ERR_UNSUPPORTED, "mod_norm_residual: D=%d exceeds 8192", D);
   }
 #undef H3_MNR_CASE
+#undef H3_MNR_LAUNCH
   return cuda_fail(cudaGetLastError(), "mod_norm_residual launch");
 }
 

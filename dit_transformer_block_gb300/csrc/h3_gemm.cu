@@ -376,16 +376,9 @@ static h3_status launch_gemm_impl(const void* A, int64_t lda_bytes, const float*
                                   int64_t ldb_bytes, const float* sb, void* C, int64_t ldc, int L,
                                   int N, int K, GemmEpilogue ep, cudaStream_t s,
                                   const GemmExtra* extra) {
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return cuda_fail(e, "gemm: set shared memory size");
-    attr_done[dev] = true;
-  }
+  static std::atomic<bool> done[64];
+  h3_status st = set_smem_limit(done, gemm_kernel<FP8>, SMEM_BYTES, "gemm: set shared memory size");
+  if (st != H3_OK) return st;
   constexpr int kb_elems = FP8 ? 2 * BK : BK;
   GemmArgs a{};
   a.C = C;
@@ -404,7 +397,7 @@ static h3_status launch_gemm_impl(const void* A, int64_t lda_bytes, const float*
   a.num_n = N / tile_n;
   a.num_k = (K + kb_elems - 1) / kb_elems;
   a.num_tiles = a.num_m * a.num_n;
-  h3_status st = dev_err(&a.err);
+  st = dev_err(&a.err);
   if (st != H3_OK) return st;
 
   CUtensorMap tmA, tmB;

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/h3block.h"
@@ -18,6 +19,24 @@ void clear_error();
 h3_status dev_err(DevErr* out);
 int num_sms();
 
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device (done[] holds the devices already set; ordinals
+// past its end are set on every call). Safe to call from several threads:
+// the attribute call is idempotent and the flags are atomic.
+template <typename Kernel>
+h3_status set_smem_limit(std::atomic<bool> (&done)[64], Kernel kernel, size_t bytes,
+                         const char* what) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  if (dev < 64 && done[dev].load(std::memory_order_acquire)) return H3_OK;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes));
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  if (dev < 64) done[dev].store(true, std::memory_order_release);
+  return H3_OK;
+}
+
 // ---- TMA descriptors (h3_abi.cu). A 2D bf16 tensor of `outer` rows x `inner`
 // elements with the given row stride, boxes of box_inner x box_outer, 128-byte
 // swizzle, zero fill outside the tensor.
@@ -32,12 +51,21 @@ h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream
 h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float* q_gain,
                               const float* k_gain, const int32_t* pos, const int* axis_dims,
                               int L, int H, float theta, float eps, cudaStream_t s);
+// The RoPE (cos, sin) table of rows [0, L) (see launch_rope_table), written
+// by the modulation kernel beside its own work when requested.
+struct RopeRequest {
+  const int32_t* pos;    // [L, 3] positions
+  const int* axis_dims;  // host [3]
+  float theta;
+  float2* out;           // [L, 64]
+};
 // seg (optional): per-row token-group index into a table whose groups are
 // seg_stride floats apart (gate/shift/scale point at group 0).
 h3_status launch_mod_norm_residual(float* resid, const void* delta, const float* gate,
                                    const float* shift, const float* scale, void* normed, int L,
                                    int D, float eps, cudaStream_t s, const int32_t* seg = nullptr,
-                                   int num_seg = 1, int64_t seg_stride = 0);
+                                   int num_seg = 1, int64_t seg_stride = 0,
+                                   const RopeRequest* rope = nullptr);
 
 // (cos, sin) of every RoPE angle of rows [0, L): out[i * 64 + p] for channel
 // pair p of a 128-channel head, the angle formed and reduced exactly as

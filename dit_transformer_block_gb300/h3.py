@@ -434,8 +434,8 @@ def block_workspace_bytes(cfg: BlockConfig) -> int:
 BLOCK_STAGES = 7
 STAGE_NAMES = ("mod_norm", "qkv_proj_qk_norm_rope", "attention", "out_proj",
                "residual_mod_norm", "gate_up_swiglu", "down_proj_residual")
-# kernels one block launches: the stages plus the RoPE table pass
-BLOCK_LAUNCHES = BLOCK_STAGES + 1
+# kernels one block launches: one per stage
+BLOCK_LAUNCHES = BLOCK_STAGES
 
 
 def block_weights(weights: dict) -> BlockWeights:
