@@ -34,6 +34,9 @@ equations, so the formulas below are the plainest readings, listed here:
   * RoPE: head_dim is split into axis sections (d_0, d_1, d_2) for positions
     (t, h, w); inside section a the pair (o_a + 2j, o_a + 2j + 1) is rotated by
     angle pos_a * theta^(-2j / d_a) (interleaved pairs, section-local exponent).
+    The split-half layout pairs (o_a + j, o_a + d_a/2 + j) instead, with the
+    same angle for pair j; it is the interleaved rotation under a fixed
+    permutation of each section's channels.
   * QKV weight rows are [q | k | v], each head-major; the FFN up weight rows
     are [gate | up]; no biases.
   * attention: softmax(q k^T * scale) v over keys [0, L), bidirectional;
@@ -153,27 +156,61 @@ def rope_angles(pos, axis_dims, theta: float) -> np.ndarray:
     return np.concatenate(cols, axis=1)
 
 
-def rope_apply(x, phi) -> np.ndarray:
-    """Rotate interleaved pairs (2i, 2i+1) of x[..., head_dim] by phi[..., head_dim//2].
+def rope_pairs(axis_dims, pairing: str = "interleaved"):
+    """Channel indices (first, second) of every rotated pair, in the pair order
+    of rope_angles (section a, then pair j inside it).
+
+    interleaved: (o_a + 2j, o_a + 2j + 1); half: (o_a + j, o_a + d_a/2 + j),
+    o_a being the first channel of section a.
+    """
+    first, second = [], []
+    o = 0
+    for d in axis_dims:
+        for j in range(d // 2):
+            if pairing == "interleaved":
+                first.append(o + 2 * j)
+                second.append(o + 2 * j + 1)
+            elif pairing == "half":
+                first.append(o + j)
+                second.append(o + d // 2 + j)
+            else:
+                raise ValueError(pairing)
+        o += d
+    return np.array(first), np.array(second)
+
+
+def rope_apply(x, phi, axis_dims=None, pairing: str = "interleaved") -> np.ndarray:
+    """Rotate the pairs of x[..., head_dim] by phi[..., head_dim//2].
 
     x has shape [rows, heads, head_dim] and phi [rows, head_dim // 2] (the
-    same angles for every head of a token).
+    same angles for every head of a token). Interleaved pairs (2i, 2i+1) by
+    default; pairing="half" rotates the split-half pairs of rope_pairs
+    (axis_dims needed).
     """
     x = np.asarray(x, dtype=np.float64)
     c = np.cos(phi)[:, None, :]
     s = np.sin(phi)[:, None, :]
-    x0 = x[..., 0::2]
-    x1 = x[..., 1::2]
+    if pairing == "interleaved":
+        x0 = x[..., 0::2]
+        x1 = x[..., 1::2]
+        out = np.empty_like(x)
+        out[..., 0::2] = x0 * c - x1 * s
+        out[..., 1::2] = x0 * s + x1 * c
+        return out
+    first, second = rope_pairs(axis_dims, pairing)
+    x0 = x[..., first]
+    x1 = x[..., second]
     out = np.empty_like(x)
-    out[..., 0::2] = x0 * c - x1 * s
-    out[..., 1::2] = x0 * s + x1 * c
+    out[..., first] = x0 * c - x1 * s
+    out[..., second] = x0 * s + x1 * c
     return out
 
 
-def qk_norm_rope(x, gain, pos, axis_dims, theta: float, eps: float) -> np.ndarray:
+def qk_norm_rope(x, gain, pos, axis_dims, theta: float, eps: float,
+                 pairing: str = "interleaved") -> np.ndarray:
     """RMSNorm per head, then RoPE, rounded to bf16. x [rows, heads, head_dim]."""
     n = rms_norm(x, gain, eps)
-    return round_bf16(rope_apply(n, rope_angles(pos, axis_dims, theta)))
+    return round_bf16(rope_apply(n, rope_angles(pos, axis_dims, theta), axis_dims, pairing))
 
 
 # ---------------------------------------------------------------------------
@@ -267,7 +304,8 @@ def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
                   *, L: int, heads: int, head_dim: int, axis_dims, theta: float,
                   eps_ln: float = 1e-6, eps_qk: float = 1e-6, rows=None,
                   kv_chunk: int = 4096, return_intermediates: bool = False, seg=None,
-                  fp8: bool = False, fp8_attention: bool = False):
+                  fp8: bool = False, fp8_attention: bool = False,
+                  rope_pairing: str = "interleaved"):
     """Forward pass of one DiT block for query rows `rows` (default all < L).
 
     resid [S, D] float32 residual stream; mod [6, D]; weights bf16-valued
@@ -279,7 +317,7 @@ def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
     intermediates for those rows. seg: optional token-group index per row,
     with mod a table [G, 6, D] (see modulation_rows). fp8: the four
     projections run as online FP8 (weights and inputs quantised per row,
-    see quantize_fp8_rows / linear_fp8).
+    see quantize_fp8_rows / linear_fp8). rope_pairing: see rope_pairs.
     """
     qw_cache = {}
 
@@ -316,15 +354,17 @@ def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
         _, h1c = mod_norm_residual(r_all[c0:c1], shift=shc, scale=scc, eps=eps_ln)
         if fp8_attention:
             qc = proj(h1c, w_q).reshape(c1 - c0, heads, head_dim)
-            q_all[c0:c1] = qk_norm_rope(qc, q_gain, pos[c0:c1], axis_dims, theta, eps_qk)
+            q_all[c0:c1] = qk_norm_rope(qc, q_gain, pos[c0:c1], axis_dims, theta, eps_qk,
+                                          rope_pairing)
         kc = proj(h1c, w_k).reshape(c1 - c0, heads, head_dim)
-        k_all[c0:c1] = qk_norm_rope(kc, k_gain, pos[c0:c1], axis_dims, theta, eps_qk)
+        k_all[c0:c1] = qk_norm_rope(kc, k_gain, pos[c0:c1], axis_dims, theta, eps_qk,
+                                      rope_pairing)
         v_all[c0:c1] = proj(h1c, w_v).reshape(c1 - c0, heads, head_dim)
 
     r = r_all[rows]
     _, h1 = mod_norm_residual(r, shift=sh1, scale=sc1, eps=eps_ln)
     q = proj(h1, w_q).reshape(len(rows), heads, head_dim)
-    q = qk_norm_rope(q, q_gain, np.asarray(pos)[rows], axis_dims, theta, eps_qk)
+    q = qk_norm_rope(q, q_gain, np.asarray(pos)[rows], axis_dims, theta, eps_qk, rope_pairing)
     if fp8_attention:
         q_full = q_all
     else:
@@ -349,7 +389,7 @@ def block_forward(resid, mod, w_qkv, w_o, w_gu, w_down, q_gain, k_gain, pos,
 
 def stack_forward(resid, mods, weights, q_gains, k_gains, pos, *, L: int, heads: int,
                   head_dim: int, axis_dims, theta: float, eps_ln: float = 1e-6,
-                  eps_qk: float = 1e-6, seg=None):
+                  eps_qk: float = 1e-6, seg=None, rope_pairing: str = "interleaved"):
     """Blocks applied one after another to the whole residual stream (all
     rows < L); the denoiser runs its transformer blocks in sequence for every
     forward (vLLM-Omni H3 blog, section 5: FastH3's forwards). mods[b] and
@@ -359,7 +399,8 @@ def stack_forward(resid, mods, weights, q_gains, k_gains, pos, *, L: int, heads:
         w_qkv, w_o, w_gu, w_down = weights[b]
         r[:L] = block_forward(r, mods[b], w_qkv, w_o, w_gu, w_down, q_gains[b], k_gains[b], pos,
                               L=L, heads=heads, head_dim=head_dim, axis_dims=axis_dims,
-                              theta=theta, eps_ln=eps_ln, eps_qk=eps_qk, seg=seg)
+                              theta=theta, eps_ln=eps_ln, eps_qk=eps_qk, seg=seg,
+                              rope_pairing=rope_pairing)
     return r[:L]
 
 

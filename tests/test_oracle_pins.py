@@ -144,6 +144,46 @@ def check_rope(o):
     assert not math.isclose(dot(5, 2), dot(5, 3), rel_tol=1e-6)
 
 
+def check_rope_half(o):
+    # worked example, one 4-channel section: pairs (0, 2) and (1, 3); a quarter
+    # turn of pair 0 maps (x0, x2) = (1, 3) to (-3, 1), pair 1 stays
+    y = o.rope_apply(np.array([1.0, 2.0, 3.0, 4.0]).reshape(1, 1, 4), np.array([[np.pi / 2, 0.0]]),
+                     (4, 0, 0), "half")
+    assert np.allclose(y.reshape(-1), [-3.0, 2.0, 1.0, 4.0], atol=1e-15)
+    # sections two channels wide: both layouts pair (o, o + 1)
+    x = rng(60).standard_normal((3, 2, 6))
+    phi = rng(61).standard_normal((3, 3))
+    assert np.array_equal(o.rope_apply(x, phi, (2, 2, 2), "half"), o.rope_apply(x, phi))
+    for dims in ((32, 48, 48), (128, 0, 0), (16, 0, 112)):
+        x = rng(62).standard_normal((5, 3, 128))
+        pos = rng(63).integers(0, 90, size=(5, 3))
+        phi = o.rope_angles(pos, dims, 1e4)
+        y = o.rope_apply(x, phi, dims, "half")
+        # the split-half layout is the interleaved one under a per-section
+        # permutation: interleaved slot o+2j <- half slot o+j, o+2j+1 <- o+d/2+j
+        perm = []
+        base = 0
+        for d in dims:
+            for j in range(d // 2):
+                perm += [base + j, base + d // 2 + j]
+            base += d
+        perm = np.array(perm)
+        assert np.allclose(y[..., perm], o.rope_apply(x[..., perm], phi), atol=1e-13)
+        # pair by pair (explicit loop): norm kept, angle added
+        base = 0
+        p = 0
+        for d in dims:
+            for j in range(d // 2):
+                a, b = base + j, base + d // 2 + j
+                z0 = complex(x[0, 1, a], x[0, 1, b]) * complex(math.cos(phi[0, p]), math.sin(phi[0, p]))
+                assert math.isclose(y[0, 1, a], z0.real, abs_tol=1e-13)
+                assert math.isclose(y[0, 1, b], z0.imag, abs_tol=1e-13)
+                p += 1
+            base += d
+        # turning back restores the input
+        assert np.allclose(o.rope_apply(y, -phi, dims, "half"), x, atol=1e-13)
+
+
 def check_qk_norm_rope(o):
     # norm first, then rope: with all positions 0 the result is the rounded RMSNorm
     x = bf16_values(rng(11).standard_normal((4, 3, 128)))
@@ -165,6 +205,10 @@ def test_rms_norm():
 
 def test_rope():
     check_rope(O)
+
+
+def test_rope_half():
+    check_rope_half(O)
 
 
 def test_qk_norm_rope():
@@ -410,11 +454,18 @@ def _mutant(**repl):
     return m
 
 
-def _rope_wrong_sign(x, phi):
-    return O.rope_apply(x, -phi)
+def _rope_wrong_sign(x, phi, *args):
+    return O.rope_apply(x, -phi, *args)
 
 
-def _rope_half_split(x, phi):
+def _rope_half_whole_head(x, phi, axis_dims=None, pairing="interleaved"):
+    # split-half pairs taken across the whole head instead of per section
+    if pairing == "interleaved":
+        return O.rope_apply(x, phi)
+    return _rope_half_split(x, phi)
+
+
+def _rope_half_split(x, phi, *args):
     x = np.asarray(x, np.float64)
     h = x.shape[-1] // 2
     c, s = np.cos(phi)[:, None, :], np.sin(phi)[:, None, :]
@@ -487,6 +538,8 @@ def _rms_no_eps_mean(x, gain, eps):
     ("rope sign", dict(rope_apply=_rope_wrong_sign), ["check_rope"]),
     ("rope half-split pairing", dict(rope_apply=_rope_half_split), ["check_rope"]),
     ("rope global exponent", dict(rope_angles=_angles_global_exponent), ["check_rope"]),
+    ("split-half pairs across the head", dict(rope_apply=_rope_half_whole_head),
+     ["check_rope_half"]),
     ("modulation without 1+", dict(mod_norm_residual=_mod_no_one_plus), ["check_mod_norm_residual"]),
     ("swiglu halves swapped", dict(swiglu=_swiglu_swapped), ["check_swiglu"]),
     ("layernorm not centred", dict(layer_norm=_ln_no_center), ["check_layer_norm"]),
