@@ -246,9 +246,23 @@ h3_status h3_mod_norm_residual(float* resid, const void* delta, const float* gat
                                   reinterpret_cast<cudaStream_t>(stream));
 }
 
-h3_status h3_qk_norm_rope(void* q, void* k, const float* q_gain, const float* k_gain,
-                          const int32_t* pos, const int* axis_dims, int S, int L, int H, int Dh,
-                          float theta, float eps, h3_stream_t stream) {
+// pairing 0: interleaved pairs; 1: split-half pairs, every section a
+// multiple of 16 wide (so each half is whole 8-channel slices).
+static h3_status check_pairing(const int* axis_dims, int pairing) {
+  H3_REQUIRE(pairing == 0 || pairing == 1, H3_ERR_INVALID_ARG, "rope pairing %d (0 or 1)",
+             pairing);
+  if (pairing == 1)
+    for (int a = 0; a < 3; ++a)
+      H3_REQUIRE(axis_dims[a] % 16 == 0, H3_ERR_UNSUPPORTED,
+                 "split-half RoPE needs sections that are multiples of 16 (axis_dims[%d]=%d)", a,
+                 axis_dims[a]);
+  return H3_OK;
+}
+
+static h3_status qk_norm_rope_impl(void* q, void* k, const float* q_gain, const float* k_gain,
+                                   const int32_t* pos, const int* axis_dims, int S, int L, int H,
+                                   int Dh, float theta, float eps, int pairing,
+                                   h3_stream_t stream) {
   clear_error();
   h3_status st = check_rows(S, L);
   if (st != H3_OK) return st;
@@ -263,12 +277,28 @@ h3_status h3_qk_norm_rope(void* q, void* k, const float* q_gain, const float* k_
     sum += axis_dims[a];
   }
   H3_REQUIRE(sum == Dh, H3_ERR_INVALID_ARG, "axis_dims sum %d != head_dim %d", sum, Dh);
+  if ((st = check_pairing(axis_dims, pairing)) != H3_OK) return st;
   H3_REQUIRE(theta > 0.f && eps >= 0.f, H3_ERR_INVALID_ARG, "theta must be > 0 and eps >= 0");
   H3_REQUIRE(aligned16(q) && aligned16(k) && aligned16(q_gain) && aligned16(k_gain),
              H3_ERR_MISALIGNED, "q, k and the gains must be 16-byte aligned");
   if (L == 0) return H3_OK;
   return launch_qk_norm_rope(q, k, static_cast<int64_t>(H) * Dh, q_gain, k_gain, pos, axis_dims,
-                             L, H, theta, eps, reinterpret_cast<cudaStream_t>(stream));
+                             L, H, theta, eps, reinterpret_cast<cudaStream_t>(stream), pairing);
+}
+
+h3_status h3_qk_norm_rope(void* q, void* k, const float* q_gain, const float* k_gain,
+                          const int32_t* pos, const int* axis_dims, int S, int L, int H, int Dh,
+                          float theta, float eps, h3_stream_t stream) {
+  return qk_norm_rope_impl(q, k, q_gain, k_gain, pos, axis_dims, S, L, H, Dh, theta, eps, 0,
+                           stream);
+}
+
+h3_status h3_qk_norm_rope_layout(void* q, void* k, const float* q_gain, const float* k_gain,
+                                 const int32_t* pos, const int* axis_dims, int S, int L, int H,
+                                 int Dh, float theta, float eps, int pairing,
+                                 h3_stream_t stream) {
+  return qk_norm_rope_impl(q, k, q_gain, k_gain, pos, axis_dims, S, L, H, Dh, theta, eps,
+                           pairing, stream);
 }
 
 h3_status h3_attention_varlen(const void* q, const void* k, const void* v, void* o, int S,
@@ -398,7 +428,7 @@ h3_status h3_linear_swiglu(const void* x, const void* w_gu, void* out, int S, in
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
-static h3_status check_axis_dims(const int* axis_dims, float theta) {
+static h3_status check_axis_dims(const int* axis_dims) {
   H3_REQUIRE(axis_dims != nullptr, H3_ERR_INVALID_ARG, "axis_dims is NULL");
   int sum = 0;
   for (int a = 0; a < 3; ++a) {
@@ -407,7 +437,6 @@ static h3_status check_axis_dims(const int* axis_dims, float theta) {
     sum += axis_dims[a];
   }
   H3_REQUIRE(sum == 128, H3_ERR_INVALID_ARG, "axis_dims sum %d != head_dim 128", sum);
-  H3_REQUIRE(theta > 0.f, H3_ERR_INVALID_ARG, "theta must be > 0");
   return H3_OK;
 }
 
@@ -417,7 +446,8 @@ h3_status h3_rope_table(const int32_t* pos, const int* axis_dims, int S, int L, 
   h3_status st = check_rows(S, L);
   if (st != H3_OK) return st;
   H3_REQUIRE(pos && table, H3_ERR_INVALID_ARG, "a required pointer is NULL");
-  if ((st = check_axis_dims(axis_dims, theta)) != H3_OK) return st;
+  if ((st = check_axis_dims(axis_dims)) != H3_OK) return st;
+  H3_REQUIRE(theta > 0.f, H3_ERR_INVALID_ARG, "theta must be > 0");
   H3_REQUIRE(aligned16(table), H3_ERR_MISALIGNED, "table must be 16-byte aligned");
   if (L == 0) return H3_OK;
   return launch_rope_table(pos, axis_dims, L, theta, reinterpret_cast<float2*>(table),
@@ -426,8 +456,8 @@ h3_status h3_rope_table(const int32_t* pos, const int* axis_dims, int S, int L, 
 
 h3_status h3_linear_qk_norm_rope(const void* x, const void* w_qkv, void* qkv,
                                  const float* q_gain, const float* k_gain,
-                                 const float* rope_table, int S, int L, int H, int K, float eps,
-                                 h3_stream_t stream) {
+                                 const float* rope_table, const int* axis_dims, int pairing,
+                                 int S, int L, int H, int K, float eps, h3_stream_t stream) {
   clear_error();
   h3_status st = check_rows(S, L);
   if (st != H3_OK) return st;
@@ -436,6 +466,8 @@ h3_status h3_linear_qk_norm_rope(const void* x, const void* w_qkv, void* qkv,
   H3_REQUIRE(H > 0 && H % 2 == 0, H3_ERR_UNSUPPORTED, "H=%d must be even", H);
   H3_REQUIRE(K > 0 && K % 64 == 0, H3_ERR_UNSUPPORTED, "K=%d must be a multiple of 64", K);
   H3_REQUIRE(eps >= 0.f, H3_ERR_INVALID_ARG, "eps must be >= 0");
+  if ((st = check_axis_dims(axis_dims)) != H3_OK) return st;
+  if ((st = check_pairing(axis_dims, pairing)) != H3_OK) return st;
   H3_REQUIRE(aligned16(x) && aligned16(w_qkv) && aligned16(qkv) && aligned16(q_gain) &&
                  aligned16(k_gain) && aligned16(rope_table),
              H3_ERR_MISALIGNED, "pointers must be 16-byte aligned");
@@ -447,6 +479,7 @@ h3_status h3_linear_qk_norm_rope(const void* x, const void* w_qkv, void* qkv,
   ex.rope = reinterpret_cast<const float2*>(rope_table);
   ex.d_model = D;
   ex.eps = eps;
+  if (pairing == 1) rope_pieces(axis_dims, &ex);
   return launch_gemm(x, K, w_qkv, K, qkv, 3LL * D, L, 3 * D, K, GEMM_QK_NORM_ROPE,
                      reinterpret_cast<cudaStream_t>(stream), &ex);
 }
@@ -479,6 +512,8 @@ static h3_status check_block_config(const h3_block_config* c) {
              "D=%d must be a multiple of 256 and at most 8192", c->D);
   H3_REQUIRE(c->F > 0 && c->F % 128 == 0, H3_ERR_UNSUPPORTED, "F=%d must be a multiple of 128",
              c->F);
+  st = check_pairing(c->axis_dims, c->rope_pairing);
+  if (st != H3_OK) return st;
   int sum = 0;
   for (int a = 0; a < 3; ++a) {
     H3_REQUIRE(c->axis_dims[a] >= 0 && c->axis_dims[a] % 2 == 0, H3_ERR_INVALID_ARG,
@@ -622,6 +657,7 @@ static h3_status stack_forward_impl(const h3_block_config* cfg, const h3_block_w
     qk.rope = rope;
     qk.d_model = D;
     qk.eps = cfg->eps_qk;
+    if (cfg->rope_pairing == 1) rope_pieces(cfg->axis_dims, &qk);
     H3_STAGE(1, launch_gemm(h, D, wb.w_qkv, D, qkv, ld_qkv, L, 3 * D, D, GEMM_QK_NORM_ROPE, s,
                             &qk));
     // 2: a = softmax(q k^T / sqrt(Dh)) v over keys < L
@@ -855,6 +891,7 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
   qk.rope = rope;
   qk.d_model = D;
   qk.eps = cfg->eps_qk;
+  if (cfg->rope_pairing == 1) rope_pieces(cfg->axis_dims, &qk);
   GemmExtra res;
   res.gate = mod + 5 * D;
   const int64_t ld_qkv = 3LL * D;

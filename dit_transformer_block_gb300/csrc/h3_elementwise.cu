@@ -71,6 +71,11 @@ constexpr int QK_BATCH = 8;  // head pairs loaded per batch (16 heads)
 struct RopeTable {
   double omega[QK_HEAD_DIM / 2];  // angle per unit position for each pair
   int axis[QK_HEAD_DIM / 2];      // which position (t, h, w) drives the pair
+  // split-half layout, per 8-channel slice s of a head: the slice holding the
+  // partners, whether s holds first elements, and the pair of its channel 0
+  int half_src[QK_HEAD_DIM / 8];
+  int half_first[QK_HEAD_DIM / 8];
+  int half_pair0[QK_HEAD_DIM / 8];
 };
 
 constexpr double kTwoPi = 6.283185307179586476925286766559;
@@ -98,6 +103,11 @@ __global__ void __launch_bounds__(256)
   out[i] = make_float2(cs, sn);
 }
 
+// HALF: split-half pairs (o + j, o + d/2 + j) per section instead of
+// interleaved ones. Each half of a section is a multiple of 8 channels, so a
+// lane's slice holds only first or only second elements, of 8 consecutive
+// pairs, and reads its partners from one other lane of its half-warp.
+template <bool HALF>
 __global__ void __launch_bounds__(QK_WARPS * 32)
     qk_norm_rope_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
                         int64_t row_stride, const float* __restrict__ q_gain,
@@ -117,14 +127,18 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
   const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp + 4));
   const float gain[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 
-  // Angles of this lane's pairs
+  // Angles of this lane's pairs (4 interleaved pairs, or 8 split-half ones)
+  constexpr int NP = HALF ? 8 : 4;
   const int32_t p3[3] = {__ldg(pos + 3 * row), __ldg(pos + 3 * row + 1), __ldg(pos + 3 * row + 2)};
-  float cs[4], sn[4];
+  float cs[NP], sn[NP];
+  const int pair0 = HALF ? tab.half_pair0[sub] : sub * 4;
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int pr = sub * 4 + t;
+  for (int t = 0; t < NP; ++t) {
+    const int pr = pair0 + t;
     rope_angle(p3[tab.axis[pr]], tab.omega[pr], sn[t], cs[t]);
   }
+  const int src_lane = (half << 4) + (HALF ? tab.half_src[sub] : 0);
+  const bool first = HALF ? tab.half_first[sub] != 0 : true;
 
   for (int h0 = 0; h0 < H; h0 += 2 * QK_BATCH) {
     uint4 v[QK_BATCH];
@@ -152,11 +166,24 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
       for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
       const float inv = rsqrtf(ss * (1.0f / QK_HEAD_DIM) + eps);
       uint32_t o[4];
+      if constexpr (HALF) {
+        float y[8];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float a = x[2 * t] * inv * gain[2 * t];
-        const float b = x[2 * t + 1] * inv * gain[2 * t + 1];
-        o[t] = pack_bf16x2(a * cs[t] - b * sn[t], a * sn[t] + b * cs[t]);
+        for (int j = 0; j < 8; ++j) {
+          const float a = x[j] * inv * gain[j];
+          const float b = __shfl_sync(0xffffffffu, a, src_lane);  // the pair's other element
+          // first elements: a c - b s; second elements: b s + a c
+          y[j] = first ? a * cs[j] - b * sn[j] : b * sn[j] + a * cs[j];
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) o[t] = pack_bf16x2(y[2 * t], y[2 * t + 1]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float a = x[2 * t] * inv * gain[2 * t];
+          const float b = x[2 * t + 1] * inv * gain[2 * t + 1];
+          o[t] = pack_bf16x2(a * cs[t] - b * sn[t], a * sn[t] + b * cs[t]);
+        }
       }
       if (head < H)
         *reinterpret_cast<uint4*>(base + head * QK_HEAD_DIM) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -432,14 +459,25 @@ h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream
 }
 
 static RopeTable rope_table(const int* axis_dims, float theta) {
-  RopeTable tab;
+  RopeTable tab{};
   int pr = 0;
+  int o = 0;  // first channel of section a
   for (int a = 0; a < 3; ++a) {
     const int d = axis_dims[a];
     for (int j = 0; j < d / 2; ++j, ++pr) {
       tab.omega[pr] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(d));
       tab.axis[pr] = a;
     }
+    // split-half slices (meaningful when d % 16 == 0): slice s of the first
+    // half pairs with slice s + d/16 of the second half
+    for (int c = 0; c + 8 <= d; c += 8) {
+      const int s = (o + c) / 8;
+      const bool fst = c < d / 2;
+      tab.half_first[s] = fst ? 1 : 0;
+      tab.half_src[s] = fst ? s + d / 16 : s - d / 16;
+      tab.half_pair0[s] = o / 2 + (fst ? c : c - d / 2);
+    }
+    o += d;
   }
   return tab;
 }
@@ -455,13 +493,19 @@ h3_status launch_rope_table(const int32_t* pos, const int* axis_dims, int L, flo
 
 h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float* q_gain,
                               const float* k_gain, const int32_t* pos, const int* axis_dims,
-                              int L, int H, float theta, float eps, cudaStream_t s) {
+                              int L, int H, float theta, float eps, cudaStream_t s,
+                              int pairing) {
   const RopeTable tab = rope_table(axis_dims, theta);
   const int64_t warps = 2LL * L;
   const int grid = static_cast<int>((warps + QK_WARPS - 1) / QK_WARPS);
-  qk_norm_rope_kernel<<<grid, QK_WARPS * 32, 0, s>>>(
-      static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k), row_stride, q_gain, k_gain,
-      pos, L, H, eps, tab);
+  auto* qq = static_cast<__nv_bfloat16*>(q);
+  auto* kk = static_cast<__nv_bfloat16*>(k);
+  if (pairing == 1)
+    qk_norm_rope_kernel<true><<<grid, QK_WARPS * 32, 0, s>>>(qq, kk, row_stride, q_gain, k_gain,
+                                                             pos, L, H, eps, tab);
+  else
+    qk_norm_rope_kernel<false><<<grid, QK_WARPS * 32, 0, s>>>(qq, kk, row_stride, q_gain, k_gain,
+                                                              pos, L, H, eps, tab);
   return cuda_fail(cudaGetLastError(), "qk_norm_rope launch");
 }
 

@@ -70,6 +70,25 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmArgs& a, int& mb
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// 8 accumulator columns [col, col + 8) of this thread's row (col a multiple
+// of 8, relative to taddr's column), FP8-scaled when FP8, each rounded to
+// bf16. Loads the 16-column block holding them.
+template <bool FP8>
+__device__ __forceinline__ void load8_bf16(uint32_t taddr, int col, float sa_row, const float* sb,
+                                           float (&x)[8]) {
+  uint32_t v[16];
+  tmem_ld16(taddr + static_cast<uint32_t>(col & ~15), v);
+  tmem_ld_wait();
+  tmem_reg_fence(v);
+  const bool hi = (col & 8) != 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float f = __uint_as_float(hi ? v[8 + j] : v[j]);
+    if constexpr (FP8) f *= sa_row * __ldg(sb + col + j);
+    x[j] = round_to_bf16(f);
+  }
+}
+
 // 32 accumulator columns of this thread's row, FP8-scaled when FP8, each
 // rounded to bf16 (returned as floats).
 template <bool FP8>
@@ -304,6 +323,35 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 32; ++j) ss = fmaf(f[j], f[j], ss);
           }
           const float inv = rsqrtf(ss * (1.0f / 128.0f) + a.x.eps);
+          if (a.x.pairing == 1) {
+            // pass 2, split-half pairs: eight pieces of eight pairs
+#pragma unroll 1
+            for (int pc = 0; pc < 8; ++pc) {
+              const int f0 = a.x.piece_first[pc], s0 = a.x.piece_second[pc];
+              const int p0 = a.x.piece_pair[pc];
+              float xf[8], xs[8];
+              load8_bf16<FP8>(t_head, f0, sa_row, a.sb + hcol, xf);
+              load8_bf16<FP8>(t_head, s0, sa_row, a.sb + hcol, xs);
+              float yf[8], ys[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float2 r = __ldg(rope + p0 + j);
+                const float x0 = xf[j] * inv * __ldg(gain + f0 + j);
+                const float x1 = xs[j] * inv * __ldg(gain + s0 + j);
+                yf[j] = x0 * r.x - x1 * r.y;
+                ys[j] = x0 * r.y + x1 * r.x;
+              }
+              if (row_ok) {
+                *reinterpret_cast<uint4*>(crow + hcol + f0) =
+                    make_uint4(pack_bf16x2(yf[0], yf[1]), pack_bf16x2(yf[2], yf[3]),
+                               pack_bf16x2(yf[4], yf[5]), pack_bf16x2(yf[6], yf[7]));
+                *reinterpret_cast<uint4*>(crow + hcol + s0) =
+                    make_uint4(pack_bf16x2(ys[0], ys[1]), pack_bf16x2(ys[2], ys[3]),
+                               pack_bf16x2(ys[4], ys[5]), pack_bf16x2(ys[6], ys[7]));
+              }
+            }
+            continue;
+          }
           // pass 2: scale, gain, rotate, store
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -411,6 +459,20 @@ static h3_status launch_gemm_impl(const void* A, int64_t lda_bytes, const float*
   const int grid = std::min(a.num_tiles, num_sms());
   gemm_kernel<FP8><<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, a);
   return cuda_fail(cudaGetLastError(), "gemm launch");
+}
+
+void rope_pieces(const int* axis_dims, GemmExtra* ex) {
+  int n = 0, o = 0;
+  for (int a = 0; a < 3; ++a) {
+    const int d = axis_dims[a];
+    for (int c = 0; c < d / 2 && n < 8; c += 8, ++n) {
+      ex->piece_first[n] = o + c;
+      ex->piece_second[n] = o + d / 2 + c;
+      ex->piece_pair[n] = o / 2 + c;
+    }
+    o += d;
+  }
+  ex->pairing = 1;
 }
 
 h3_status launch_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C,

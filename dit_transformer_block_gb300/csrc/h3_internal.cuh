@@ -48,9 +48,12 @@ h3_status make_tmap_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint
 
 // ---- kernel launchers (arguments already validated)
 h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream_t s);
+// pairing: 0 interleaved pairs (2j, 2j + 1), 1 split-half pairs
+// (o + j, o + d/2 + j) per section (every section a multiple of 16 wide).
 h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float* q_gain,
                               const float* k_gain, const int32_t* pos, const int* axis_dims,
-                              int L, int H, float theta, float eps, cudaStream_t s);
+                              int L, int H, float theta, float eps, cudaStream_t s,
+                              int pairing = 0);
 // The RoPE (cos, sin) table of rows [0, L) (see launch_rope_table), written
 // by the modulation kernel beside its own work when requested.
 struct RopeRequest {
@@ -100,7 +103,17 @@ struct GemmExtra {
   const float2* rope = nullptr;
   int d_model = 0;
   float eps = 0.f;
+  // split-half RoPE pairs (pairing 1): eight pieces of eight pairs, piece i
+  // rotating columns piece_first[i] + j with piece_second[i] + j by table
+  // entry piece_pair[i] + j (set by rope_pieces)
+  int pairing = 0;
+  int piece_first[8] = {};
+  int piece_second[8] = {};
+  int piece_pair[8] = {};
 };
+// Fills ex's split-half pieces for the RoPE sections axis_dims (each a
+// multiple of 16, summing to 128) and sets ex->pairing = 1.
+void rope_pieces(const int* axis_dims, GemmExtra* ex);
 // C[:L, :] = epilogue(A[:L, :K] @ B^T). A row stride lda, B [N, K] row stride
 // ldb, C row stride ldc (elements of C). For GEMM_SWIGLU, N is the width of C
 // (= F) and B holds 2N rows.

@@ -33,7 +33,8 @@ class H3Error(RuntimeError):
 class BlockConfig(ctypes.Structure):
     _fields_ = [("S", ctypes.c_int), ("L", ctypes.c_int), ("D", ctypes.c_int), ("H", ctypes.c_int),
                 ("Dh", ctypes.c_int), ("F", ctypes.c_int), ("axis_dims", ctypes.c_int * 3),
-                ("theta", ctypes.c_float), ("eps_ln", ctypes.c_float), ("eps_qk", ctypes.c_float)]
+                ("theta", ctypes.c_float), ("eps_ln", ctypes.c_float), ("eps_qk", ctypes.c_float),
+                ("rope_pairing", ctypes.c_int)]
 
 
 class BlockWeightsFp8(ctypes.Structure):
@@ -69,7 +70,8 @@ _SIGS = {
     "h3_linear": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_linear_swiglu": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_rope_table": (_I, [_P, _P, _I, _I, _F, _P, _P]),
-    "h3_linear_qk_norm_rope": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
+    "h3_linear_qk_norm_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "h3_qk_norm_rope_layout": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _I, _P]),
     "h3_linear_residual": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_block_workspace_bytes": (_SZ, [ctypes.POINTER(BlockConfig)]),
     "h3_block_forward": (_I, [ctypes.POINTER(BlockConfig), ctypes.POINTER(BlockWeights), _P, _P,
@@ -191,17 +193,24 @@ def mod_norm_residual_seg(resid, table, seg, delta=None, gate_idx=None, shift_id
         _p(normed), S, L, D, eps, _s(stream)))
 
 
-def qk_norm_rope(q, k, q_gain, k_gain, pos, axis_dims, L=None, theta=1e4, eps=1e-6, stream=None):
-    """In-place per-head RMSNorm + RoPE of q, k [S,H,Dh] bf16."""
+def qk_norm_rope(q, k, q_gain, k_gain, pos, axis_dims, L=None, theta=1e4, eps=1e-6, stream=None,
+                 pairing=0):
+    """In-place per-head RMSNorm + RoPE of q, k [S,H,Dh] bf16 (pairing 0:
+    interleaved pairs, 1: split-half pairs per section)."""
     _need(q, torch.bfloat16, "q")
     _need(k, torch.bfloat16, "k")
     _need(pos, torch.int32, "pos")
     S, H, Dh = q.shape
     L = S if L is None else L
-    ax = (ctypes.c_int * 3)(*axis_dims)
-    _check("qk_norm_rope", lib().h3_qk_norm_rope(
-        _p(q), _p(k), _p(q_gain), _p(k_gain), _p(pos), ctypes.cast(ax, ctypes.c_void_p), S, L, H,
-        Dh, theta, eps, _s(stream)))
+    ax = ctypes.cast((ctypes.c_int * 3)(*axis_dims), ctypes.c_void_p)
+    if pairing == 0:
+        _check("qk_norm_rope", lib().h3_qk_norm_rope(
+            _p(q), _p(k), _p(q_gain), _p(k_gain), _p(pos), ax, S, L, H, Dh, theta, eps,
+            _s(stream)))
+    else:
+        _check("qk_norm_rope_layout", lib().h3_qk_norm_rope_layout(
+            _p(q), _p(k), _p(q_gain), _p(k_gain), _p(pos), ax, S, L, H, Dh, theta, eps, pairing,
+            _s(stream)))
 
 
 def attention_varlen(q, k, v, o, L=None, scale=None, stream=None):
@@ -298,17 +307,20 @@ def rope_table(pos, axis_dims, table, L=None, theta=1e4, stream=None):
                                               theta, _p(table), _s(stream)))
 
 
-def linear_qk_norm_rope(x, w_qkv, qkv, q_gain, k_gain, table, L=None, eps=1e-6, stream=None):
+def linear_qk_norm_rope(x, w_qkv, qkv, q_gain, k_gain, table, axis_dims, L=None, eps=1e-6,
+                        pairing=0, stream=None):
     """qkv[:L] = x @ w_qkv^T with per-head Q/K RMSNorm + RoPE (table from
-    rope_table) in the epilogue; x [S,K], w_qkv [3D,K], qkv [S,3D] bf16."""
+    rope_table, sections axis_dims, pairing as qk_norm_rope) in the epilogue;
+    x [S,K], w_qkv [3D,K], qkv [S,3D] bf16."""
     for n, t in (("x", x), ("w_qkv", w_qkv), ("qkv", qkv)):
         _need(t, torch.bfloat16, n)
     S, K = x.shape
     H = w_qkv.shape[0] // 3 // 128
     L = S if L is None else L
+    ax = ctypes.cast((ctypes.c_int * 3)(*axis_dims), ctypes.c_void_p)
     _check("linear_qk_norm_rope", lib().h3_linear_qk_norm_rope(
-        _p(x), _p(w_qkv), _p(qkv), _p(q_gain), _p(k_gain), _p(table), S, L, H, K, eps,
-        _s(stream)))
+        _p(x), _p(w_qkv), _p(qkv), _p(q_gain), _p(k_gain), _p(table), ax, pairing, S, L, H, K,
+        eps, _s(stream)))
 
 
 def linear_residual(x, w, resid, gate, L=None, stream=None):
@@ -323,8 +335,10 @@ def linear_residual(x, w, resid, gate, L=None, stream=None):
                                                         N, K, _s(stream)))
 
 
-def block_config(S, L, D, H, Dh, F, axis_dims, theta=1e4, eps_ln=1e-6, eps_qk=1e-6) -> BlockConfig:
-    return BlockConfig(S, L, D, H, Dh, F, (ctypes.c_int * 3)(*axis_dims), theta, eps_ln, eps_qk)
+def block_config(S, L, D, H, Dh, F, axis_dims, theta=1e4, eps_ln=1e-6, eps_qk=1e-6,
+                 rope_pairing=0) -> BlockConfig:
+    return BlockConfig(S, L, D, H, Dh, F, (ctypes.c_int * 3)(*axis_dims), theta, eps_ln, eps_qk,
+                       rope_pairing)
 
 
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

@@ -48,7 +48,7 @@ def main(argv):
         tab = torch.empty(M, 64, 2, device=dev)
         gains = torch.ones(128, device=dev)
         runs.append(lambda: h3.rope_table(pos, (32, 48, 48), tab, M))
-        runs.append(lambda: h3.linear_qk_norm_rope(x, w, y, gains, gains, tab, M))
+        runs.append(lambda: h3.linear_qk_norm_rope(x, w, y, gains, gains, tab, (32, 48, 48), M))
         xd, wd = rnd(M, 14336), rnd(5376, 14336, std=0.02)
         rd = torch.randn(M, 5376, generator=g, device=dev)
         gate = torch.randn(5376, generator=g, device=dev) * 0.1

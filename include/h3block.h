@@ -111,6 +111,20 @@ h3_status h3_qk_norm_rope(void* q, void* k, const float* q_gain, const float* k_
                           int Dh, float theta, float eps, h3_stream_t stream);
 
 /*
+ * a2 with a choice of channel pairing (the pages fix RoPE per token but not
+ * its channel layout; interleaved pairs are the reading the block uses by
+ * default). pairing 0: pairs (o_a + 2j, o_a + 2j + 1), exactly
+ * h3_qk_norm_rope. pairing 1: split-half pairs (o_a + j, o_a + d_a/2 + j)
+ * inside each section, the same angle for pair j; every axis_dims[a] must
+ * then be a multiple of 16 (H3_ERR_UNSUPPORTED otherwise). Other arguments
+ * as h3_qk_norm_rope.
+ */
+h3_status h3_qk_norm_rope_layout(void* q, void* k, const float* q_gain, const float* k_gain,
+                                 const int32_t* pos, const int* axis_dims, int S, int L, int H,
+                                 int Dh, float theta, float eps, int pairing,
+                                 h3_stream_t stream);
+
+/*
  * a3 — dense bidirectional attention over the valid length (blog section 3.1:
  * the backend takes the valid sequence length; no work on tail padding):
  *   o[i,h,:] = sum_{j<L} softmax_j(q[i,h,:] . k[j,h,:] * softmax_scale) v[j,h,:]
@@ -218,13 +232,14 @@ h3_status h3_rope_table(const int32_t* pos, const int* axis_dims, int S, int L, 
  *   h3_qk_norm_rope would do it; v columns are the plain product.
  *   x [S, K] bf16, w_qkv [384H, K] bf16, qkv [S, 384H] bf16
  *   q_gain, k_gain [128] float32; rope_table from h3_rope_table
- * H even, K % 64 == 0. Equals h3_linear followed by h3_qk_norm_rope up to the
- * order of the FP32 sum of squares inside the RMS.
+ *   axis_dims HOST [3] (sum 128), pairing as h3_qk_norm_rope_layout
+ * H even, K % 64 == 0. Equals h3_linear followed by h3_qk_norm_rope_layout up
+ * to the order of the FP32 sum of squares inside the RMS.
  */
 h3_status h3_linear_qk_norm_rope(const void* x, const void* w_qkv, void* qkv,
                                  const float* q_gain, const float* k_gain,
-                                 const float* rope_table, int S, int L, int H, int K, float eps,
-                                 h3_stream_t stream);
+                                 const float* rope_table, const int* axis_dims, int pairing,
+                                 int S, int L, int H, int K, float eps, h3_stream_t stream);
 
 /*
  * a4 + a1 fused — a projection whose product goes straight into the FP32
@@ -251,6 +266,7 @@ typedef struct h3_block_config {
   float theta;       /* RoPE base                                     */
   float eps_ln;      /* LayerNorm epsilon of the modulation steps     */
   float eps_qk;      /* Q/K RMSNorm epsilon                           */
+  int rope_pairing;  /* 0 interleaved, 1 split-half (h3_qk_norm_rope_layout) */
 } h3_block_config;
 
 /* Block weights (device pointers, caller-owned). */

@@ -80,12 +80,20 @@ def test_linear_argument_errors(lib):
     assert st(lib, "h3_linear", P, P, P, 8, 9, 256, 64, NULL) == 1
     assert st(lib, "h3_linear_swiglu", P, P, P, 8, 8, 100, 64, NULL) == 2
     gain = ctypes.c_void_p(4096)
+    ax = ctypes.cast((ctypes.c_int * 3)(32, 48, 48), ctypes.c_void_p)
     f = "h3_linear_qk_norm_rope"
-    assert st(lib, f, P, P, P, gain, gain, P, 8, 8, 3, 64, 1e-6, NULL) == 2     # odd H
-    assert st(lib, f, P, P, P, gain, gain, P, 8, 8, 2, 60, 1e-6, NULL) == 2     # K % 64
-    assert st(lib, f, P, P, P, gain, gain, NULL, 8, 8, 2, 64, 1e-6, NULL) == 1  # no table
-    assert st(lib, f, P, P, PM, gain, gain, P, 8, 8, 2, 64, 1e-6, NULL) == 3
-    assert st(lib, f, P, P, P, gain, gain, P, 8, 8, 2, 64, -1.0, NULL) == 1     # eps < 0
+    assert st(lib, f, P, P, P, gain, gain, P, ax, 0, 8, 8, 3, 64, 1e-6, NULL) == 2     # odd H
+    assert st(lib, f, P, P, P, gain, gain, P, ax, 0, 8, 8, 2, 60, 1e-6, NULL) == 2     # K % 64
+    assert st(lib, f, P, P, P, gain, gain, NULL, ax, 0, 8, 8, 2, 64, 1e-6, NULL) == 1  # no table
+    assert st(lib, f, P, P, PM, gain, gain, P, ax, 0, 8, 8, 2, 64, 1e-6, NULL) == 3
+    assert st(lib, f, P, P, P, gain, gain, P, ax, 0, 8, 8, 2, 64, -1.0, NULL) == 1     # eps < 0
+    assert st(lib, f, P, P, P, gain, gain, P, ax, 2, 8, 8, 2, 64, 1e-6, NULL) == 1     # pairing
+    # split-half pairs need every section a multiple of 16: 32/48/48 is, 40/40/48 is not
+    ax40 = ctypes.cast((ctypes.c_int * 3)(40, 40, 48), ctypes.c_void_p)
+    assert st(lib, f, P, P, P, gain, gain, P, ax40, 1, 8, 8, 2, 64, 1e-6, NULL) == 2
+    f = "h3_qk_norm_rope_layout"
+    assert st(lib, f, P, P, P, P, P, ax40, 8, 8, 2, 128, 1e4, 1e-6, 1, NULL) == 2
+    assert st(lib, f, P, P, P, P, P, ax, 8, 8, 2, 128, 1e4, 1e-6, 3, NULL) == 1
     f = "h3_linear_residual"
     assert st(lib, f, P, P, P, P, 8, 8, 200, 64, NULL) == 2
     assert st(lib, f, P, P, P, NULL, 8, 8, 256, 64, NULL) == 1                 # no gate

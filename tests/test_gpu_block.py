@@ -13,9 +13,10 @@ pytestmark = pytest.mark.gpu
 dev = "cuda"
 
 
-def gpu_block(h3lib, shape, inp):
+def gpu_block(h3lib, shape, inp, rope_pairing=0):
     cfg = h3lib.block_config(shape.S, shape.L, shape.D, shape.H, shape.Dh, shape.F,
-                             shape.axis_dims, shape.theta, shape.eps_ln, shape.eps_qk)
+                             shape.axis_dims, shape.theta, shape.eps_ln, shape.eps_qk,
+                             rope_pairing)
     ws = torch.empty(h3lib.block_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     resid = inp["resid"].clone()
     h3lib.block_forward(cfg, inp, resid, inp["mod"], inp["pos"], ws)
@@ -23,14 +24,14 @@ def gpu_block(h3lib, shape, inp):
     return resid
 
 
-def check_block(out_rows, shape, inp, rows=None, what="block"):
+def check_block(out_rows, shape, inp, rows=None, what="block", rope_pairing="interleaved"):
     """Compares GPU output rows with the oracle's, with the block tolerance."""
     n = {k: np64(v) if v.is_floating_point() else v.cpu().numpy() for k, v in inp.items()}
     ref, mids = O.block_forward(n["resid"], n["mod"], n["w_qkv"], n["w_o"], n["w_gu"],
                                 n["w_down"], n["q_gain"], n["k_gain"], n["pos"], L=shape.L,
                                 heads=shape.H, head_dim=shape.Dh, axis_dims=shape.axis_dims,
                                 theta=shape.theta, eps_ln=shape.eps_ln, eps_qk=shape.eps_qk,
-                                rows=rows, return_intermediates=True)
+                                rows=rows, return_intermediates=True, rope_pairing=rope_pairing)
     r_in = n["resid"][:shape.L] if rows is None else n["resid"][rows]
     assert_close_block(np64(out_rows), ref, mids["f"], mids["o"], n["mod"][2], n["mod"][5], r_in,
                        what)
@@ -47,6 +48,17 @@ def test_block_small(h3lib, shape):
     inp = {k: v.to(dev) for k, v in I.block_inputs(shape, seed=0).items()}
     out = gpu_block(h3lib, shape, inp)
     check_block(out[:shape.L], shape, inp)
+    assert torch.equal(out[shape.L:], inp["resid"][shape.L:]), "pad rows written"
+
+
+@pytest.mark.parametrize("shape", SMALL[:2], ids=["tiny", "ragged3d"])
+def test_block_small_split_half_rope(h3lib, shape):
+    inp = {k: v.to(dev) for k, v in I.block_inputs(shape, seed=5).items()}
+    out = gpu_block(h3lib, shape, inp, rope_pairing=1)
+    check_block(out[:shape.L], shape, inp, what="block split-half", rope_pairing="half")
+    # the layout matters: the interleaved block gives a different result
+    other = gpu_block(h3lib, shape, inp, rope_pairing=0)
+    assert not torch.equal(out[:shape.L], other[:shape.L])
     assert torch.equal(out[shape.L:], inp["resid"][shape.L:]), "pad rows written"
 
 

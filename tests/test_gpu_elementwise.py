@@ -36,17 +36,19 @@ def test_swiglu_full_size(h3lib):
     assert bool((out[L:] == SENT).all())
 
 
-def run_qk(h3lib, S, L, H, axis_dims, pos, seed, rows=None):
+def run_qk(h3lib, S, L, H, axis_dims, pos, seed, rows=None, pairing=0):
     inp = I.qk_inputs(S, L, H, 128, seed, device=dev)
     q0, k0 = inp["q"].clone(), inp["k"].clone()
     q, k = inp["q"], inp["k"]
-    h3lib.qk_norm_rope(q, k, inp["q_gain"], inp["k_gain"], pos.to(dev), axis_dims, L, 1e4, 1e-6)
+    h3lib.qk_norm_rope(q, k, inp["q_gain"], inp["k_gain"], pos.to(dev), axis_dims, L, 1e4, 1e-6,
+                       pairing=pairing)
     h3lib.check_device_error()
     rows = np.arange(L) if rows is None else rows
     tr = torch.from_numpy(rows).to(dev)
     p = pos.numpy()[rows]
     for name, x0, x, g in (("q", q0, q, inp["q_gain"]), ("k", k0, k, inp["k_gain"])):
-        ref = O.qk_norm_rope(np64(x0[tr]), np64(g), p, axis_dims, 1e4, 1e-6)
+        ref = O.qk_norm_rope(np64(x0[tr]), np64(g), p, axis_dims, 1e4, 1e-6,
+                             ("interleaved", "half")[pairing])
         assert_close_bf16(np64(x[tr]), ref, f"qk_norm_rope {name}")
         assert torch.equal(x[L:], x0[L:]), "pad rows written"
 
@@ -60,6 +62,19 @@ def test_qk_norm_rope_3d_small(h3lib):
     S, L = 200, 190
     pos = I.positions_3d(S, L, grid=(3, 5, 12), n_tail=22)
     run_qk(h3lib, S, L, 5, (32, 48, 48), pos, seed=22)
+
+
+@pytest.mark.parametrize("S,L,H,axis", [(256, 250, 4, (32, 48, 48)), (70, 65, 3, (128, 0, 0)),
+                                         (200, 190, 5, (16, 64, 48)), (8, 1, 2, (0, 96, 32))])
+def test_qk_norm_rope_split_half(h3lib, S, L, H, axis):
+    pos = I.positions_3d(S, L, grid=(3, 5, 12), n_tail=max(0, L - 180))
+    run_qk(h3lib, S, L, H, axis, pos, seed=24, pairing=1)
+
+
+def test_qk_norm_rope_split_half_full_size(h3lib):
+    S, L, H = 58816, 58758, 42
+    run_qk(h3lib, S, L, H, (32, 48, 48), I.positions_3d(S, L), seed=25,
+           rows=sample_rows(L, 512, 25), pairing=1)
 
 
 def test_qk_norm_rope_full_size(h3lib):

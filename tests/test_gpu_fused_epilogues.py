@@ -52,14 +52,16 @@ def qkv_case(S, L, H, K, axis, pos, seed):
     return x, w, qg, kg
 
 
-@pytest.mark.parametrize("S,L,H,K,kind", [(256, 250, 4, 512, "3d"), (130, 129, 2, 64, "1d"),
-                                          (1000, 999, 6, 320, "3d")])
-def test_linear_qk_norm_rope_matches_unfused_and_oracle(h3lib, S, L, H, K, kind):
+@pytest.mark.parametrize("S,L,H,K,kind,pairing", [
+    (256, 250, 4, 512, "3d", 0), (130, 129, 2, 64, "1d", 0), (1000, 999, 6, 320, "3d", 0),
+    (256, 250, 4, 512, "3d", 1), (130, 129, 2, 64, "1d", 1), (300, 290, 2, 128, "3d16", 1)])
+def test_linear_qk_norm_rope_matches_unfused_and_oracle(h3lib, S, L, H, K, kind, pairing):
     D = H * 128
     if kind == "1d":
         pos, axis = I.positions_1d(S, L), (128, 0, 0)
     else:
-        pos, axis = I.positions_3d(S, L, grid=(3, 5, 12), n_tail=max(0, L - 180)), (32, 48, 48)
+        pos = I.positions_3d(S, L, grid=(3, 5, 12), n_tail=max(0, L - 180))
+        axis = (32, 48, 48) if kind == "3d" else (16, 64, 48)
     x, w, qg, kg = qkv_case(S, L, H, K, axis, pos, seed=H + K)
     tab = torch.empty(S, 64, 2, dtype=torch.float32, device=dev)
     h3lib.rope_table(pos.to(dev), axis, tab, L)
@@ -70,8 +72,8 @@ def test_linear_qk_norm_rope_matches_unfused_and_oracle(h3lib, S, L, H, K, kind)
     q, k = un[:, :D].view(S, H, 128), un[:, D:2 * D].view(S, H, 128)
     # q, k are strided views of the qkv buffer: run the unfused kernel on copies
     qc, kc = q.contiguous(), k.contiguous()
-    h3lib.qk_norm_rope(qc, kc, qg, kg, pos.to(dev), axis, L, 1e4, 1e-6)
-    h3lib.linear_qk_norm_rope(x, w, fu, qg, kg, tab, L, eps=1e-6)
+    h3lib.qk_norm_rope(qc, kc, qg, kg, pos.to(dev), axis, L, 1e4, 1e-6, pairing=pairing)
+    h3lib.linear_qk_norm_rope(x, w, fu, qg, kg, tab, axis, L, eps=1e-6, pairing=pairing)
     h3lib.check_device_error()
     # v columns: the plain product, bit for bit
     assert torch.equal(fu[:, 2 * D:], raw[:, 2 * D:])
@@ -88,9 +90,10 @@ def test_linear_qk_norm_rope_matches_unfused_and_oracle(h3lib, S, L, H, K, kind)
     # against the oracle: projection rounded to bf16, then RMSNorm + RoPE
     ref_qkv = O.linear(np64(x[:L]), np64(w))
     p = pos.numpy()[:L]
+    lay = ("interleaved", "half")[pairing]
     for name, lo, gain in (("q", 0, qg), ("k", D, kg)):
         ref = O.qk_norm_rope(ref_qkv[:, lo:lo + D].reshape(L, H, 128), np64(gain), p, axis, 1e4,
-                             1e-6)
+                             1e-6, lay)
         assert_close_bf16(np64(fu[:L, lo:lo + D]).reshape(L, H, 128), ref, f"fused {name}")
     assert_close_bf16(np64(fu[:L, 2 * D:]), ref_qkv[:, 2 * D:], "fused v")
     assert bool((fu[L:] == SENT).all()), "pad rows written"
@@ -104,7 +107,7 @@ def test_linear_qk_norm_rope_full_size_sampled(h3lib):
     tab = torch.empty(S, 64, 2, dtype=torch.float32, device=dev)
     h3lib.rope_table(pos.to(dev), axis, tab, L)
     fu = torch.full((S, 3 * D), SENT, dtype=torch.bfloat16, device=dev)
-    h3lib.linear_qk_norm_rope(x, w, fu, qg, kg, tab, L, eps=1e-6)
+    h3lib.linear_qk_norm_rope(x, w, fu, qg, kg, tab, axis, L, eps=1e-6)
     h3lib.check_device_error()
     rows = sample_rows(L, 128, 19)
     tr = torch.from_numpy(rows).to(dev)
