@@ -244,6 +244,52 @@ def oracle_sample(shape, n_kv=8192, n_q=96, seed=3):
     return ms, desc, t_kv + t_q
 
 
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                low = line.lower()
+                if low.startswith("model name") or low.startswith("cpu part") or \
+                        low.startswith("hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+_TINY_CODE = """
+import time, numpy as np, torch
+import oracle.h3_oracle as O
+from dit_transformer_block_gb300 import inputs as I
+sh = I.TINY
+n = {k: v.double().numpy() if v.is_floating_point() else v.numpy()
+     for k, v in I.block_inputs(sh, seed=0).items()}
+best = 1e9
+for _ in range(3):
+    t0 = time.perf_counter()
+    O.block_forward(n["resid"], n["mod"], n["w_qkv"], n["w_o"], n["w_gu"], n["w_down"],
+                    n["q_gain"], n["k_gain"], n["pos"], L=sh.L, heads=sh.H, head_dim=sh.Dh,
+                    axis_dims=sh.axis_dims, theta=sh.theta)
+    best = min(best, time.perf_counter() - t0)
+print(best * 1e3)
+"""
+
+
+def oracle_tiny_ms(threads=None):
+    """Whole oracle block on the 256-row configuration (every row), best of
+    three, in a child process so that the BLAS thread count can be fixed."""
+    env = dict(os.environ)
+    if threads is not None:
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[v] = str(threads)
+    out = subprocess.run([sys.executable, "-c", _TINY_CODE], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=300)
+    if out.returncode != 0:
+        return None
+    return round(float(out.stdout.strip().splitlines()[-1]), 2)
+
+
 def cpu_cores():
     try:
         import numpy  # noqa: F401
@@ -425,6 +471,8 @@ def run_ours(a):
     stage_ms = [statistics.mean(events[k][i].elapsed_time(events[k][i + 1])
                                 for k in range(a.steps)) for i in range(h3.BLOCK_STAGES)]
     step_ms = total_ms / a.steps
+    per_step = sorted(events[k][0].elapsed_time(events[k][h3.BLOCK_STAGES])
+                      for k in range(a.steps))
     red = max_over_ranks([step_ms] + stage_ms, device=dev)
     step_ms, stage_ms = red[0], red[1:]
 
@@ -502,11 +550,17 @@ def run_ours(a):
     if not a.no_cpu_baseline and world == 1:
         ms, desc, secs = oracle_sample(shape)
         cpu = {"value": round(ms, 1), "unit": "ms", "cores": cpu_cores(), "kind": "oracle",
-               "sample": desc + f" ({secs:.1f} s of CPU work)"}
+               "sample": desc + f" ({secs:.1f} s of CPU work)", "cpu_model": cpu_model(),
+               "tiny_block_ms": {"all_threads": oracle_tiny_ms(),
+                                 "one_thread": oracle_tiny_ms(1),
+                                 "workload": "whole oracle block, 256-row configuration "
+                                             "(L=250, D=512, 4 heads, F=1536), every row"}}
     value = job_value(step_ms, world)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "ms", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(step_ms, 3),
+        "ms_per_step_median": round(statistics.median(per_step), 3),
+        "ms_per_step_min": round(per_step[0], 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded: x~N(0,1), W~N(0,0.02) bf16; FP32 residual and modulation)",
         "config": {"workload": WORKLOAD, "S": S, "L": L, "D": D, "heads": H, "head_dim": Dh,
