@@ -127,18 +127,34 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
   const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp + 4));
   const float gain[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 
-  // Angles of this lane's pairs (4 interleaved pairs, or 8 split-half ones)
+  // Angles of this lane's pairs: 4 interleaved pairs; or, split-half, 8 pairs
+  // shared with the partner lane, each lane evaluating 4 of them
   constexpr int NP = HALF ? 8 : 4;
   const int32_t p3[3] = {__ldg(pos + 3 * row), __ldg(pos + 3 * row + 1), __ldg(pos + 3 * row + 2)};
   float cs[NP], sn[NP];
-  const int pair0 = HALF ? tab.half_pair0[sub] : sub * 4;
-#pragma unroll
-  for (int t = 0; t < NP; ++t) {
-    const int pr = pair0 + t;
-    rope_angle(p3[tab.axis[pr]], tab.omega[pr], sn[t], cs[t]);
-  }
   const int src_lane = (half << 4) + (HALF ? tab.half_src[sub] : 0);
   const bool first = HALF ? tab.half_first[sub] != 0 : true;
+  const int pair0 = (HALF ? tab.half_pair0[sub] : sub * 4) + (first ? 0 : 4);
+  float c4[4], s4[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int pr = pair0 + t;
+    rope_angle(p3[tab.axis[pr]], tab.omega[pr], s4[t], c4[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    if constexpr (HALF) {
+      const float oc = __shfl_sync(0xffffffffu, c4[t], src_lane);
+      const float os = __shfl_sync(0xffffffffu, s4[t], src_lane);
+      cs[t] = first ? c4[t] : oc;
+      sn[t] = first ? s4[t] : os;
+      cs[4 + t] = first ? oc : c4[t];
+      sn[4 + t] = first ? os : s4[t];
+    } else {
+      cs[t] = c4[t];
+      sn[t] = s4[t];
+    }
+  }
 
   for (int h0 = 0; h0 < H; h0 += 2 * QK_BATCH) {
     uint4 v[QK_BATCH];

@@ -10,7 +10,8 @@ capture of the second launch ends within a minute or two:
               plain and with Q/K RMSNorm + RoPE in the epilogue (after its RoPE
               table), then the down projection shape M = 8192, N = 5376,
               K = 14336 with the residual update in the epilogue (565 MB)
-  elementwise qk_norm_rope on 16384 x 42 x 128, SwiGLU on 16384 x 2 x 14336,
+  elementwise qk_norm_rope on 16384 x 42 x 128 (interleaved, then split-half
+              pairs), SwiGLU on 16384 x 2 x 14336,
               modulation/LN/residual on 16384 x 5376
   fp8         FP8 GEMM (QKV shape, M = 8192), per-row FP8 quantisation of
               8192 x 5376, SAGE quantisation and FP8 attention at S = L = 16384
@@ -65,6 +66,7 @@ def main(argv):
         hh = torch.empty(S, 5376, device=dev, dtype=torch.bfloat16)
         mod = torch.randn(6, 5376, generator=g, device=dev) * 0.1
         runs.append(lambda: h3.qk_norm_rope(qq, kk, ones, ones, pos, (32, 48, 48), S))
+        runs.append(lambda: h3.qk_norm_rope(qq, kk, ones, ones, pos, (32, 48, 48), S, pairing=1))
         runs.append(lambda: h3.swiglu(gu, u, S))
         runs.append(lambda: h3.mod_norm_residual(r, d, mod[2], mod[3], mod[4], hh, S))
     if "fp8" in which:
