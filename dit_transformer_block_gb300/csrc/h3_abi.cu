@@ -877,7 +877,6 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
   const int L = cfg->L, D = cfg->D, H = cfg->H, F = cfg->F;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  void* h = base + ws.bf.h;
   uint8_t* qkv = base + ws.bf.qkv;
   void* attn = base + ws.bf.attn;
   void* proj = base + ws.bf.proj;
@@ -917,18 +916,19 @@ h3_status h3_block_forward_fp8(const h3_block_config* cfg, const h3_block_weight
     return launch_attention_fp8(aq, ak, av, D, sq, sk, sv, out, D, L, H, sm_scale, s);
   };
   const RopeRequest rq{pos, cfg->axis_dims, cfg->theta, rope};
-  if ((st = launch_mod_norm_residual(resid, nullptr, nullptr, m, m + D, h, L, D, cfg->eps_ln,
-                                     s, nullptr, 1, 0, &rq)) != H3_OK ||
-      (st = quant(h, D)) != H3_OK ||
+  // the modulated LayerNorm passes write the FP8 codes of h1 / h2 directly
+  uint8_t* c8 = static_cast<uint8_t*>(codes);
+  if ((st = launch_mod_norm_residual(resid, nullptr, nullptr, m, m + D, nullptr, L, D,
+                                     cfg->eps_ln, s, nullptr, 1, 0, &rq, c8, sc)) != H3_OK ||
       (st = launch_gemm_fp8(codes, D, sc, w->w_qkv, D, w->s_qkv, qkv, ld_qkv, L, 3 * D, D,
                             GEMM_QK_NORM_ROPE, s, &qk)) != H3_OK ||
       (st = attention(qkv, attn)) != H3_OK ||
       (st = quant(attn, D)) != H3_OK ||
       (st = launch_gemm_fp8(codes, D, sc, w->w_o, D, w->s_o, proj, D, L, D, D, GEMM_STORE_BF16,
                             s)) != H3_OK ||
-      (st = launch_mod_norm_residual(resid, proj, m + 2 * D, m + 3 * D, m + 4 * D, h, L, D,
-                                     cfg->eps_ln, s)) != H3_OK ||
-      (st = quant(h, D)) != H3_OK ||
+      (st = launch_mod_norm_residual(resid, proj, m + 2 * D, m + 3 * D, m + 4 * D, nullptr, L,
+                                     D, cfg->eps_ln, s, nullptr, 1, 0, nullptr, c8, sc)) !=
+          H3_OK ||
       (st = launch_gemm_fp8(codes, D, sc, w->w_gu, D, w->s_gu, ffn, F, L, F, D, GEMM_SWIGLU,
                             s)) != H3_OK ||
       (st = quant(ffn, F)) != H3_OK ||

@@ -214,6 +214,27 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
 // two-pass mean/variance.
 constexpr int MNR_THREADS = 256;
 
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+// Block-wide max over MNR_THREADS threads; red[] may still be read from a
+// previous reduction, hence the leading barrier.
+__device__ __forceinline__ float block_max_mnr(float v, float* red) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = (lane < 256 / 32) ? red[lane] : 0.f;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, m));
+  return t;
+}
+
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
@@ -232,14 +253,18 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // Indices outside [0, num_seg) are clamped so every read stays in the table.
 // ROPE: the CTA also writes its row of the RoPE (cos, sin) table (threads
 // 0-63, one pair each, while the row's loads are in flight).
-template <int VPT, bool ROPE>
+// Q8: instead of the bf16 row, the row's E4M3 codes and scale, the per-row
+// quantisation of quantize_fp8_rows applied to the bf16-rounded values (the
+// same arithmetic, so the codes equal the unfused path's).
+template <int VPT, bool ROPE, bool Q8>
 __global__ void __launch_bounds__(MNR_THREADS)
     mod_norm_residual_kernel(float* __restrict__ resid, const __nv_bfloat16* __restrict__ delta,
                              const float* __restrict__ gate, const float* __restrict__ shift,
                              const float* __restrict__ scale, __nv_bfloat16* __restrict__ normed,
                              int D, float eps, const int32_t* __restrict__ seg, int num_seg,
                              int64_t seg_stride, const int32_t* __restrict__ pos,
-                             float2* __restrict__ rope_out, const RopeTable tab) {
+                             float2* __restrict__ rope_out, const RopeTable tab,
+                             uint8_t* __restrict__ codes, float* __restrict__ code_scale) {
   __shared__ float red[MNR_THREADS / 32];
   const int row = blockIdx.x;
   if (seg != nullptr) {
@@ -281,7 +306,7 @@ __global__ void __launch_bounds__(MNR_THREADS)
       }
     }
   }
-  if (normed == nullptr) return;
+  if (!Q8 && normed == nullptr) return;
   float s = 0.f;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) s += (x[v].x + x[v].y) + (x[v].z + x[v].w);
@@ -297,6 +322,37 @@ __global__ void __launch_bounds__(MNR_THREADS)
   }
   const float var = block_sum(s2, red) / static_cast<float>(D);
   const float rstd = rsqrtf(var + eps);
+  if constexpr (Q8) {
+    float hv[VPT][4];
+    float amax = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = threadIdx.x + v * MNR_THREADS;
+      hv[v][0] = hv[v][1] = hv[v][2] = hv[v][3] = 0.f;
+      if (c < D4) {
+        const float4 sc = __ldg(reinterpret_cast<const float4*>(scale) + c);
+        const float4 sh = __ldg(reinterpret_cast<const float4*>(shift) + c);
+        hv[v][0] = round_to_bf16(fmaf((x[v].x - mean) * rstd, 1.0f + sc.x, sh.x));
+        hv[v][1] = round_to_bf16(fmaf((x[v].y - mean) * rstd, 1.0f + sc.y, sh.y));
+        hv[v][2] = round_to_bf16(fmaf((x[v].z - mean) * rstd, 1.0f + sc.z, sh.z));
+        hv[v][3] = round_to_bf16(fmaf((x[v].w - mean) * rstd, 1.0f + sc.w, sh.w));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv[v][0]), fabsf(hv[v][1])),
+                                 fmaxf(fabsf(hv[v][2]), fabsf(hv[v][3]))));
+      }
+    }
+    amax = block_max_mnr(amax, red);
+    const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 0.f;
+    uint32_t* qrow = reinterpret_cast<uint32_t*>(codes + static_cast<int64_t>(row) * D);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = threadIdx.x + v * MNR_THREADS;
+      if (c < D4)
+        qrow[c] = e4m3x4(__fmul_rn(hv[v][0], inv), __fmul_rn(hv[v][1], inv),
+                         __fmul_rn(hv[v][2], inv), __fmul_rn(hv[v][3], inv));
+    }
+    if (threadIdx.x == 0) code_scale[row] = __fdiv_rn(amax, 448.0f);
+    return;
+  }
   uint2* hrow = reinterpret_cast<uint2*>(normed + static_cast<int64_t>(row) * D);
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
@@ -378,12 +434,6 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, m));
   return t;
-}
-
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return lo | (hi << 16);
 }
 
 template <int VPT>  // 8-element chunks per thread
@@ -528,7 +578,8 @@ h3_status launch_qk_norm_rope(void* q, void* k, int64_t row_stride, const float*
 h3_status launch_mod_norm_residual(float* resid, const void* delta, const float* gate,
                                    const float* shift, const float* scale, void* normed, int L,
                                    int D, float eps, cudaStream_t s, const int32_t* seg,
-                                   int num_seg, int64_t seg_stride, const RopeRequest* rope) {
+                                   int num_seg, int64_t seg_stride, const RopeRequest* rope,
+                                   uint8_t* codes, float* code_scale) {
   const int vpt = (D / 4 + MNR_THREADS - 1) / MNR_THREADS;
   const auto* d = static_cast<const __nv_bfloat16*>(delta);
   auto* n = static_cast<__nv_bfloat16*>(normed);
@@ -536,16 +587,23 @@ h3_status launch_mod_norm_residual(float* resid, const void* delta, const float*
   if (rope != nullptr) tab = rope_table(rope->axis_dims, rope->theta);
   const int32_t* pos = rope ? rope->pos : nullptr;
   float2* out = rope ? rope->out : nullptr;
-#define H3_MNR_LAUNCH(V, R)                                                              \
-  mod_norm_residual_kernel<V, R><<<L, MNR_THREADS, 0, s>>>(resid, d, gate, shift, scale, n, D, \
-                                                           eps, seg, num_seg, seg_stride, pos, \
-                                                           out, tab)
-#define H3_MNR_CASE(V)                  \
-  case V:                               \
-    if (rope != nullptr)                \
-      H3_MNR_LAUNCH(V, true);           \
-    else                                \
-      H3_MNR_LAUNCH(V, false);          \
+#define H3_MNR_LAUNCH(V, R, Q)                                                          \
+  mod_norm_residual_kernel<V, R, Q><<<L, MNR_THREADS, 0, s>>>(                          \
+      resid, d, gate, shift, scale, n, D, eps, seg, num_seg, seg_stride, pos, out, tab, \
+      codes, code_scale)
+#define H3_MNR_CASE(V)                      \
+  case V:                                   \
+    if (codes != nullptr) {                 \
+      if (rope != nullptr)                  \
+        H3_MNR_LAUNCH(V, true, true);       \
+      else                                  \
+        H3_MNR_LAUNCH(V, false, true);      \
+    } else {                                \
+      if (rope != nullptr)                  \
+        H3_MNR_LAUNCH(V, true, false);      \
+      else                                  \
+        H3_MNR_LAUNCH(V, false, false);     \
+    }                                       \
     break;
   switch (vpt) {
     H3_MNR_CASE(1)

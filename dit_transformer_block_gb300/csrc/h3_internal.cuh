@@ -64,11 +64,15 @@ struct RopeRequest {
 };
 // seg (optional): per-row token-group index into a table whose groups are
 // seg_stride floats apart (gate/shift/scale point at group 0).
+// codes (optional): write the normalised row as per-row E4M3 codes [L, D]
+// and scales code_scale [L] (launch_quantize_fp8_rows of the bf16 row)
+// instead of the bf16 row `normed`.
 h3_status launch_mod_norm_residual(float* resid, const void* delta, const float* gate,
                                    const float* shift, const float* scale, void* normed, int L,
                                    int D, float eps, cudaStream_t s, const int32_t* seg = nullptr,
                                    int num_seg = 1, int64_t seg_stride = 0,
-                                   const RopeRequest* rope = nullptr);
+                                   const RopeRequest* rope = nullptr, uint8_t* codes = nullptr,
+                                   float* code_scale = nullptr);
 
 // (cos, sin) of every RoPE angle of rows [0, L): out[i * 64 + p] for channel
 // pair p of a 128-channel head, the angle formed and reduced exactly as

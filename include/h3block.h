@@ -400,7 +400,9 @@ size_t h3_block_workspace_bytes_fp8(const h3_block_config* cfg);
 
 /* h3_block_forward with the four projections in FP8: every projection input
  * (h1, the attention output, h2, the SwiGLU output) is quantised per token
- * with h3_quantize_fp8_rows before its FP8 GEMM. fp8_attention != 0 also runs
+ * as h3_quantize_fp8_rows does it before its FP8 GEMM (h1 and h2 by the
+ * modulated LayerNorm passes themselves, from their bf16-rounded rows, so no
+ * bf16 copy of them is written). fp8_attention != 0 also runs
  * the attention in FP8 (h3_sage_quantize + h3_attention_fp8); otherwise the
  * attention and everything else (modulation, Q/K RMSNorm + RoPE, SwiGLU) is
  * the BF16/FP32 path. D % 128 == 0, F % 128 == 0 in addition to
