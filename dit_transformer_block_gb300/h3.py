@@ -103,7 +103,7 @@ def lib() -> ctypes.CDLL:
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is not built; run `python -m "
-                               "dit_transformer_block_gb300.build` or __graft_entry__.build()")
+                               "dit_transformer_block_gb300.build`")
         L = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in _SIGS.items():
             f = getattr(L, name)
