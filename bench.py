@@ -249,9 +249,11 @@ def cpu_model():
         with open("/proc/cpuinfo") as f:
             for line in f:
                 low = line.lower()
-                if low.startswith("model name") or low.startswith("cpu part") or \
-                        low.startswith("hardware"):
+                if low.startswith("model name") or low.startswith("hardware"):
                     return line.split(":", 1)[1].strip()
+                if low.startswith("cpu part"):
+                    import platform
+                    return f"{platform.machine()} CPU part {line.split(':', 1)[1].strip()}"
     except OSError:
         pass
     import platform
