@@ -78,6 +78,23 @@ def test_block_deterministic_and_pad_invariant(h3lib):
     assert torch.equal(a[:shape.L], c[:shape.L])
 
 
+def test_block_valid_rows_unchanged_when_the_buffer_grows(h3lib):
+    # the same valid rows in a buffer with 128 more pad rows give the same bits
+    shape = I.TINY
+    inp = {k: v.to(dev) for k, v in I.block_inputs(shape, seed=2).items()}
+    a = gpu_block(h3lib, shape, inp)
+    big = I.BlockShape(S=shape.S + 128, L=shape.L, D=shape.D, H=shape.H, Dh=shape.Dh,
+                       F=shape.F, axis_dims=shape.axis_dims, theta=shape.theta)
+    grow = lambda t, fill: torch.cat([t, torch.full((128,) + tuple(t.shape[1:]), fill,
+                                                    dtype=t.dtype, device=dev)])
+    inp2 = dict(inp)
+    inp2["resid"] = grow(inp["resid"], 3.5)
+    inp2["pos"] = grow(inp["pos"], 7)
+    b = gpu_block(h3lib, big, inp2)
+    assert torch.equal(a[:shape.L], b[:shape.L])
+    assert torch.equal(b[shape.L:], inp2["resid"][shape.L:])
+
+
 @pytest.mark.slow
 def test_block_full_size_sampled(h3lib):
     shape = I.FULL
