@@ -78,6 +78,19 @@ def test_block_deterministic_and_pad_invariant(h3lib):
     assert torch.equal(a[:shape.L], c[:shape.L])
 
 
+@pytest.mark.parametrize("L", [300, 129])
+def test_block_full_width_short_sequence(h3lib, L):
+    # the full hidden width (5376, 42 heads, SwiGLU 14336) on a short ragged
+    # sequence: every row against the oracle
+    S = (L + 63) // 64 * 64
+    shape = I.BlockShape(S=S, L=L, D=5376, H=42, Dh=128, F=14336, axis_dims=(32, 48, 48),
+                         pos_kind="3d", grid=(31, 24, 79), n_tail=22)
+    inp = I.block_inputs(shape, seed=L, device=dev)
+    out = gpu_block(h3lib, shape, inp)
+    check_block(out[:L], shape, inp, what=f"full-width block L={L}")
+    assert torch.equal(out[L:], inp["resid"][L:])
+
+
 def test_block_valid_rows_unchanged_when_the_buffer_grows(h3lib):
     # the same valid rows in a buffer with 128 more pad rows give the same bits
     shape = I.TINY
