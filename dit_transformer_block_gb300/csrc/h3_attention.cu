@@ -98,6 +98,54 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
     for (int c = 0; c < 128; ++c)
       if (c >= valid) sr[c] = 0xff800000u;
   }
+  if constexpr (!F8 && !SKIP) {
+    if (o_live) {
+      // Speculative pass (every tile after the first, whose running max is
+      // finite for every row): the exponentials use the current running max
+      // while the tile's max forms beside them, so the max is off the
+      // critical path. When no row of the warp exceeds the running max by
+      // more than the threshold — nearly always after the first tiles — this
+      // is exactly the pass below with m unchanged (same operations, same
+      // order); otherwise P is recomputed by the exact pass below.
+      const float neg_m0 = -m;
+      float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
+      float xa = -INFINITY, xb = -INFINITY, xc = -INFINITY, xd = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float s0 = __uint_as_float(sr[c * 32 + 2 * i]);
+          const float s1 = __uint_as_float(sr[c * 32 + 2 * i + 1]);
+          if ((i & 3) == 0)
+            xa = max3f(xa, s0, s1);
+          else if ((i & 3) == 1)
+            xb = max3f(xb, s0, s1);
+          else if ((i & 3) == 2)
+            xc = max3f(xc, s0, s1);
+          else
+            xd = max3f(xd, s0, s1);
+          float x0, x1;
+          ffma2_bc(x0, x1, s0, s1, scale_log2, neg_m0);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          if (i & 1)
+            fadd2(sc, sd, p0, p1);
+          else
+            fadd2(sa, sb, p0, p1);
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      const float mxs = max3f(xa, xb, fmaxf(xc, xd)) * scale_log2;
+      if (!__any_sync(0xffffffffu, mxs > m + RESCALE_THRESHOLD)) {
+        l += (sa + sb) + (sc + sd);
+        tmem_st_wait();
+        return false;
+      }
+      tmem_st_wait();  // the exact pass overwrites P
+    }
+  }
   // Row max of the raw products (the scale is positive, so it commutes with
   // max), four independent 3-input max chains.
   float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
