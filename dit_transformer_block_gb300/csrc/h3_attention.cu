@@ -22,7 +22,10 @@
 //   * online softmax in base 2 with the scale folded in (packed FP32 FMA and
 //     add, 3-input max); the running max is raised only when a row's new max
 //     exceeds it by more than 8 (then O and the row sum are rescaled), so
-//     most tiles skip the O round trip; only the last KV tile is masked.
+//     most tiles skip the O round trip; after the first tile the
+//     exponentials run against the current max while the tile max forms
+//     beside them, the exact pass only redoing a tile whose max crossed the
+//     threshold; only the last KV tile is masked.
 // Both query tiles read every K/V tile from shared memory, which halves the
 // shared-memory operand traffic per FLOP of a one-tile-per-CTA design.
 #include <cuda_bf16.h>

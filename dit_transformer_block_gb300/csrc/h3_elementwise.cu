@@ -213,8 +213,8 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
 // VPT float4 of the row in registers between the residual update and the
 // two-pass mean/variance.
 // 256 threads per row for the passes without a residual add, 512 for those
-// with one (measured at the full width: 6.97 vs 6.28 TB/s and 6.09 vs
-// 6.65 TB/s respectively).
+// with one: at the full width 256 threads beat 512 on the first kind
+// (6.97 vs 6.28 TB/s) and 512 beat 256 on the second (6.65 vs 6.09 TB/s).
 constexpr int MNR_THREADS = 256;
 constexpr int MNR_THREADS_RESID = 512;
 
