@@ -404,10 +404,22 @@ def profile_traffic(kernel_file: str, profile_md: str):
     h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", text)
     if not m or not h:
         return None
-    src = open(os.path.join(ROOT, "dit_transformer_block_gb300", "csrc", kernel_file), "rb").read()
-    if not hashlib.sha256(src).hexdigest().startswith(h.group(1)):
+    src = open(os.path.join(ROOT, "dit_transformer_block_gb300", "csrc", kernel_file)).read()
+    if not code_sha256(src).startswith(h.group(1)):
         return None
     return float(m.group(1))
+
+
+def code_sha256(src: str) -> str:
+    """SHA-256 of a CUDA source with its // comments, trailing blanks and
+    empty lines removed, so that only a change of the code itself makes a
+    recorded counter stale."""
+    lines = []
+    for line in src.splitlines():
+        line = re.sub(r"//.*$", "", line).rstrip()
+        if line:
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
 def run_ours(a):
