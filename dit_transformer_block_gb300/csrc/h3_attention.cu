@@ -294,7 +294,8 @@ enum Bar2 {
   B2_S = B2_KV_EMPTY + KV_SLOTS,
   B2_P = B2_S + 2,
   B2_O = B2_P + 2,
-  B2_NUM = B2_O + 2
+  B2_DRAIN = B2_O + 2,  // the MMA thread's last commit, waited on before exit
+  B2_NUM = B2_DRAIN + 1
 };
 // barriers, the TMEM address word (padded to 16 bytes) and 16 vote flags
 static_assert(B2_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
@@ -354,6 +355,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
           tma_load_2d(smem_u32(sQ + i * T_BYTES + BOX_BYTES), &tmQ, bar(B2_Q), col0 + 64,
                       q0 + i * BQ);
       }
+      int issued = 0;
       for (int t = 0; t < 2 * n; ++t) {  // even t: K_{t/2}, odd t: V_{t/2}
         const int slot = t % KV_SLOTS;
         const uint32_t use = static_cast<uint32_t>(t / KV_SLOTS);
@@ -366,7 +368,18 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         tma_load_2d(smem_u32(dst), m, full, col0, (t >> 1) * BKV);
         if constexpr (!F8)
           tma_load_2d(smem_u32(dst + BOX_BYTES), m, full, col0 + 64, (t >> 1) * BKV);
+        issued = t + 1;
       }
+      // No copy of this CTA may still be landing when it exits (after an
+      // error the consumers may not have waited for them): wait, bounded, for
+      // Q and for the last load of every slot. In a normal run these phases
+      // completed long ago.
+      const uint64_t t0 = globaltimer_ns();
+      const uint64_t lim = drain_limit_ns(a.err);
+      mbar_wait_drain(bar(B2_Q), 0u, t0, lim);
+      for (int t = issued > KV_SLOTS ? issued - KV_SLOTS : 0; t < issued; ++t)
+        mbar_wait_drain(bar(B2_KV_FULL + t % KV_SLOTS),
+                        static_cast<uint32_t>(t / KV_SLOTS) & 1u, t0, lim);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
@@ -448,6 +461,11 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
           mma_commit(bar(B2_KV_EMPTY + slot_of(2 * j + 2)));
         }
       }
+      // Every MMA issued here must be done with shared and tensor memory
+      // before the CTA frees them (after an error no consumer may have waited
+      // for the last ones): commit and wait, bounded.
+      mma_commit(bar(B2_DRAIN));
+      mbar_wait_drain(bar(B2_DRAIN), 0u, globaltimer_ns(), drain_limit_ns(a.err));
     }
   } else {
     // ---------------------------------------------------------- softmax

@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* empty = bars + STAGES;       // [STAGES]
   uint64_t* tfull = bars + 2 * STAGES;   // [2]
   uint64_t* tempty = tfull + 2;          // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* drain = tempty + 2;          // the MMA thread's last commit
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&tfull[b]), 1);
       mbar_init(smem_u32(&tempty[b]), 4);
     }
+    mbar_init(smem_u32(drain), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int issued = 0;  // stage loads issued: load i went to stage i % STAGES, parity (i / STAGES) & 1
       for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
         int mb, nb;
         tile_coords(tile, a, mb, nb);
@@ -179,12 +182,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, fb, kx, mb * BM);
           tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB, fb, kx, b_row0);
           tma_load_2d(smem_u32(sB + stage * B_BYTES + B_BYTES / 2), &tmB, fb, kx, b_row1);
+          ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
+      // No copy of this CTA may still be landing when it exits (after an
+      // error the consumer may not have waited for them): wait, bounded, for
+      // the last load of every stage.
+      const uint64_t t0 = globaltimer_ns();
+      for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+        mbar_wait_drain(smem_u32(&full[i % STAGES]), static_cast<uint32_t>(i / STAGES) & 1u, t0,
+                        drain_limit_ns(a.err));
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
@@ -227,6 +238,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
+      // every MMA issued here must be done with shared and tensor memory
+      // before the CTA frees them: commit and wait, bounded
+      mma_commit(smem_u32(drain));
+      mbar_wait_drain(smem_u32(drain), 0u, globaltimer_ns(), drain_limit_ns(a.err));
     }
   } else {
     // ------------------------------------------------------ epilogue warps

@@ -90,6 +90,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const D
   }
 }
 
+// Waits for a phase that copies this CTA issued will complete, ignoring the
+// device error word (so a CTA that is leaving because of an error still lets
+// its own copies land first), until limit_ns after t0. Returns whether the
+// phase completed.
+// Limit for such waits: the wait limit, but at least 100 ms (a copy lands in
+// microseconds; a short wait limit must not cut the drain short).
+__device__ __forceinline__ uint64_t drain_limit_ns(const DevErr& e) {
+  return e.timeout_ns > 100000000ull ? e.timeout_ns : 100000000ull;
+}
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t t0,
+                                                uint64_t limit_ns) {
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
