@@ -61,10 +61,6 @@ struct AttnArgs {
   DevErr err;
 };
 
-__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // One KV tile of the online softmax for the calling thread's query row (TMEM
 // lane). S_j is read from tS; P_j (bf16 pairs) is written over its first 64
 // columns. valid = keys of this tile that are < L (>= BKV: none masked).
@@ -73,7 +69,10 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
 // Skip-Softmax (skip != 0): the four warps of a query tile vote; when every
 // row's tile maximum lies more than skip_log2 below its running maximum the
 // tile is skipped (no exp2, no P; flags[quarter] tells the MMA warp to leave
-// out its P V product) and the function returns true.
+// out its P V product) and the function returns true. The vote is exchanged
+// through flags and the mbarrier vote_bar (one arrival per warp, phase
+// vote_parity), waited on with the usual limit; if that wait runs out, ok is
+// cleared and the function returns at once.
 // F8: P is written as E4M3 codes (four per column, 32 columns) and the
 // running max is kept an integer, so every P is an exact power-of-two multiple
 // of the P against any other integer reference.
@@ -81,7 +80,8 @@ template <bool F8, bool SKIP>
 __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid, bool o_live,
                                              float scale_log2, float& m, float& l,
                                              float skip_log2, volatile uint32_t* flags,
-                                             int bar_id) {
+                                             uint32_t vote_bar, uint32_t vote_parity,
+                                             const DevErr& err, bool& ok) {
   uint32_t sr[128];
   {
     uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
@@ -165,7 +165,12 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
     const uint32_t warp_skip = __all_sync(0xffffffffu, row_skip) ? 1u : 0u;
     const int quarter = (threadIdx.x >> 5) & 3;
     if ((threadIdx.x & 31) == 0) flags[quarter] = warp_skip;
-    named_barrier_sync(bar_id, 128);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(vote_bar);
+    if (!mbar_wait(vote_bar, vote_parity, err, ERR_WAIT_ATTN_SOFTMAX)) {
+      ok = false;
+      return true;
+    }
     if (flags[0] & flags[1] & flags[2] & flags[3]) return true;
   }
   // Raise the running max only when it is exceeded by more than the
@@ -295,7 +300,8 @@ enum Bar2 {
   B2_P = B2_S + 2,
   B2_O = B2_P + 2,
   B2_DRAIN = B2_O + 2,  // the MMA thread's last commit, waited on before exit
-  B2_NUM = B2_DRAIN + 1
+  B2_VOTE = B2_DRAIN + 1,  // Skip-Softmax vote of each query tile's four warps
+  B2_NUM = B2_VOTE + 2
 };
 // barriers, the TMEM address word (padded to 16 bytes) and 16 vote flags
 static_assert(B2_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
@@ -330,7 +336,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
   const int n = a.num_kv;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B2_NUM; ++i) mbar_init(bar(i), (i == B2_P || i == B2_P + 1) ? 128 : 1);
+    for (int i = 0; i < B2_NUM; ++i)
+      mbar_init(bar(i), (i == B2_P || i == B2_P + 1) ? 128 : (i >= B2_VOTE ? 4 : 1));
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -493,7 +500,9 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       // multiplier positive
       if constexpr (F8) mul = fmaxf(mul * sq_tile * __ldg(a.sk + j * a.H + blockIdx.y), 1e-30f);
       softmax_tile<F8, SKIP>(tS, tO, a.L - j * BKV, j > 0, mul, m, l, a.skip_log2,
-                             skip_flags + (tile * 2 + (j & 1)) * 4, 1 + tile);
+                             skip_flags + (tile * 2 + (j & 1)) * 4, bar(B2_VOTE + tile),
+                             static_cast<uint32_t>(j) & 1u, a.err, ok);
+      if (!ok) break;
       tc_fence_before();
       mbar_arrive(bar(B2_P + tile));
     }
