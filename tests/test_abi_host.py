@@ -2,6 +2,7 @@
 exports every function include/h3block.h declares, and rejects bad
 arguments on the host with the documented status before any launch."""
 import ctypes
+import os
 
 import pytest
 
@@ -162,3 +163,27 @@ def test_stack_and_segmented_argument_errors(lib):
     assert g(P, P, P, NULL, NULL, P, 2, 32, NULL, 8, 8, 64, 1e-6, NULL) == 1    # stride < D
     assert g(P, P, P, NULL, NULL, P, 2, 66, NULL, 8, 8, 64, 1e-6, NULL) == 3    # stride % 4
     assert g(P, P, P, NULL, NULL, P, 0, 512, NULL, 8, 8, 64, 1e-6, NULL) == 1   # no groups
+
+
+def test_stage_tables_agree_with_the_header():
+    # the binding's stage count and names, the bench's per-stage work model and
+    # the header's H3_BLOCK_STAGES describe the same stages
+    import re
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    hdr = open(os.path.join(root, "include", "h3block.h")).read()
+    n = int(re.search(r"#define H3_BLOCK_STAGES (\d+)", hdr).group(1))
+    assert h3.BLOCK_STAGES == n == len(h3.STAGE_NAMES)
+    work = bench.stage_work(58816, 58758, 5376, 42, 128, 14336)
+    assert len(work) == n
+    # the tensor-bound stages carry the GEMM and attention FLOPs exactly
+    bw = bench.block_work(58816, 58758, 5376, 42, 128, 14336)
+    tensor = sum(w for b, w, _ in work if b == "tensor")
+    assert abs(tensor - (bw["gemm_flop"] + bw["attn_flop"])) < 1e-6 * tensor
+
+
+def test_recorded_traffic_hash_ignores_comments():
+    import bench
+    code = "int f() {\n  return 1;  // one\n}\n"
+    assert bench.code_sha256(code) == bench.code_sha256("// header\nint f() {\n\n  return 1;\n}")
+    assert bench.code_sha256(code) != bench.code_sha256("int f() {\n  return 2;\n}\n")
