@@ -311,13 +311,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float4* gp = reinterpret_cast<const float4*>(grow + c * 32);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              float4 r = rp[q];
+              float4 r = __ldcs(rp + q);
               const float4 g = __ldg(gp + q);
               r.x = fmaf(g.x, f[4 * q + 0], r.x);
               r.y = fmaf(g.y, f[4 * q + 1], r.y);
               r.z = fmaf(g.z, f[4 * q + 2], r.z);
               r.w = fmaf(g.w, f[4 * q + 3], r.w);
-              rp[q] = r;
+              __stcs(rp + q, r);
             }
           }
         }
