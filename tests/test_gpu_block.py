@@ -62,6 +62,33 @@ def test_block_small_split_half_rope(h3lib, shape):
     assert torch.equal(out[shape.L:], inp["resid"][shape.L:]), "pad rows written"
 
 
+def test_block_forward_events_times_every_stage_and_changes_nothing(h3lib):
+    # h3_block_forward_events runs the same kernels as h3_block_forward and
+    # records one event before every stage and one after the last
+    shape = SMALL[1]
+    inp = {k: v.to(dev) for k, v in I.block_inputs(shape, seed=4).items()}
+    plain = gpu_block(h3lib, shape, inp)
+    cfg = h3lib.block_config(shape.S, shape.L, shape.D, shape.H, shape.Dh, shape.F,
+                             shape.axis_dims, shape.theta, shape.eps_ln, shape.eps_qk)
+    ws = torch.empty(h3lib.block_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(h3lib.BLOCK_STAGES + 1)]
+    for e in events:  # create the handles before they are handed to the library
+        e.record(stream)
+    resid = inp["resid"].clone()
+    h3lib.block_forward(cfg, inp, resid, inp["mod"], inp["pos"], ws, events=events)
+    h3lib.check_device_error()
+    torch.cuda.synchronize()
+    assert torch.equal(resid, plain)
+    stage = [events[i].elapsed_time(events[i + 1]) for i in range(h3lib.BLOCK_STAGES)]
+    total = events[0].elapsed_time(events[-1])
+    assert all(t > 0 for t in stage)
+    assert abs(sum(stage) - total) <= 1e-3 * total + 1e-3
+    # a wrong number of events is refused before anything runs
+    with pytest.raises(h3lib.H3Error):
+        h3lib.block_forward(cfg, inp, resid, inp["mod"], inp["pos"], ws, events=events[:-1])
+
+
 def test_block_deterministic_and_pad_invariant(h3lib):
     shape = I.TINY
     inp = {k: v.to(dev) for k, v in I.block_inputs(shape, seed=1).items()}
