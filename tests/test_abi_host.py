@@ -187,3 +187,20 @@ def test_recorded_traffic_hash_ignores_comments():
     code = "int f() {\n  return 1;  // one\n}\n"
     assert bench.code_sha256(code) == bench.code_sha256("// header\nint f() {\n\n  return 1;\n}")
     assert bench.code_sha256(code) != bench.code_sha256("int f() {\n  return 2;\n}\n")
+
+
+def test_binding_argument_counts_match_the_header():
+    # every prototype's parameter count equals the ctypes signature's, so a
+    # header change that the binding missed fails here rather than on a GPU
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "h3block.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"(h3_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text):
+        args = m.group(2).strip()
+        n = 0 if args in ("", "void") else len([a for a in args.split(",") if a.strip()])
+        protos[m.group(1)] = n
+    assert set(protos) == set(h3._SIGS)
+    for name, (_, argtypes) in h3._SIGS.items():
+        assert len(argtypes) == protos[name], (name, len(argtypes), protos[name])
