@@ -35,7 +35,7 @@ def _rank(rank, world, port, out):
 
 def test_max_over_ranks_two_gloo_ranks():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of a multi-threaded process
     out = mgr.dict()
     mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
     for r in range(world):
