@@ -517,23 +517,22 @@ def attention_skip(q, k, v, L: int, scale: float, eps: float, tile: int = 128):
 
 
 # ---------------------------------------------------------------------------
-# FP8 ("SAGE") attention ([vLLM-Omni H3 blog] section 4.3: the attention
-# backend can quantise Q, K, P and V to FP8 for the QK and PV products). The
-# pages give no scaling scheme; the reading here:
+# FP8 ("SAGE") attention ([vLLM-Omni H3 blog] section 4.3, Fig. 6: the
+# attention backend can quantise Q, K, P and V to FP8 for the QK and PV
+# products). The pages give no scaling scheme; the reading here treats every
+# one of the four operands the same way, with absmax scaling into E4M3's full
+# range (inv = 448 / amax, code = e4m3(x * inv), scale = amax / 448, every
+# step in float32):
 #   * K is first smoothed by subtracting its per-(head, channel) mean over the
-#     L valid keys, taken in float32 (softmax is unchanged: each row's scores
-#     move by one constant);
-#   * Q and the smoothed K are quantised to E4M3 per (128-row tile, head)
-#     block, V per (head, channel) over the valid keys, each with absmax
-#     scaling (inv = 448 / amax, code = e4m3(x * inv), scale = amax / 448,
-#     every step in float32);
-#   * scores = (Q codes . K codes) * sq * sk; softmax in base 2 against an
-#     integer reference at or above the row maximum (the ceiling of the row
-#     maximum: any integer reference gives P values that differ by an exact
-#     power of two, so their E4M3 codes agree in the normal range); 224 * P
-#     (at most 448) is rounded to E4M3 for the PV product, which keeps P down
-#     to 2^-14 of the row maximum in E4M3's normal range; the row sum uses the
-#     unrounded 224 * P; O = (P codes . V codes) * sv / sum.
+#     L valid keys (the exact mean rounded once to float32; softmax is
+#     unchanged because each row's scores move by one constant);
+#   * Q and the smoothed K are quantised per (128-row tile, head) block, V per
+#     (head, channel) over the valid keys;
+#   * scores = (Q codes . K codes) * sq * sk; the softmax weights are
+#     p = 2^(z - max z) with the exact row maximum, so every row of P has
+#     absmax exactly 1 and is quantised as 448 * p (scale 1 / 448);
+#   * the row sum uses the unrounded p; O = (P codes . V codes) * sv / 448 /
+#     sum p.
 # ---------------------------------------------------------------------------
 
 def _absmax_codes(x32, axis):
@@ -546,19 +545,16 @@ def _absmax_codes(x32, axis):
     return codes, scale
 
 
-def sage_quantize(q, k, v, L: int, tile: int = 128, k_mean=None):
+def sage_quantize(q, k, v, L: int, tile: int = 128):
     """FP8 operands of SAGE attention. q, k, v [S, H, Dh] bf16 values.
-    k_mean: the per-(head, channel) mean of K to subtract (float32 values);
-    computed here (float64, rounded to float32) when not given.
-    Returns dict: qc [L,H,Dh], sq [nt,H], kc, sk [nt,H], vc, sv [H,Dh],
-    k_mean [H,Dh]."""
+    Returns dict: qc [L,H,Dh], sq [nt,H], kc, sk [nt,H], vc, sv [H,Dh] and
+    k_mean [H,Dh] (float32 values: the float64 mean of the valid keys, rounded
+    once to float32)."""
     q = np.asarray(q, np.float32)[:L]
     k = np.asarray(k, np.float32)[:L]
     v = np.asarray(v, np.float32)[:L]
     H, Dh = q.shape[1], q.shape[2]
-    if k_mean is None:
-        k_mean = np.asarray(k, np.float64).mean(axis=0)
-    k_mean = np.asarray(k_mean, np.float32).astype(np.float64)
+    k_mean = round_f32(np.asarray(k, np.float64).mean(axis=0))
     ks = (k - k_mean.astype(np.float32)[None]).astype(np.float32)
     nt = (L + tile - 1) // tile
     qc = np.empty((L, H, Dh)); kc = np.empty((L, H, Dh))
@@ -573,22 +569,55 @@ def sage_quantize(q, k, v, L: int, tile: int = 128, k_mean=None):
     return dict(qc=qc, sq=sq, kc=kc, sk=sk, vc=vc, sv=sv[0], k_mean=k_mean)
 
 
+def _sage_weights(ops, h, rows, L, scale, tile):
+    """Softmax weights p = 2^(z - max z) of head h for the given query rows
+    (exact row maximum), float64 [len(rows), L]."""
+    qc, kc = ops["qc"], ops["kc"]
+    sq = ops["sq"].astype(np.float64)
+    sk = ops["sk"].astype(np.float64)
+    key_tile = np.arange(L) // tile
+    s = (qc[rows, h, :] @ kc[:L, h, :].T) * sq[rows // tile, h][:, None] * sk[key_tile, h][None, :]
+    z = s * scale / np.log(2.0)
+    return np.exp2(z - z.max(axis=1, keepdims=True))
+
+
 def attention_sage(ops, L: int, scale: float, rows=None, tile: int = 128):
     """FP8 attention from sage_quantize's operands, for query rows `rows`."""
     if rows is None:
         rows = np.arange(L)
     rows = np.asarray(rows)
-    qc, kc, vc = ops["qc"], ops["kc"], ops["vc"]
-    sq = ops["sq"].astype(np.float64)
-    sk = ops["sk"].astype(np.float64)
+    vc = ops["vc"]
     sv = ops["sv"].astype(np.float64)
-    H, Dh = qc.shape[1], qc.shape[2]
-    key_tile = np.arange(L) // tile
+    H, Dh = vc.shape[1], vc.shape[2]
     out = np.empty((len(rows), H, Dh))
     for h in range(H):
-        s = (qc[rows, h, :] @ kc[:, h, :].T) * sq[rows // tile, h][:, None] * sk[key_tile, h][None, :]
-        z = s * scale / np.log(2.0)
-        p = 224.0 * np.exp2(z - np.ceil(z.max(axis=1, keepdims=True)))
-        pc = round_e4m3(p)
-        out[:, h, :] = (pc @ vc[:, h, :]) * sv[h][None, :] / p.sum(axis=1, keepdims=True)
+        p = _sage_weights(ops, h, rows, L, scale, tile)
+        pc = round_e4m3(_E4M3_MAX * p)
+        out[:, h, :] = (pc @ vc[:L, h, :]) * sv[h][None, :] / (_E4M3_MAX * p.sum(axis=1, keepdims=True))
     return round_bf16(out)
+
+
+def sage_error_terms(ops, L: int, scale: float, rows=None, tile: int = 128):
+    """Per-element sums that bound how far two correct FP8 evaluations of
+    attention_sage may differ when they quantise P at different scales
+    (their E4M3 roundings of the same weight then differ): with
+    w = V codes * sv (the dequantised V) and p the exact weights,
+      a1[i,h,d] = sum_k p_k |w_kd| / sum_k p_k
+      a0[i,h,d] = sum_k |w_kd| / sum_k p_k
+      v2[i,h,d] = sum_k p_k^2 w_kd^2 / (sum_k p_k)^2
+    Returns (a1, a0, v2), each [len(rows), H, Dh] float64."""
+    if rows is None:
+        rows = np.arange(L)
+    rows = np.asarray(rows)
+    vc = ops["vc"]
+    sv = ops["sv"].astype(np.float64)
+    H, Dh = vc.shape[1], vc.shape[2]
+    a1 = np.empty((len(rows), H, Dh)); a0 = np.empty_like(a1); v2 = np.empty_like(a1)
+    for h in range(H):
+        p = _sage_weights(ops, h, rows, L, scale, tile)
+        tot = p.sum(axis=1, keepdims=True)
+        w = np.abs(vc[:L, h, :] * sv[h][None, :])
+        a1[:, h, :] = (p @ w) / tot
+        a0[:, h, :] = w.sum(axis=0)[None, :] / tot
+        v2[:, h, :] = ((p * p) @ (w * w)) / (tot * tot)
+    return a1, a0, v2

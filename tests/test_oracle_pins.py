@@ -443,6 +443,7 @@ def test_stack_is_two_torch_blocks():
 def _mutant(**repl):
     m = types.ModuleType("oracle_mutant")
     m.__dict__.update({k: v for k, v in O.__dict__.items() if not k.startswith("__")})
+    m.__dict__["__builtins__"] = O.__dict__["__builtins__"]  # numpy's keyword calls need them
     for name, fn in repl.items():
         m.__dict__[name] = fn
     # functions look their helpers up in their own globals: rebind them
@@ -732,8 +733,9 @@ def check_sage(o):
     k = bf16_values(r.standard_normal((S, H, Dh)) + 3.0)  # a large common offset
     v = bf16_values(r.standard_normal((S, H, Dh)))
     ops = o.sage_quantize(q, k, v, L)
-    # smoothing removes the per-channel mean
-    assert np.allclose(ops["k_mean"], k.mean(0), rtol=1e-6, atol=1e-7)
+    # smoothing removes the per-channel mean of the valid keys, a float32 value
+    assert np.allclose(ops["k_mean"], k.mean(0), rtol=2 ** -23, atol=0)
+    assert np.array_equal(ops["k_mean"], ops["k_mean"].astype(np.float32).astype(np.float64))
     # dequantised operands are within half an E4M3 step of the originals
     for c, s, x, kind in ((ops["qc"], ops["sq"], q, "q"), (ops["kc"], ops["sk"],
                           k - ops["k_mean"][None], "k")):
@@ -741,31 +743,58 @@ def check_sage(o):
         assert np.all(np.abs(deq - x) <= np.abs(x) * 2.0 ** -4 + 2.0 ** -9 * np.max(np.abs(x)) + 1e-12), kind
     deq_v = ops["vc"] * ops["sv"][None].astype(np.float64)
     assert np.all(np.abs(deq_v - v) <= np.abs(v) * 2.0 ** -4 + 2.0 ** -9 * np.abs(v).max(0) + 1e-12)
+    # smoothing is exact in the score: subtracting a per-channel constant from
+    # every key moves each query row's scores by one constant, which softmax
+    # ignores
+    s_full = q[:, 0] @ k[:, 0].T
+    s_smooth = q[:, 0] @ (k[:, 0] - ops["k_mean"][0]).T
+    d = s_full - s_smooth
+    assert np.allclose(d, d[:, :1], atol=1e-9)
     # the FP8 result stays close to dense attention: per-element E4M3 noise on
     # P and V is about 2^-4 / sqrt(3) each, ~5 % of the output for random V
     scale = Dh ** -0.5
     dense = o.attention(q, k, v, L, scale)
     out = o.attention_sage(ops, L, scale)
     assert np.linalg.norm(out - dense) / np.linalg.norm(dense) < 0.1
-    # all scores 0 (q = 0): every p is exactly 1, an E4M3 value, so the output
-    # is the mean of the dequantised V rows
+    # all scores 0 (q = 0): every weight is exactly 1, whose code 448 is exact,
+    # so the output is the mean of the dequantised V rows
     opu = o.sage_quantize(np.zeros_like(q), k, v, L)
     deq_v = opu["vc"] * opu["sv"][None].astype(np.float64)
     assert np.allclose(o.attention_sage(opu, L, scale),
                        o.round_bf16(deq_v.mean(0))[None].repeat(L, 0), rtol=2 ** -8, atol=1e-12)
-    # one key far above the others: every other p underflows E4M3, so the
-    # output is that key's dequantised V row times one factor (its E4M3 code
-    # over its exact p) within half an E4M3 step of 1
+    # one key far above the others: its weight is 1 (code 448, exact), every
+    # other weight underflows, so the output is that key's dequantised V row
     kd = np.zeros_like(k)
     kd[7] = 8.0
     opd = o.sage_quantize(np.ones_like(q), kd, v, L)
     deq_vd = opd["vc"] * opd["sv"][None].astype(np.float64)
-    outd = o.attention_sage(opd, L, 1.0)
-    ratio = outd / deq_vd[7][None]
-    big = np.abs(deq_vd[7][None]) > 0.05
-    lam = np.median(ratio[np.broadcast_to(big, ratio.shape)])
-    assert abs(lam - 1) <= 2 ** -4
-    assert np.allclose(outd, lam * deq_vd[7][None], rtol=2 ** -7, atol=2 ** -7 * 0.05)
+    assert np.allclose(o.attention_sage(opd, L, 1.0),
+                       np.broadcast_to(o.round_bf16(deq_vd[7]), (L, H, Dh)), rtol=2 ** -8,
+                       atol=1e-12)
+    # hand-built operands (attention_sage takes any values): one query, scale
+    # ln 2 so that the base-2 logit is the plain dot product. Key 0 has logit
+    # 0.3 (the row maximum, not an integer); keys 1..7 sit log2(270/448)
+    # below it, so their weight is 270/448 and its code rounds 270 down to 256
+    # (E4M3 step 32 in [256, 512); 272 would be the tie). Key 0's V row is
+    # (1, 0) and the others' (0, 1):
+    #   out = (448 * (1, 0) + 7 * 256 * (0, 1)) / (448 * (1 + 7 * 270 / 448))
+    #       = (448, 1792) / 2338
+    n = 8
+    hand = dict(qc=np.ones((n, 1, 1)), sq=np.ones((1, 1), np.float32),
+                kc=np.full((n, 1, 1), 0.3 + math.log2(270 / 448)),
+                sk=np.ones((1, 1), np.float32),
+                vc=np.zeros((n, 1, 2)), sv=np.ones((1, 2), np.float32))
+    hand["kc"][0] = 0.3
+    hand["vc"][0, 0, 0] = 1.0
+    hand["vc"][1:, 0, 1] = 1.0
+    got = o.attention_sage(hand, n, math.log(2.0), rows=np.array([0]))
+    assert np.array_equal(got[0, 0], bf16_values([448 / 2338, 1792 / 2338])), got
+    # two keys a whole binade apart (logits 0.3 and -0.7): weights 1 and 1/2,
+    # codes 448 and 224, both exact: out = (w0 + w1 / 2) / (3 / 2)
+    two = dict(hand, kc=np.array([[[0.3]], [[-0.7]]]), vc=np.array([[[2.0, -1.0]], [[4.0, 8.0]]]),
+               sv=np.array([[0.25, 0.5]], np.float32))
+    got = o.attention_sage(two, 2, math.log(2.0), rows=np.array([0]))
+    assert np.array_equal(got[0, 0], bf16_values([(0.5 + 0.5) / 1.5, (-0.5 + 2.0) / 1.5])), got
 
 
 def test_sage():
@@ -779,6 +808,41 @@ def _sage_no_smoothing(q, k, v, L, tile=128):
     return ops2
 
 
-def test_planted_sage_mistake_is_caught():
+def _sage_p_unscaled(ops, L, scale, rows=None, tile=128):
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    vc, sv = ops["vc"], ops["sv"].astype(np.float64)
+    out = np.empty((len(rows),) + vc.shape[1:])
+    for h in range(vc.shape[1]):
+        p = O._sage_weights(ops, h, rows, L, scale, tile)
+        out[:, h, :] = (O.round_e4m3(p) @ vc[:L, h, :]) * sv[h][None, :] / p.sum(1, keepdims=True)
+    return O.round_bf16(out)
+
+
+def _sage_sum_of_codes(ops, L, scale, rows=None, tile=128):
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    vc, sv = ops["vc"], ops["sv"].astype(np.float64)
+    out = np.empty((len(rows),) + vc.shape[1:])
+    for h in range(vc.shape[1]):
+        pc = O.round_e4m3(448.0 * O._sage_weights(ops, h, rows, L, scale, tile))
+        out[:, h, :] = (pc @ vc[:L, h, :]) * sv[h][None, :] / pc.sum(1, keepdims=True)
+    return O.round_bf16(out)
+
+
+def _sage_weights_ceil_max(ops, h, rows, L, scale, tile):
+    # weights against the next integer above the row maximum, at half scale
+    # (224 * 2^(z - ceil max z) after the 448 of attention_sage)
+    qc, kc = ops["qc"], ops["kc"]
+    key_tile = np.arange(L) // tile
+    s = (qc[rows, h, :] @ kc[:L, h, :].T) * ops["sq"].astype(np.float64)[rows // tile, h][:, None] \
+        * ops["sk"].astype(np.float64)[key_tile, h][None, :]
+    z = s * scale / np.log(2.0)
+    return 0.5 * np.exp2(z - np.ceil(z.max(axis=1, keepdims=True)))
+
+
+@pytest.mark.parametrize("mut", [dict(sage_quantize=_sage_no_smoothing),
+                                 dict(attention_sage=_sage_p_unscaled),
+                                 dict(attention_sage=_sage_sum_of_codes),
+                                 dict(_sage_weights=_sage_weights_ceil_max)])
+def test_planted_sage_mistake_is_caught(mut):
     with pytest.raises(AssertionError):
-        check_sage(_mutant(sage_quantize=_sage_no_smoothing))
+        check_sage(_mutant(**mut))
