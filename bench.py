@@ -207,12 +207,7 @@ def oracle_sample(shape, n_kv=8192, n_q=96, seed=3):
     pos = I.positions_3d(shape.S, L).numpy()
     x_kv = bf(n_kv, D)
     x_q = bf(n_q, D)
-    key = (L, H, Dh)
-    if key not in _KV_CACHE:
-        gk = torch.Generator().manual_seed(12345)
-        kv = lambda: torch.randn(L, H, Dh, generator=gk).to(torch.bfloat16).double().numpy()
-        _KV_CACHE[key] = (kv(), kv())
-    k_all, v_all = _KV_CACHE[key]
+    k_all, v_all = _kv(shape)
 
     t0 = time.perf_counter()
     for c0 in range(0, n_kv, 2048):
@@ -241,7 +236,65 @@ def oracle_sample(shape, n_kv=8192, n_q=96, seed=3):
     ms = L * (t_kv / n_kv + t_q / n_q) * 1e3
     desc = (f"oracle (NumPy FP64) on the key/value stage of {n_kv} rows and the full query path "
             f"of {n_q} rows of the L={L} block, extrapolated linearly to all rows")
-    return ms, desc, t_kv + t_q
+    return ms, desc, t_kv + t_q, dict(kv_rows=n_kv, kv_ms=round(t_kv * 1e3, 1),
+                                       kv_all_rows_ms_extrapolated=round(t_kv / n_kv * L * 1e3, 1),
+                                       query_rows=n_q, query_ms=round(t_q * 1e3, 1),
+                                       query_all_rows_ms_extrapolated=round(t_q / n_q * L * 1e3, 1))
+
+
+def oracle_qk_rows(shape, n=512, seed=1):
+    """Oracle Q/K RMSNorm + RoPE on n seeded rows of the full-size workload
+    (all 42 heads, q and k); returns (ms for the n rows, ms extrapolated
+    linearly to all L rows)."""
+    import numpy as np
+    import torch
+
+    import oracle.h3_oracle as O
+    from dit_transformer_block_gb300 import inputs as I
+
+    L, H, Dh = shape.L, shape.H, shape.Dh
+    g = torch.Generator().manual_seed(seed)
+    rows = np.sort(np.random.default_rng(seed).choice(L, n, replace=False))
+    q = torch.randn(n, H, Dh, generator=g).to(torch.bfloat16).double().numpy()
+    k = torch.randn(n, H, Dh, generator=g).to(torch.bfloat16).double().numpy()
+    gain = 1 + 0.1 * torch.randn(Dh, generator=g).double().numpy()
+    pos = I.positions_3d(shape.S, L).numpy()[rows]
+    t0 = time.perf_counter()
+    for x in (q, k):
+        O.qk_norm_rope(x, gain, pos, shape.axis_dims, shape.theta, shape.eps_qk)
+    ms = (time.perf_counter() - t0) * 1e3
+    return ms, ms * L / n
+
+
+def oracle_attention_rows(shape, n=512, seed=2):
+    """Oracle attention for n seeded query rows over all L keys of the
+    full-size workload (42 heads); returns (ms for the n rows, ms extrapolated
+    linearly to all L rows). The keys and values are drawn once per process,
+    untimed (they are this configuration's inputs)."""
+    import numpy as np
+
+    import oracle.h3_oracle as O
+
+    L, H, Dh = shape.L, shape.H, shape.Dh
+    k_all, v_all = _kv(shape)
+    rows = np.sort(np.random.default_rng(seed).choice(L, n, replace=False))
+    q = np.zeros((L, H, Dh))
+    q[rows] = k_all[rows[::-1]]  # unit-RMS-like rows; their values do not change the cost
+    t0 = time.perf_counter()
+    O.attention(q, k_all, v_all, L, Dh ** -0.5, rows=rows)
+    ms = (time.perf_counter() - t0) * 1e3
+    return ms, ms * L / n
+
+
+def _kv(shape):
+    """Full-length bf16-valued keys and values, drawn once per process."""
+    import torch
+    key = (shape.L, shape.H, shape.Dh)
+    if key not in _KV_CACHE:
+        gk = torch.Generator().manual_seed(12345)
+        kv = lambda: torch.randn(*key, generator=gk).to(torch.bfloat16).double().numpy()
+        _KV_CACHE[key] = (kv(), kv())
+    return _KV_CACHE[key]
 
 
 def cpu_model():
@@ -304,6 +357,11 @@ def cpu_cores():
 def measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk):
     """Rows beyond the BF16 block, timed after the main measurement with CUDA
     events on the launching stream (3 warm-up launches each):
+      qk_norm_rope  Q/K RMSNorm + RoPE alone on its full-size workload, both
+                    channel pairings (GB/s against the copy bandwidth)
+      attention     attention alone on its full-size workload (unit-RMS q, k)
+      sage_quantize, attention_fp8   the FP8 (SAGE) operands and attention on
+                    the same inputs
       fp8_block     the block with online FP8 projections
       stack4        4 blocks in one h3_stack_forward call (fused boundaries)
       frames_to_u8  output preparation of the 10 s, 1344 x 768 clip"""
@@ -320,6 +378,39 @@ def measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk):
         return s.elapsed_time(e) / n
 
     out = {}
+    from dit_transformer_block_gb300 import inputs as I
+    S, L, H = shape.S, shape.L, shape.H
+    # Q/K RMSNorm + RoPE alone (q, k ~ N(0,1) [58816, 42, 128], 3-axis RoPE,
+    # seed 1): 8 bytes per (row, head, channel) read + written for q and k
+    qk = I.qk_inputs(S, L, H, 128, seed=1, device=inp["resid"].device)
+    pos = I.positions_3d(S, L).to(inp["resid"].device)
+    qk_bytes = L * H * 128 * 2 * 2 * 2
+    out["qk_norm_rope"] = {"workload": "q, k ~ N(0,1) bf16 [58816, 42, 128], 58,758 valid, "
+                           "3-axis RoPE 32/48/48, seed 1", "bytes": qk_bytes}
+    for name, pairing in (("interleaved", 0), ("split_half", 1)):
+        ms = timeit(lambda: h3.qk_norm_rope(qk["q"], qk["k"], qk["q_gain"], qk["k_gain"], pos,
+                                            shape.axis_dims, L=L, pairing=pairing), 20)
+        gbs = qk_bytes / ms / 1e6
+        out["qk_norm_rope"][name] = {"ms": round(ms, 4), "achieved_gbs": round(gbs, 1),
+                                     "frac_hbm": round(gbs / pk["hbm"], 3)}
+    del qk
+    # attention alone (q, k unit-RMS, v ~ N(0,1), [58816, 42, 128], seed 2)
+    at = I.attention_inputs(S, L, H, 128, seed=2, device=inp["resid"].device)
+    o_at = torch.empty_like(at["q"])
+    flop = 4.0 * L * L * H * 128
+    ms = timeit(lambda: h3.attention_varlen(at["q"], at["k"], at["v"], o_at, L), 3)
+    tf = flop / ms / 1e9
+    out["attention"] = {"workload": "q, k unit-RMS, v ~ N(0,1) bf16 [58816, 42, 128], 58,758 "
+                        "valid, seed 2", "ms": round(ms, 3), "tflops": round(tf, 1),
+                        "frac_bf16_sustained": round(tf / pk["bf16_sustained"], 3),
+                        "frac_bf16_burst": round(tf / pk["bf16"], 3)}
+    ops = h3.sage_quantize(at["q"], at["k"], at["v"], L)
+    ms = timeit(lambda: h3.sage_quantize(at["q"], at["k"], at["v"], L), 5)
+    out["sage_quantize"] = {"ms": round(ms, 3),
+                            "achieved_gbs": round(L * H * 128 * 9 / ms / 1e6, 1)}
+    ms = timeit(lambda: h3.attention_fp8(ops, o_at, L), 3)
+    out["attention_fp8"] = {"ms": round(ms, 3), "tflops_dense_equivalent": round(flop / ms / 1e9, 1)}
+    del at, o_at, ops
     r = inp["resid"].clone()
     w8 = h3.quantize_block_weights_fp8(inp)
     ws8 = torch.empty(h3.block_workspace_bytes_fp8(cfg), dtype=torch.uint8, device=r.device)
@@ -338,7 +429,6 @@ def measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk):
     # buffers padded to a multiple of 64: ms per block and TFLOP/s vs length
     del ws
     sweep = []
-    from dit_transformer_block_gb300 import inputs as I
     for L_s, grid in ((29034, (16, 24, 79)), (58758, (31, 24, 79)), (87846, (47, 24, 79))):
         S_s = (L_s + 63) // 64 * 64
         sh = I.BlockShape(S=S_s, L=L_s, D=shape.D, H=shape.H, Dh=shape.Dh, F=shape.F,
@@ -374,7 +464,7 @@ def run_reference(a):
     times = []
     desc = ""
     for i in range(a.warmup + a.steps):
-        ms, desc, _ = oracle_sample(shape, n_kv=2048, n_q=24, seed=100 + i)
+        ms, desc, _, _ = oracle_sample(shape, n_kv=2048, n_q=24, seed=100 + i)
         if i >= a.warmup:
             times.append(ms)
     value = statistics.mean(times)
@@ -508,27 +598,46 @@ def run_ours(a):
     up_s, down_s = torch.cuda.Stream(), torch.cuda.Stream()
     comp_s = torch.cuda.Stream()  # not the legacy default stream, which would serialise the copies
 
-    def e2e_run(n):
-        up = [torch.cuda.Event() for _ in range(n)]
-        done = [torch.cuda.Event() for _ in range(n)]
-        down = [torch.cuda.Event() for _ in range(n)]
+    def e2e_run(n, timeline=False):
+        ev = lambda: torch.cuda.Event(enable_timing=timeline)
+        up0 = [ev() for _ in range(n)]
+        up = [ev() for _ in range(n)]
+        c0 = [ev() for _ in range(n)]
+        done = [ev() for _ in range(n)]
+        dn0 = [ev() for _ in range(n)]
+        down = [ev() for _ in range(n)]
         for k in range(n):
             b = k % 2
             with torch.cuda.stream(up_s):
                 if k >= 2:
                     up_s.wait_event(down[k - 2])  # buffer b is free again
+                up0[k].record(up_s)
                 for d, h in zip(d_buf[b], h_in[b]):
                     d.copy_(h, non_blocking=True)
                 up[k].record(up_s)
             comp_s.wait_event(up[k])
+            c0[k].record(comp_s)
             h3.block_forward(cfg, weights, d_buf[b][0], d_buf[b][1], d_buf[b][2], ws,
                              stream=comp_s)
             done[k].record(comp_s)
             with torch.cuda.stream(down_s):
                 down_s.wait_event(done[k])
+                dn0[k].record(down_s)
                 h_out[b].copy_(d_buf[b][0], non_blocking=True)
                 down[k].record(down_s)
         torch.cuda.synchronize()
+        if not timeline:
+            return None
+        mean = lambda xs: round(statistics.mean(xs), 3) if xs else None
+        return {
+            "upload_ms": mean([up0[k].elapsed_time(up[k]) for k in range(n)]),
+            "compute_ms": mean([c0[k].elapsed_time(done[k]) for k in range(n)]),
+            "download_ms": mean([dn0[k].elapsed_time(down[k]) for k in range(n)]),
+            # idle time of the compute stream between consecutive blocks
+            "compute_gap_ms": mean([done[k - 1].elapsed_time(c0[k]) for k in range(1, n)]),
+            # first upload start to last download end, on the device
+            "span_ms": round(up0[0].elapsed_time(down[n - 1]), 3),
+        }
 
     e2e_run(2)
     barrier()
@@ -537,6 +646,7 @@ def run_ours(a):
     e2e_ms = (time.perf_counter() - t0) * 1e3 / a.e2e_steps
     barrier()
     e2e_ms = max_over_ranks([e2e_ms], device=dev)[0]
+    e2e_timeline = e2e_run(a.e2e_steps, timeline=True)
     h3.check_device_error()
 
     if rank != 0:
@@ -562,9 +672,17 @@ def run_ours(a):
     extras = None if a.no_extras else measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk)
     cpu = None
     if not a.no_cpu_baseline and world == 1:
-        ms, desc, secs = oracle_sample(shape)
+        ms, desc, secs, parts = oracle_sample(shape, n_kv=4096, n_q=512)
+        qk_ms, qk_all = oracle_qk_rows(shape)
+        at_ms, at_all = oracle_attention_rows(shape)
         cpu = {"value": round(ms, 1), "unit": "ms", "cores": cpu_cores(), "kind": "oracle",
                "sample": desc + f" ({secs:.1f} s of CPU work)", "cpu_model": cpu_model(),
+               "per_config": {
+                   "qk_norm_rope": {"rows": 512, "ms": round(qk_ms, 1),
+                                    "all_rows_ms_extrapolated": round(qk_all, 1)},
+                   "attention": {"rows": 512, "ms": round(at_ms, 1),
+                                 "all_rows_ms_extrapolated": round(at_all, 1)},
+                   "block": parts},
                "tiny_block_ms": {"all_threads": oracle_tiny_ms(),
                                  "one_thread": oracle_tiny_ms(1),
                                  "workload": "whole oracle block, 256-row configuration "
@@ -600,6 +718,7 @@ def run_ours(a):
         "e2e_note": (f"{a.e2e_steps} steps timed from the first upload to the last download "
                      "(pipeline fill and drain included); uploads and downloads on their own "
                      "streams, two buffer sets: copies overlap compute"),
+        "e2e_timeline": e2e_timeline,
         "clocks": clocks.summary(),
         "extras": extras,
     }

@@ -320,7 +320,7 @@ h3_status h3_attention_varlen(const void* q, const void* k, const void* v, void*
 
 h3_status h3_attention_varlen_skip(const void* q, const void* k, const void* v, void* o, int S,
                                    int L, int H, int Dh, float softmax_scale, float skip_eps,
-                                   h3_stream_t stream) {
+                                   int32_t* kept_tiles, h3_stream_t stream) {
   clear_error();
   H3_REQUIRE(skip_eps >= 0.f && skip_eps < 1.f, H3_ERR_INVALID_ARG,
              "skip_eps=%g must be in [0, 1)", static_cast<double>(skip_eps));
@@ -335,7 +335,7 @@ h3_status h3_attention_varlen_skip(const void* q, const void* k, const void* v, 
   if (L == 0) return H3_OK;
   const int64_t ld = static_cast<int64_t>(H) * Dh;
   return launch_attention(q, k, v, ld, o, ld, L, H, softmax_scale,
-                          reinterpret_cast<cudaStream_t>(stream), skip_eps);
+                          reinterpret_cast<cudaStream_t>(stream), skip_eps, kept_tiles);
 }
 
 size_t h3_sage_scratch_bytes(int L, int H) {

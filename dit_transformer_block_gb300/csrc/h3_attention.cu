@@ -50,7 +50,9 @@ struct AttnArgs {
   int L;
   int num_kv;
   float scale_log2;  // softmax_scale * log2(e)
-  float skip_log2;   // Skip-Softmax: skip a key tile when every row's tile max < m - skip_log2
+  float skip_log2;   // Skip-Softmax: skip a key tile when every valid row's tile max is below
+                     // its exact running maximum over the kept tiles minus skip_log2
+  int* kept;         // Skip-Softmax (optional): kept key tiles per (query tile, head)
   // FP8 operands: score multiplier of (query tile t, key tile j, head h) is
   // sq[t * H + h] * sk[j * H + h]; output column d of head h is scaled by
   // sv[h * 128 + d].
@@ -66,10 +68,12 @@ struct AttnArgs {
 // columns. valid = keys of this tile that are < L (>= BKV: none masked).
 // o_live: O already holds earlier tiles (so raising the max rescales it).
 // m, l: running max (times scale_log2) and row sum. Warp-collective.
-// Skip-Softmax (skip != 0): the four warps of a query tile vote; when every
-// row's tile maximum lies more than skip_log2 below its running maximum the
-// tile is skipped (no exp2, no P; flags[quarter] tells the MMA warp to leave
-// out its P V product) and the function returns true. The vote is exchanged
+// Skip-Softmax (SKIP): the four warps of a query tile vote; when every valid
+// row's tile maximum lies more than skip_log2 below m_keep, the row's exact
+// running maximum over the key tiles kept so far (rows >= L, row_valid
+// false, vote to skip), the tile is skipped (no exp2, no P; flags[quarter]
+// tells the MMA warp to leave out its P V product) and the function returns
+// true; otherwise m_keep takes in the tile's maximum. The vote is exchanged
 // through flags and the mbarrier vote_bar (one arrival per warp, phase
 // vote_parity), waited on with the usual limit; if that wait runs out, ok is
 // cleared and the function returns at once.
@@ -79,9 +83,9 @@ struct AttnArgs {
 template <bool F8, bool SKIP>
 __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid, bool o_live,
                                              float scale_log2, float& m, float& l,
-                                             float skip_log2, volatile uint32_t* flags,
-                                             uint32_t vote_bar, uint32_t vote_parity,
-                                             const DevErr& err, bool& ok) {
+                                             float skip_log2, float& m_keep, bool row_valid,
+                                             volatile uint32_t* flags, uint32_t vote_bar,
+                                             uint32_t vote_parity, const DevErr& err, bool& ok) {
   uint32_t sr[128];
   {
     uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
@@ -161,7 +165,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
   }
   const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
   if constexpr (SKIP) {
-    const bool row_skip = mx < m - skip_log2;  // never on the first tile (m = -inf)
+    // never on the first tile for a valid row (m_keep = -inf)
+    const bool row_skip = !row_valid || mx < m_keep - skip_log2;
     const uint32_t warp_skip = __all_sync(0xffffffffu, row_skip) ? 1u : 0u;
     const int quarter = (threadIdx.x >> 5) & 3;
     if ((threadIdx.x & 31) == 0) flags[quarter] = warp_skip;
@@ -172,6 +177,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
       return true;
     }
     if (flags[0] & flags[1] & flags[2] & flags[3]) return true;
+    m_keep = fmaxf(m_keep, mx);
   }
   // Raise the running max only when it is exceeded by more than the
   // threshold; the decision is warp-uniform because the O rescale uses
@@ -418,11 +424,13 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         }
         mma_commit(bar(B2_S + i));
       };
+      int kept[2] = {0, 0};  // Skip-Softmax: key tiles kept per query tile
       auto pv = [&](int i, int j) {  // O_i += P_i V_j (left out when the tile was skipped)
         const uint32_t v_addr = kv_addr + slot_of(2 * j + 1) * T_BYTES;
         volatile uint32_t* f = skip_flags + (i * 2 + (j & 1)) * 4;
         const bool skipped = SKIP && (f[0] & f[1] & f[2] & f[3]);
         if (!skipped) {
+          ++kept[i];
           if constexpr (F8) {
             // 32 keys per step: 32 rows of 128 bytes = 4 KB further; P codes
             // take 8 TMEM columns per step
@@ -468,6 +476,12 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
           mma_commit(bar(B2_KV_EMPTY + slot_of(2 * j + 2)));
         }
       }
+      if (SKIP && a.kept != nullptr && ok) {
+        for (int i = 0; i < 2; ++i) {
+          const int qt = blockIdx.x * 2 + i;
+          if (qt * BQ < a.L) a.kept[qt * a.H + blockIdx.y] = kept[i];
+        }
+      }
       // Every MMA issued here must be done with shared and tensor memory
       // before the CTA frees them (after an error no consumer may have waited
       // for the last ones): commit and wait, bounded.
@@ -482,7 +496,9 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
     const uint32_t tS = tmem + lane_base + tile * 128;
     const uint32_t tO = tmem + lane_base + 256 + tile * 128;
     float m = -INFINITY, l = 0.f;
+    float m_keep = -INFINITY;  // Skip-Softmax: exact running max of the kept tiles
     bool ok = true;
+    const bool row_valid = q0 + tile * BQ + quarter * 32 + lane < a.L;
     float sq_tile = 1.f;
     if constexpr (F8) {
       const int qt = blockIdx.x * 2 + tile;  // 128-row query tile index
@@ -499,9 +515,9 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       // a zero tile scale would turn masked (-inf) scores into NaN: keep the
       // multiplier positive
       if constexpr (F8) mul = fmaxf(mul * sq_tile * __ldg(a.sk + j * a.H + blockIdx.y), 1e-30f);
-      softmax_tile<F8, SKIP>(tS, tO, a.L - j * BKV, j > 0, mul, m, l, a.skip_log2,
-                             skip_flags + (tile * 2 + (j & 1)) * 4, bar(B2_VOTE + tile),
-                             static_cast<uint32_t>(j) & 1u, a.err, ok);
+      softmax_tile<F8, SKIP>(tS, tO, a.L - j * BKV, j > 0, mul, m, l, a.skip_log2, m_keep,
+                             row_valid, skip_flags + (tile * 2 + (j & 1)) * 4,
+                             bar(B2_VOTE + tile), static_cast<uint32_t>(j) & 1u, a.err, ok);
       if (!ok) break;
       tc_fence_before();
       mbar_arrive(bar(B2_P + tile));
@@ -535,7 +551,7 @@ static h3_status set_attention_smem() {
 
 h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
                            void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
-                           float skip_eps) {
+                           float skip_eps, int* kept) {
   const bool skip = skip_eps > 0.f;
   h3_status st = skip ? set_attention_smem<false, true>() : set_attention_smem<false, false>();
   if (st != H3_OK) return st;
@@ -547,6 +563,7 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   a.num_kv = (L + BKV - 1) / BKV;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.skip_log2 = skip ? -log2f(skip_eps) : 0.f;
+  a.kept = skip ? kept : nullptr;
   if ((st = dev_err(&a.err)) != H3_OK) return st;
   CUtensorMap tq, tk, tv;
   const uint64_t width = static_cast<uint64_t>(H) * DH;

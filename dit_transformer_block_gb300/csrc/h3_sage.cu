@@ -2,8 +2,11 @@
 // P and V quantised to FP8 for the QK and PV products).
 //
 //   1. kv_stats_partial / kv_stats_final: per (head, channel) mean of K and
-//      absmax of V over the L valid rows, in two deterministic passes (chunk
-//      partials with compensated sums, then an in-order combine);
+//      absmax of V over the L valid rows: chunk partial sums in FP64, then an
+//      FP64 combine, a division by L in FP64 and one rounding to float32. A
+//      sum of at most 2^17 bf16 values is exact in FP64 unless a channel holds
+//      a nonzero |k| < 2^-27, so the mean is the exact mean rounded once,
+//      whatever the order of the additions;
 //   2. qk_tile_quant: Q, and K minus its mean, to E4M3 per (128-row tile,
 //      head) block with absmax scaling;
 //   3. v_quant: V to E4M3 per (head, channel) with the V absmax.
@@ -23,47 +26,58 @@ namespace {
 constexpr int DH = 128;
 constexpr int ST_ROWS = 512;  // rows per statistics chunk
 
-// Compensated (two-float) accumulation: s + c carries the running sum.
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
-  const float y = __fsub_rn(x, c);
-  const float t = __fadd_rn(s, y);
-  c = __fsub_rn(__fsub_rn(t, s), y);
-  s = t;
-}
-
 // grid (chunks, H), 128 threads: thread d owns channel d of head blockIdx.y.
+// Four independent FP64 partial sums per thread (the additions are exact, so
+// their grouping does not change the result).
 __global__ void __launch_bounds__(DH)
     kv_stats_partial_kernel(const __nv_bfloat16* __restrict__ k,
                             const __nv_bfloat16* __restrict__ v, int64_t ld, int L,
-                            float* __restrict__ psum, float* __restrict__ pmax) {
+                            double* __restrict__ psum, float* __restrict__ pmax) {
   const int chunk = blockIdx.x, h = blockIdx.y, d = threadIdx.x, H = gridDim.y;
   const int r0 = chunk * ST_ROWS, r1 = min(L, r0 + ST_ROWS);
   const int64_t col = static_cast<int64_t>(h) * DH + d;
-  float s = 0.f, c = 0.f, mx = 0.f;
-  for (int r = r0; r < r1; ++r) {
+  double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
+  float mx = 0.f;
+  int r = r0;
+  for (; r + 4 <= r1; r += 4) {
     const int64_t off = static_cast<int64_t>(r) * ld + col;
-    kahan_add(s, c, __bfloat162float(k[off]));
+    const float k0 = __bfloat162float(k[off]), k1 = __bfloat162float(k[off + ld]);
+    const float k2 = __bfloat162float(k[off + 2 * ld]), k3 = __bfloat162float(k[off + 3 * ld]);
+    const float v0 = fabsf(__bfloat162float(v[off])), v1 = fabsf(__bfloat162float(v[off + ld]));
+    const float v2 = fabsf(__bfloat162float(v[off + 2 * ld]));
+    const float v3 = fabsf(__bfloat162float(v[off + 3 * ld]));
+    s0 = __dadd_rn(s0, static_cast<double>(k0));
+    s1 = __dadd_rn(s1, static_cast<double>(k1));
+    s2 = __dadd_rn(s2, static_cast<double>(k2));
+    s3 = __dadd_rn(s3, static_cast<double>(k3));
+    mx = fmaxf(mx, max3f(v0, v1, fmaxf(v2, v3)));
+  }
+  for (; r < r1; ++r) {
+    const int64_t off = static_cast<int64_t>(r) * ld + col;
+    s0 = __dadd_rn(s0, static_cast<double>(__bfloat162float(k[off])));
     mx = fmaxf(mx, fabsf(__bfloat162float(v[off])));
   }
   const int64_t o = (static_cast<int64_t>(chunk) * H + h) * DH + d;
-  psum[o] = __fadd_rn(s, -c);
+  psum[o] = __dadd_rn(__dadd_rn(s0, s1), __dadd_rn(s2, s3));
   pmax[o] = mx;
 }
 
-// grid H, 128 threads: combine the chunks in order.
+// grid H, 128 threads: combine the chunks (FP64), mean = sum / L in FP64,
+// rounded once to float32.
 __global__ void __launch_bounds__(DH)
-    kv_stats_final_kernel(const float* __restrict__ psum, const float* __restrict__ pmax,
+    kv_stats_final_kernel(const double* __restrict__ psum, const float* __restrict__ pmax,
                           int chunks, int L, float* __restrict__ k_mean, float* __restrict__ sv,
                           float* __restrict__ inv_v) {
   const int h = blockIdx.x, d = threadIdx.x, H = gridDim.x;
-  float s = 0.f, c = 0.f, mx = 0.f;
+  double s = 0.0;
+  float mx = 0.f;
   for (int ch = 0; ch < chunks; ++ch) {
     const int64_t o = (static_cast<int64_t>(ch) * H + h) * DH + d;
-    kahan_add(s, c, psum[o]);
+    s = __dadd_rn(s, psum[o]);
     mx = fmaxf(mx, pmax[o]);
   }
   const int i = h * DH + d;
-  k_mean[i] = __fdiv_rn(__fadd_rn(s, -c), static_cast<float>(L));
+  k_mean[i] = __double2float_rn(__ddiv_rn(s, static_cast<double>(L)));
   sv[i] = __fdiv_rn(mx, 448.0f);
   inv_v[i] = mx > 0.f ? __fdiv_rn(448.0f, mx) : 0.f;
 }
@@ -160,7 +174,8 @@ __global__ void __launch_bounds__(256)
 
 size_t sage_scratch_bytes(int L, int H) {
   const size_t chunks = (static_cast<size_t>(L) + ST_ROWS - 1) / ST_ROWS;
-  return 2 * chunks * H * DH * sizeof(float) + static_cast<size_t>(H) * DH * sizeof(float);
+  return chunks * H * DH * (sizeof(double) + sizeof(float)) +
+         static_cast<size_t>(H) * DH * sizeof(float);
 }
 
 h3_status launch_sage_quantize(const void* q, const void* k, const void* v, int64_t ld, int L,
@@ -168,8 +183,8 @@ h3_status launch_sage_quantize(const void* q, const void* k, const void* v, int6
                                float* sq, float* sk, float* sv, float* k_mean, void* scratch,
                                cudaStream_t s) {
   const int chunks = (L + ST_ROWS - 1) / ST_ROWS;
-  float* psum = static_cast<float*>(scratch);
-  float* pmax = psum + static_cast<size_t>(chunks) * H * DH;
+  double* psum = static_cast<double*>(scratch);
+  float* pmax = reinterpret_cast<float*>(psum + static_cast<size_t>(chunks) * H * DH);
   float* inv_v = pmax + static_cast<size_t>(chunks) * H * DH;
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   const auto* kk = static_cast<const __nv_bfloat16*>(k);

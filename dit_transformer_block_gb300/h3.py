@@ -66,7 +66,7 @@ _SIGS = {
     "h3_sage_quantize": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                               _P]),
     "h3_attention_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
-    "h3_attention_varlen_skip": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P]),
+    "h3_attention_varlen_skip": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P]),
     "h3_linear": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_linear_swiglu": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_rope_table": (_I, [_P, _P, _I, _I, _F, _P, _P]),
@@ -224,15 +224,21 @@ def attention_varlen(q, k, v, o, L=None, scale=None, stream=None):
         _p(q), _p(k), _p(v), _p(o), S, L, H, Dh, scale, _s(stream)))
 
 
-def attention_varlen_skip(q, k, v, o, L=None, scale=None, skip_eps=0.0, stream=None):
-    """attention_varlen with Skip-Softmax tile skipping (skip_eps = 0: dense)."""
+def attention_varlen_skip(q, k, v, o, L=None, scale=None, skip_eps=0.0, kept=None, stream=None):
+    """attention_varlen with Skip-Softmax tile skipping (skip_eps = 0: dense).
+    kept (optional): int32 [ceil(L/128), H], receives the key tiles kept per
+    (query tile, head)."""
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
         _need(t, torch.bfloat16, n)
     S, H, Dh = q.shape
     L = S if L is None else L
     scale = Dh ** -0.5 if scale is None else scale
+    if kept is not None:
+        _need(kept, torch.int32, "kept")
+        if tuple(kept.shape) != ((L + 127) // 128, H):
+            raise ValueError(f"kept must be [{(L + 127) // 128}, {H}]")
     _check("attention_varlen_skip", lib().h3_attention_varlen_skip(
-        _p(q), _p(k), _p(v), _p(o), S, L, H, Dh, scale, skip_eps, _s(stream)))
+        _p(q), _p(k), _p(v), _p(o), S, L, H, Dh, scale, skip_eps, _p(kept), _s(stream)))
 
 
 def sage_quantize(q, k, v, L=None, stream=None) -> dict:

@@ -137,42 +137,51 @@ h3_status h3_attention_varlen(const void* q, const void* k, const void* v, void*
                               int L, int H, int Dh, float softmax_scale, h3_stream_t stream);
 
 /*
- * a3 with Skip-Softmax (next step after dense attention; blog section 4.3:
- * skip the softmax and P x V of tiles the QK scores show to be negligible,
- * decided per tile). Keys are taken in tiles of 128 from key 0 and queries in
- * tiles of 128 from row 0. A key tile is left out for a query tile when, for
- * every row of that query tile, the tile's largest score is below
- * skip_eps times the row's running maximum weight (base-2 exponent more than
- * log2(1/skip_eps) below the running maximum over the tiles kept so far; the
- * running maximum may lag the exact one by up to 2^8, which only makes the
- * test more conservative). skip_eps == 0 is exactly h3_attention_varlen.
- * The first key tile is never skipped. Arguments as h3_attention_varlen;
- * 0 <= skip_eps < 1.
+ * a3 with Skip-Softmax (next step after dense attention; blog section 4.3,
+ * Fig. 6: skip the softmax and P x V of tiles the QK scores show to be
+ * negligible, decided per tile). Keys are taken in tiles of 128 from key 0 and
+ * queries in tiles of 128 from row 0. A key tile is left out for a query tile
+ * when, for every valid row of that query tile, the tile's largest base-2
+ * logit (score * softmax_scale * log2(e)) lies more than log2(1/skip_eps)
+ * below the row's exact running maximum over the key tiles kept so far (rows
+ * >= L of a ragged last query tile take no part). The first key tile is never
+ * skipped; skip_eps == 0 is exactly h3_attention_varlen.
+ *   kept_tiles  [ceil(L/128), H] int32 device, or NULL: receives the number of
+ *               key tiles kept for every (query tile, head), the first one
+ *               included (only with skip_eps > 0; left untouched otherwise)
+ * Other arguments as h3_attention_varlen; 0 <= skip_eps < 1; kept_tiles
+ * 4-byte aligned.
  */
 h3_status h3_attention_varlen_skip(const void* q, const void* k, const void* v, void* o, int S,
                                    int L, int H, int Dh, float softmax_scale, float skip_eps,
-                                   h3_stream_t stream);
+                                   int32_t* kept_tiles, h3_stream_t stream);
 
 /*
  * a3 with FP8 ("SAGE") products (next step; blog section 4.3: Q, K, P and V
  * quantised to FP8 for the QK and PV products). Two steps:
  *
  * h3_sage_quantize: K is smoothed by subtracting its per-(head, channel)
- * mean over the L valid keys (float32; softmax is unchanged), Q and the
- * smoothed K are quantised to E4M3 per (128-row tile, head) block and V per
- * (head, channel), all with absmax scaling (inv = 448 / amax, code =
- * E4M3_satfinite(x * inv), scale = amax / 448, float32 steps).
+ * mean over the L valid keys (summed in FP64, divided by L in FP64 and
+ * rounded once to float32: the exact mean rounded once for any bf16 input
+ * without nonzero values below 2^-27 in magnitude), Q and the smoothed K are
+ * quantised to E4M3 per (128-row tile, head) block and V per (head, channel),
+ * all with absmax scaling (inv = 448 / amax, code = E4M3_satfinite(x * inv),
+ * scale = amax / 448, float32 steps).
  *   q, k, v   [S, H, Dh] bf16 (row stride H*Dh)
  *   qc, kc, vc [S, H, Dh] E4M3 codes (bytes); rows >= L are not written
  *   sq, sk    [ceil(L/128), H] float32; sv, k_mean [H, Dh] float32
- *   scratch   device memory of h3_sage_scratch_bytes(L, H) bytes
+ *   scratch   device memory of h3_sage_scratch_bytes(L, H) bytes, 16-byte
+ *             aligned
  *
- * h3_attention_fp8: o[i] = sum_j E4M3(p_ij) * vc[j] * sv / sum_j p_ij with
- * p_ij = 224 * 2^(z_ij - m_i), z_ij = (qc_i . kc_j) * sq * sk * softmax_scale
- * * log2(e), m_i an integer running maximum kept within 1 of the exact one
- * (so P is an exact power-of-two multiple of the P against the exact maximum
- * and 224 * P <= 448); tcgen05 kind::f8f6f4 for QK and PV, FP32 softmax and
- * accumulation, bf16 out. Dh == 128.
+ * h3_attention_fp8: o[i] = sum_j E4M3(P_ij) * vc[j] * sv / sum_j P_ij with
+ * P_ij = 224 * 2^(z_ij - m_i), z_ij = (qc_i . kc_j) * sq * sk * softmax_scale
+ * * log2(e), m_i an integer running maximum kept in [max_j z_ij - 1,
+ * ceil(max_j z_ij)] (the kernel sees the keys once, so it cannot scale P by
+ * the exact row maximum). P_ij is therefore 448 * p_ij (p_ij = 2^(z_ij -
+ * max_j z_ij), P scaled by its row absmax) times a per-row factor in
+ * (1/4, 1], and its E4M3 rounding differs from that of 448 * p_ij by at most
+ * half an E4M3 step on each side. tcgen05 kind::f8f6f4 for QK and PV, FP32
+ * softmax and accumulation, bf16 out. Dh == 128.
  */
 size_t h3_sage_scratch_bytes(int L, int H);
 h3_status h3_sage_quantize(const void* q, const void* k, const void* v, int S, int L, int H,

@@ -605,14 +605,16 @@ def sage_error_terms(ops, L: int, scale: float, rows=None, tile: int = 128):
       a1[i,h,d] = sum_k p_k |w_kd| / sum_k p_k
       a0[i,h,d] = sum_k |w_kd| / sum_k p_k
       v2[i,h,d] = sum_k p_k^2 w_kd^2 / (sum_k p_k)^2
-    Returns (a1, a0, v2), each [len(rows), H, Dh] float64."""
+      u2[i,h,d] = sum_k w_kd^2 / (sum_k p_k)^2
+    Returns (a1, a0, v2, u2), each [len(rows), H, Dh] float64."""
     if rows is None:
         rows = np.arange(L)
     rows = np.asarray(rows)
     vc = ops["vc"]
     sv = ops["sv"].astype(np.float64)
     H, Dh = vc.shape[1], vc.shape[2]
-    a1 = np.empty((len(rows), H, Dh)); a0 = np.empty_like(a1); v2 = np.empty_like(a1)
+    a1 = np.empty((len(rows), H, Dh)); a0 = np.empty_like(a1)
+    v2 = np.empty_like(a1); u2 = np.empty_like(a1)
     for h in range(H):
         p = _sage_weights(ops, h, rows, L, scale, tile)
         tot = p.sum(axis=1, keepdims=True)
@@ -620,4 +622,5 @@ def sage_error_terms(ops, L: int, scale: float, rows=None, tile: int = 128):
         a1[:, h, :] = (p @ w) / tot
         a0[:, h, :] = w.sum(axis=0)[None, :] / tot
         v2[:, h, :] = ((p * p) @ (w * w)) / (tot * tot)
-    return a1, a0, v2
+        u2[:, h, :] = (w * w).sum(axis=0)[None, :] / (tot * tot)
+    return a1, a0, v2, u2

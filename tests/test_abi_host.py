@@ -42,12 +42,13 @@ def st(lib, fn, *args):
 def test_attention_argument_errors(lib):
     f = "h3_attention_varlen"
     assert st(lib, f, P, P, P, P, 10, 11, 2, 128, 0.1, NULL) == 1     # L > S
+    assert "L=11" in h3.last_error(), h3.last_error()
     assert st(lib, f, P, P, P, P, 10, -1, 2, 128, 0.1, NULL) == 1     # L < 0
     assert st(lib, f, NULL, P, P, P, 10, 5, 2, 128, 0.1, NULL) == 1   # null q
     assert st(lib, f, P, P, P, P, 10, 5, 2, 64, 0.1, NULL) == 2       # head_dim
     assert st(lib, f, P, PM, P, P, 10, 5, 2, 128, 0.1, NULL) == 3     # misaligned
     assert st(lib, f, P, P, P, P, 10, 0, 2, 128, 0.1, NULL) == 0      # empty: no-op
-    assert "L=11" in h3.last_error() or True
+    assert h3.last_error() == ""
 
 
 def test_elementwise_argument_errors(lib):
@@ -204,3 +205,13 @@ def test_binding_argument_counts_match_the_header():
     assert set(protos) == set(h3._SIGS)
     for name, (_, argtypes) in h3._SIGS.items():
         assert len(argtypes) == protos[name], (name, len(argtypes), protos[name])
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    # the binding's NOALLOC_SCRATCH_BYTES is the header's H3_NOALLOC_SCRATCH_BYTES
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    hdr = open(os.path.join(root, "include", "h3block.h")).read()
+    m = re.search(r"#define H3_NOALLOC_SCRATCH_BYTES \((\d+)u \* (\d+)u \* (\d+)u\)", hdr)
+    assert m, "H3_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert h3.NOALLOC_SCRATCH_BYTES == int(m.group(1)) * int(m.group(2)) * int(m.group(3))

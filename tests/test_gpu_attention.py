@@ -122,6 +122,10 @@ def test_skip_softmax_skips_the_tile_the_rule_names(h3lib):
     ref, kept = O.attention_skip(np64(q), np64(k), np64(v), L, scale, 0.5)
     assert kept[:, 0].tolist() == [[True, False, True]] * 3
     assert_close_bf16(np64(o_skip[:L]), ref, "skip-softmax")
+    kept_gpu = torch.full((3, H), -1, dtype=torch.int32, device=dev)
+    h3lib.attention_varlen_skip(q, k, v, o_skip, L, scale=scale, skip_eps=0.5, kept=kept_gpu)
+    h3lib.check_device_error()
+    assert kept_gpu.cpu().tolist() == [[2]] * 3
     o_dense = torch.full_like(q, SENT)
     h3lib.attention_varlen(q, k, v, o_dense, L, scale=scale)
     h3lib.check_device_error()
@@ -136,3 +140,38 @@ def test_skip_softmax_random_data_matches_dense_within_eps(h3lib):
     h3lib.check_device_error()
     ref = O.attention(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), L, 128 ** -0.5)
     assert_close_bf16(np64(o[:L]), ref, "skip-softmax random")
+
+
+@pytest.mark.parametrize("S,L,eps_log2", [(2048, 2000, 4), (1024, 1024, 2), (1408, 1300, 6)])
+def test_skip_softmax_random_data_matches_oracle_rule(h3lib, S, L, eps_log2):
+    """Random keys and queries with a shared direction whose per-key-tile
+    weight varies, so that whole tiles fall far below the running maximum and
+    many tiles are really skipped: the kept-tile counts equal the oracle's (the
+    kernel applies the exact running maximum of the kept tiles, as the oracle
+    does), the output matches attention over the kept tiles element by
+    element, and it differs from dense attention. The ragged last query tile's
+    pad rows take no part in the vote."""
+    H = 2
+    g = torch.Generator().manual_seed(S + eps_log2)
+    q = torch.randn(S, H, 128, generator=g)
+    k = torch.randn(S, H, 128, generator=g)
+    v = torch.randn(S, H, 128, generator=g)
+    q[:, :, 0] += 8.0
+    nk = (S + 127) // 128
+    b = torch.randn(nk, H, generator=g) * 8.0
+    k[:, :, 0] += b.repeat_interleave(128, dim=0)[:S]
+    q, k, v = (t.to(torch.bfloat16).to(dev) for t in (q, k, v))
+    eps = 2.0 ** -eps_log2
+    nq = (L + 127) // 128
+    kept_gpu = torch.full((nq, H), -1, dtype=torch.int32, device=dev)
+    o = torch.full_like(q, SENT)
+    h3lib.attention_varlen_skip(q, k, v, o, L, skip_eps=eps, kept=kept_gpu)
+    h3lib.check_device_error()
+    assert bool((o[L:] == SENT).all())
+    ref, kept = O.attention_skip(np64(q), np64(k), np64(v), L, 128 ** -0.5, eps)
+    want = kept.sum(axis=2)
+    assert want.sum() < nq * H * ((L + 127) // 128)  # tiles really are skipped
+    assert np.array_equal(kept_gpu.cpu().numpy(), want)
+    assert_close_bf16(np64(o[:L]), ref, "skip-softmax, oracle rule")
+    dense = O.attention(np64(q), np64(k), np64(v), L, 128 ** -0.5)
+    assert np.max(np.abs(ref - dense)) > 0

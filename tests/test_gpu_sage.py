@@ -1,51 +1,78 @@
-"""SAGE-style FP8 attention against the oracle: the E4M3 codes and scales bit
-for bit (quantising with the GPU's own K mean, a float32 sum whose rounding
-order the oracle does not share), the K mean to float32 accuracy, and the FP8
-attention within the bf16 tolerances given identical operands."""
+"""SAGE-style FP8 attention against the oracle.
+
+The oracle quantises the bf16 inputs itself (sage_quantize); every E4M3 code,
+every scale and the K mean (FP64 sums on both sides, rounded once to float32)
+must match it bit for bit, at small sizes and at the full 58,758-row size.
+The FP8 attention output is then compared with the oracle's attention_sage on
+the oracle's own operands within the tolerance derived from the E4M3 step of
+the softmax weights (helpers.assert_close_sage): the kernel quantises P
+against an integer running maximum, the oracle against the exact one.
+"""
 import numpy as np
 import pytest
 import torch
 
 import oracle.h3_oracle as O
 from dit_transformer_block_gb300 import inputs as I
-from helpers import assert_close_bf16, np64, rel_l2, sample_rows
+from helpers import assert_close_sage, np64, rel_l2, sample_rows
 
 pytestmark = pytest.mark.gpu
 dev = "cuda"
 SENT = -7.25
+SCALE = 128 ** -0.5
 
 
 def decode(q):
     return q.view(torch.float8_e4m3fn).to(torch.float64).cpu().numpy()
 
 
-def gpu_ops_as_oracle(ops, L):
-    return dict(qc=decode(ops["qc"][:L]), kc=decode(ops["kc"][:L]), vc=decode(ops["vc"][:L]),
-                sq=np64(ops["sq"]).astype(np.float32), sk=np64(ops["sk"]).astype(np.float32),
-                sv=np64(ops["sv"]).astype(np.float32), k_mean=np64(ops["k_mean"]))
+def assert_ops_equal(ops, ref, L):
+    """GPU codes and scales against the oracle's, bit for bit."""
+    got = dict(qc=decode(ops["qc"][:L]), kc=decode(ops["kc"][:L]), vc=decode(ops["vc"][:L]),
+               sq=np64(ops["sq"]), sk=np64(ops["sk"]), sv=np64(ops["sv"]),
+               k_mean=np64(ops["k_mean"]))
+    for key in ("k_mean", "sq", "sk", "sv", "qc", "kc", "vc"):
+        want = np.asarray(ref[key], np.float64).reshape(got[key].shape)
+        bad = int(np.sum(got[key] != want))
+        assert bad == 0, f"{key}: {bad} of {want.size} values differ"
 
 
-@pytest.mark.parametrize("S,L,H", [(256, 250, 4), (640, 600, 3), (128, 1, 2)])
+@pytest.mark.parametrize("S,L,H", [(256, 250, 4), (640, 600, 3), (128, 1, 2), (1152, 1100, 2)])
 def test_sage_codes_and_attention(h3lib, S, L, H):
     inp = I.attention_inputs(S, L, H, 128, seed=S + H, device=dev)
     q, k, v = inp["q"], inp["k"], inp["v"]
     k = (k.float() + 0.75).to(torch.bfloat16)  # a common offset the smoothing removes
     ops = h3lib.sage_quantize(q, k, v, L)
     h3lib.check_device_error()
-    mean64 = np64(k[:L]).mean(0)
-    assert np.allclose(np64(ops["k_mean"]), mean64, rtol=1e-6, atol=1e-7)
-    ref_ops = O.sage_quantize(np64(q), np64(k), np64(v), L, k_mean=np64(ops["k_mean"]))
-    g = gpu_ops_as_oracle(ops, L)
-    for key in ("qc", "kc", "vc", "sq", "sk", "sv"):
-        assert np.array_equal(g[key], ref_ops[key]), key
+    ref_ops = O.sage_quantize(np64(q), np64(k), np64(v), L)
+    assert_ops_equal(ops, ref_ops, L)
     o = torch.full_like(q, SENT)
     h3lib.attention_fp8(ops, o, L)
     h3lib.check_device_error()
-    ref = O.attention_sage(g, L, 128 ** -0.5)
-    assert_close_bf16(np64(o[:L]), ref, "sage attention")
+    ref = O.attention_sage(ref_ops, L, SCALE)
+    terms = O.sage_error_terms(ref_ops, L, SCALE)
+    assert_close_sage(np64(o[:L]), ref, terms, L)
     assert bool((o[L:] == SENT).all())
-    dense = O.attention(np64(q), np64(k), np64(v), L, 128 ** -0.5)
+    dense = O.attention(np64(q), np64(k), np64(v), L, SCALE)
     assert rel_l2(np64(o[:L]), dense) < 0.1
+
+
+def test_sage_all_scores_equal_gives_mean_of_v(h3lib):
+    """q = 0: every score is 0, every weight is exactly representable (224 in
+    the kernel, 448 in the oracle), so both give the mean of the dequantised V
+    rows: equal up to the FP32 accumulation order, within one bf16 step."""
+    S, L, H = 384, 300, 2
+    inp = I.attention_inputs(S, L, H, 128, seed=9, device=dev)
+    q = torch.zeros_like(inp["q"])
+    ops = h3lib.sage_quantize(q, inp["k"], inp["v"], L)
+    ref_ops = O.sage_quantize(np64(q), np64(inp["k"]), np64(inp["v"]), L)
+    assert_ops_equal(ops, ref_ops, L)
+    o = torch.full_like(q, SENT)
+    h3lib.attention_fp8(ops, o, L)
+    h3lib.check_device_error()
+    ref = O.attention_sage(ref_ops, L, SCALE)
+    step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
+    assert np.all(np.abs(np64(o[:L]) - ref) <= step)
 
 
 @pytest.mark.slow
@@ -56,8 +83,10 @@ def test_sage_full_size_sampled(h3lib):
     o = torch.full_like(inp["q"], SENT)
     h3lib.attention_fp8(ops, o, L)
     h3lib.check_device_error()
+    ref_ops = O.sage_quantize(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), L)
+    assert_ops_equal(ops, ref_ops, L)
     rows = sample_rows(L, 256, 12)
-    g = gpu_ops_as_oracle(ops, L)
-    ref = O.attention_sage(g, L, 128 ** -0.5, rows=rows)
-    assert_close_bf16(np64(o[torch.from_numpy(rows).to(dev)]), ref, "sage attention full")
+    ref = O.attention_sage(ref_ops, L, SCALE, rows=rows)
+    terms = O.sage_error_terms(ref_ops, L, SCALE, rows=rows)
+    assert_close_sage(np64(o[torch.from_numpy(rows).to(dev)]), ref, terms, L, "sage full size")
     assert bool((o[L:] == SENT).all())

@@ -801,6 +801,32 @@ def test_sage():
     check_sage(O)
 
 
+def test_sage_error_terms():
+    # the sums of sage_error_terms from the definition, through the library's
+    # softmax: with s = softmax of the natural-log logits, p / sum p = s and
+    # sum p = 1 / max s (the largest weight is exactly 1)
+    r = rng(81)
+    L, H, Dh = 37, 2, 8
+    q = bf16_values(r.standard_normal((L, H, Dh)))
+    k = bf16_values(r.standard_normal((L, H, Dh)))
+    v = bf16_values(r.standard_normal((L, H, Dh)))
+    ops = O.sage_quantize(q, k, v, L, tile=16)
+    rows = np.array([0, 5, 36])
+    a1, a0, v2, u2 = O.sage_error_terms(ops, L, 0.3, rows=rows, tile=16)
+    for h in range(H):
+        for n, i in enumerate(rows):
+            zq = ops["qc"][i, h] * float(ops["sq"][i // 16, h])
+            logits = [float(zq @ ops["kc"][j, h]) * float(ops["sk"][j // 16, h]) * 0.3
+                      for j in range(L)]
+            sm = torch.softmax(torch.tensor(logits, dtype=torch.float64), 0).numpy()
+            w = np.abs(ops["vc"][:, h, :] * ops["sv"][h].astype(np.float64))
+            tot = 1.0 / sm.max()
+            assert np.allclose(a1[n, h], sm @ w, rtol=1e-12)
+            assert np.allclose(a0[n, h], w.sum(0) / tot, rtol=1e-12)
+            assert np.allclose(v2[n, h], (sm * sm) @ (w * w), rtol=1e-12)
+            assert np.allclose(u2[n, h], (w * w).sum(0) / tot ** 2, rtol=1e-12)
+
+
 def _sage_no_smoothing(q, k, v, L, tile=128):
     ops = O.sage_quantize(q, k, v, L, tile)
     ops2 = O.sage_quantize(q, k, v, L, tile)
