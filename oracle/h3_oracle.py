@@ -49,6 +49,8 @@ force on tiny inputs; none is unpinned.
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 # bf16 has 8 significant bits (1 implicit + 7 stored) and the exponent range
@@ -524,8 +526,10 @@ def attention_skip(q, k, v, L: int, scale: float, eps: float, tile: int = 128):
 # range (inv = 448 / amax, code = e4m3(x * inv), scale = amax / 448, every
 # step in float32):
 #   * K is first smoothed by subtracting its per-(head, channel) mean over the
-#     L valid keys (the exact mean rounded once to float32; softmax is
-#     unchanged because each row's scores move by one constant);
+#     L valid keys (their correctly rounded sum, math.fsum, divided by L in
+#     double and rounded to float32, so that the mean depends on the values
+#     alone and not on an order of summation; softmax is unchanged because
+#     each row's scores move by one constant);
 #   * Q and the smoothed K are quantised per (128-row tile, head) block, V per
 #     (head, channel) over the valid keys;
 #   * scores = (Q codes . K codes) * sq * sk; the softmax weights are
@@ -548,13 +552,14 @@ def _absmax_codes(x32, axis):
 def sage_quantize(q, k, v, L: int, tile: int = 128):
     """FP8 operands of SAGE attention. q, k, v [S, H, Dh] bf16 values.
     Returns dict: qc [L,H,Dh], sq [nt,H], kc, sk [nt,H], vc, sv [H,Dh] and
-    k_mean [H,Dh] (float32 values: the float64 mean of the valid keys, rounded
-    once to float32)."""
+    k_mean [H,Dh] (float32 values: math.fsum of the valid keys / L, rounded
+    to float32)."""
     q = np.asarray(q, np.float32)[:L]
     k = np.asarray(k, np.float32)[:L]
     v = np.asarray(v, np.float32)[:L]
     H, Dh = q.shape[1], q.shape[2]
-    k_mean = round_f32(np.asarray(k, np.float64).mean(axis=0))
+    cols = np.ascontiguousarray(np.asarray(k, np.float64).reshape(L, H * Dh).T)
+    k_mean = round_f32(np.array([math.fsum(c.tolist()) for c in cols]).reshape(H, Dh) / L)
     ks = (k - k_mean.astype(np.float32)[None]).astype(np.float32)
     nt = (L + tile - 1) // tile
     qc = np.empty((L, H, Dh)); kc = np.empty((L, H, Dh))
