@@ -606,8 +606,10 @@ def run_ours(a):
         done = [ev() for _ in range(n)]
         dn0 = [ev() for _ in range(n)]
         down = [ev() for _ in range(n)]
+        host = []  # host seconds spent enqueueing: upload, block, download
         for k in range(n):
             b = k % 2
+            h0 = time.perf_counter()
             with torch.cuda.stream(up_s):
                 if k >= 2:
                     up_s.wait_event(down[k - 2])  # buffer b is free again
@@ -615,16 +617,19 @@ def run_ours(a):
                 for d, h in zip(d_buf[b], h_in[b]):
                     d.copy_(h, non_blocking=True)
                 up[k].record(up_s)
+            h1 = time.perf_counter()
             comp_s.wait_event(up[k])
             c0[k].record(comp_s)
             h3.block_forward(cfg, weights, d_buf[b][0], d_buf[b][1], d_buf[b][2], ws,
                              stream=comp_s)
             done[k].record(comp_s)
+            h2 = time.perf_counter()
             with torch.cuda.stream(down_s):
                 down_s.wait_event(done[k])
                 dn0[k].record(down_s)
                 h_out[b].copy_(d_buf[b][0], non_blocking=True)
                 down[k].record(down_s)
+            host.append((h1 - h0, h2 - h1, time.perf_counter() - h2))
         torch.cuda.synchronize()
         if not timeline:
             return None
@@ -637,6 +642,9 @@ def run_ours(a):
             "compute_gap_ms": mean([done[k - 1].elapsed_time(c0[k]) for k in range(1, n)]),
             # first upload start to last download end, on the device
             "span_ms": round(up0[0].elapsed_time(down[n - 1]), 3),
+            # host time spent in the calls that enqueue each part of a step
+            "host_enqueue_ms": {name: mean([1e3 * h[i] for h in host])
+                                for i, name in enumerate(("upload", "block", "download"))},
         }
 
     e2e_run(2)

@@ -539,6 +539,248 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair form (tcgen05 cta_group::2). The two CTAs of a cluster run one head
+// over 512 query rows as two M = 256 groups: group g covers rows
+// p0 + 256 g .. p0 + 256 g + 255, and CTA r holds rows p0 + 256 g + 128 r ..
+// + 127 of it (its query tile g). Every product is one M = 256 MMA issued by
+// one thread of the even CTA; each CTA supplies its own 128 rows of A (Q, or P
+// from its tensor memory) and half of B: keys 64 r .. 64 r + 63 of K_j for
+// S = Q K^T, head channels 64 r .. 64 r + 63 of V_j for O += P V. So each SM
+// reads half of every K/V tile from its own shared memory and receives the
+// other half from its peer: per KV step a CTA loads 32 KB instead of 64 KB
+// and its tensor core reads 128 KB of shared memory instead of 192 KB, for
+// the same FLOPs.
+// Roles per CTA (320 threads):
+//   warps 0-3 / 4-7: softmax of the CTA's query tile 0 / 1 (as in the one-CTA
+//     kernel); after each tile one lane per warp arrives on the even CTA's P
+//     barrier of that group;
+//   warp 8: TMA producer of the CTA's own halves: its Q tiles once, then the
+//     K and V halves through a ring of 16 KB slots, on its own barriers;
+//   warp 9: allocates tensor memory (both CTAs together); in the even CTA one
+//     lane issues the MMAs (order PV0(j), QK0(j+1), PV1(j), QK1(j+1)) and
+//     commits to the barriers of both CTAs; in the odd CTA one lane relays:
+//     each time one of its own copies has landed it arrives on the even CTA's
+//     barrier of that slot, so the MMA issuer sees both halves.
+// Every wait is bounded; both CTAs meet at a cluster barrier before they free
+// tensor memory, after the MMA issuer has waited for its last MMAs.
+constexpr int P2_SLOTS = 8;
+constexpr int HALF_BYTES = TILE_BYTES / 2;  // 64 keys x 128 ch, or 128 keys x 64 ch (bf16)
+constexpr size_t P2_SMEM_BYTES = 1024 + 2 * TILE_BYTES + P2_SLOTS * HALF_BYTES + 256;
+
+enum BarP {
+  BP_Q = 0,
+  BP_FULL = 1,
+  BP_EMPTY = BP_FULL + P2_SLOTS,
+  BP_S = BP_EMPTY + P2_SLOTS,
+  BP_P = BP_S + 2,
+  BP_O = BP_P + 2,
+  BP_DRAIN = BP_O + 2,
+  BP_NUM = BP_DRAIN + 1
+};
+static_assert(BP_NUM * 8 + 16 <= 256, "barrier region");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
+    attention_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sKV = smem;                          // P2_SLOTS halves
+  uint8_t* sQ = smem + P2_SLOTS * HALF_BYTES;   // 2 tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * TILE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BP_NUM);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int p0 = (blockIdx.x >> 1) * 4 * BQ;
+  const int col0 = blockIdx.y * DH;
+  const int n = a.num_kv;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < BP_NUM; ++i) {
+      uint32_t count = 1;
+      // the even CTA's Q and slot barriers also take the odd CTA's relay
+      if (i == BP_Q || (i >= BP_FULL && i < BP_FULL + P2_SLOTS)) count = leader ? 2 : 1;
+      if (i == BP_P || i == BP_P + 1) count = 8;  // one lane per softmax warp, both CTAs
+      mbar_init(bar(i), count);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(bar(BP_Q), 2 * TILE_BYTES);
+      for (int g = 0; g < 2; ++g) {
+        const int row = p0 + 2 * BQ * g + BQ * static_cast<int>(rank);
+        tma_load_2d(smem_u32(sQ + g * TILE_BYTES), &tmQ, bar(BP_Q), col0, row);
+        tma_load_2d(smem_u32(sQ + g * TILE_BYTES + BOX_BYTES), &tmQ, bar(BP_Q), col0 + 64, row);
+      }
+      int issued = 0;
+      for (int t = 0; t < 2 * n; ++t) {  // even t: K half of tile t/2, odd t: V half
+        const int slot = t % P2_SLOTS;
+        const uint32_t use = static_cast<uint32_t>(t / P2_SLOTS);
+        if (!mbar_wait_cluster(bar(BP_EMPTY + slot), (use & 1u) ^ 1u, a.err,
+                               ERR_WAIT_ATTN_PRODUCER))
+          break;
+        const uint32_t full = bar(BP_FULL + slot);
+        mbar_arrive_expect_tx(full, HALF_BYTES);
+        const uint32_t dst = smem_u32(sKV + slot * HALF_BYTES);
+        const int key0 = (t >> 1) * BKV;
+        if ((t & 1) == 0) {
+          const int k_row = key0 + 64 * static_cast<int>(rank);
+          tma_load_2d(dst, &tmK, full, col0, k_row);
+          tma_load_2d(dst + HALF_BYTES / 2, &tmK, full, col0 + 64, k_row);
+        } else {
+          tma_load_2d(dst, &tmV, full, col0 + 64 * static_cast<int>(rank), key0);
+        }
+        issued = t + 1;
+      }
+      // No copy of this CTA may still be landing when it exits: wait, bounded,
+      // for Q and for the last load of every slot (long done in a normal run).
+      const uint64_t t0 = globaltimer_ns();
+      const uint64_t lim = drain_limit_ns(a.err);
+      mbar_wait_cluster_drain(bar(BP_Q), 0u, t0, lim);
+      for (int t = issued > P2_SLOTS ? issued - P2_SLOTS : 0; t < issued; ++t)
+        mbar_wait_cluster_drain(bar(BP_FULL + t % P2_SLOTS),
+                                static_cast<uint32_t>(t / P2_SLOTS) & 1u, t0, lim);
+    }
+  } else if (warp == 9) {
+    if (leader && lane == 0) {
+      // -------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(2 * BQ, BKV, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(2 * BQ, DH, true);
+      const uint32_t kv_addr = smem_u32(sKV), q_addr = smem_u32(sQ);
+      constexpr uint16_t kBoth = 3;
+      auto slot_of = [](int t) { return t % P2_SLOTS; };
+      auto wait_full = [&](int t) {
+        return mbar_wait_cluster(bar(BP_FULL + slot_of(t)),
+                                 static_cast<uint32_t>(t / P2_SLOTS) & 1u, a.err,
+                                 ERR_WAIT_ATTN_MMA);
+      };
+      auto qk = [&](int g, int j) {  // S_g = Q_g K_j^T over both CTAs' rows
+        const uint32_t k_addr = kv_addr + slot_of(2 * j) * HALF_BYTES;
+        const uint32_t qa = q_addr + g * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t q_off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          const uint32_t k_off = (kk >> 2) * (HALF_BYTES / 2) + (kk & 3) * 32;
+          mma_ss_pair(tmem + g * 128, sdesc_sw128(qa + q_off, 16, 1024),
+                      sdesc_sw128(k_addr + k_off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_pair_mc(bar(BP_S + g), kBoth);
+      };
+      auto pv = [&](int g, int j) {  // O_g += P_g V_j
+        const uint32_t v_addr = kv_addr + slot_of(2 * j + 1) * HALF_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          mma_ts_pair(tmem + 256 + g * 128, tmem + g * 128 + kk * 8,
+                      sdesc_sw128(v_addr + kk * 2048, HALF_BYTES, 1024), idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_pair_mc(bar(BP_O + g), kBoth);
+      };
+      bool ok = mbar_wait_cluster(bar(BP_Q), 0, a.err, ERR_WAIT_ATTN_MMA) && wait_full(0);
+      if (ok) {
+        tc_fence_after();
+        qk(0, 0);
+        qk(1, 0);
+        mma_commit_pair_mc(bar(BP_EMPTY + slot_of(0)), kBoth);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const uint32_t par = static_cast<uint32_t>(j) & 1u;
+        if (!wait_full(2 * j + 1) ||
+            !mbar_wait_cluster(bar(BP_P), par, a.err, ERR_WAIT_ATTN_MMA))
+          break;
+        tc_fence_after();
+        pv(0, j);
+        const bool more = j + 1 < n;
+        if (more) {
+          if (!wait_full(2 * j + 2)) break;
+          tc_fence_after();
+          qk(0, j + 1);
+        }
+        if (!mbar_wait_cluster(bar(BP_P + 1), par, a.err, ERR_WAIT_ATTN_MMA)) break;
+        tc_fence_after();
+        pv(1, j);
+        mma_commit_pair_mc(bar(BP_EMPTY + slot_of(2 * j + 1)), kBoth);
+        if (more) {
+          qk(1, j + 1);
+          mma_commit_pair_mc(bar(BP_EMPTY + slot_of(2 * j + 2)), kBoth);
+        }
+      }
+      // Every MMA issued here must be done with both CTAs' shared and tensor
+      // memory before either frees them: commit and wait, bounded.
+      mma_commit_pair_mc(bar(BP_DRAIN), 1);
+      mbar_wait_cluster_drain(bar(BP_DRAIN), 0u, globaltimer_ns(), drain_limit_ns(a.err));
+    } else if (!leader && lane == 0) {
+      // ------------------------------------------------------------ relay
+      const uint32_t lead_q = mapa_shared(bar(BP_Q), 0);
+      if (mbar_wait_cluster(bar(BP_Q), 0, a.err, ERR_WAIT_ATTN_PRODUCER)) {
+        mbar_arrive_cluster(lead_q);
+        for (int t = 0; t < 2 * n; ++t) {
+          const int slot = t % P2_SLOTS;
+          if (!mbar_wait_cluster(bar(BP_FULL + slot), static_cast<uint32_t>(t / P2_SLOTS) & 1u,
+                                 a.err, ERR_WAIT_ATTN_PRODUCER))
+            break;
+          mbar_arrive_cluster(mapa_shared(bar(BP_FULL + slot), 0));
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax
+    const int tile = warp >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + tile * 128;
+    const uint32_t tO = tmem + lane_base + 256 + tile * 128;
+    const uint32_t p_bar = mapa_shared(bar(BP_P + tile), 0);  // the even CTA's
+    float m = -INFINITY, l = 0.f, m_keep = -INFINITY;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait_cluster(bar(BP_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
+                             ERR_WAIT_ATTN_SOFTMAX)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      softmax_tile<false, false>(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l, 0.f, m_keep,
+                                 true, nullptr, 0u, 0u, a.err, ok);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(p_bar);
+    }
+    if (ok && mbar_wait_cluster(bar(BP_O + tile), static_cast<uint32_t>(n - 1) & 1u, a.err,
+                                ERR_WAIT_ATTN_SOFTMAX)) {
+      tc_fence_after();
+      const int row = p0 + 2 * BQ * tile + BQ * static_cast<int>(rank) + quarter * 32 + lane;
+      store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L, nullptr);
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
 }  // namespace
 
 template <bool F8, bool SKIP>
@@ -552,8 +794,15 @@ static h3_status set_attention_smem() {
 h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
                            void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
                            float skip_eps, int* kept) {
-  const bool skip = skip_eps > 0.f;
-  h3_status st = skip ? set_attention_smem<false, true>() : set_attention_smem<false, false>();
+  const bool skip = skip_eps >= 0.f;
+  h3_status st;
+  if (skip) {
+    st = set_attention_smem<false, true>();
+  } else {
+    static std::atomic<bool> done[64];
+    st = set_smem_limit(done, attention_pair_kernel, P2_SMEM_BYTES,
+                        "attention: set shared memory size");
+  }
   if (st != H3_OK) return st;
   AttnArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
@@ -562,20 +811,24 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   a.H = H;
   a.num_kv = (L + BKV - 1) / BKV;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.skip_log2 = skip ? -log2f(skip_eps) : 0.f;
+  a.skip_log2 = skip_eps > 0.f ? -log2f(skip_eps) : INFINITY;
   a.kept = skip ? kept : nullptr;
   if ((st = dev_err(&a.err)) != H3_OK) return st;
   CUtensorMap tq, tk, tv;
   const uint64_t width = static_cast<uint64_t>(H) * DH;
   const uint64_t stride = static_cast<uint64_t>(ld_in) * 2;
   if ((st = make_tmap_bf16_2d(&tq, q, width, L, stride, 64, BQ)) != H3_OK) return st;
-  if ((st = make_tmap_bf16_2d(&tk, k, width, L, stride, 64, BKV)) != H3_OK) return st;
+  if ((st = make_tmap_bf16_2d(&tk, k, width, L, stride, 64, skip ? BKV : BKV / 2)) != H3_OK)
+    return st;
   if ((st = make_tmap_bf16_2d(&tv, v, width, L, stride, 64, BKV)) != H3_OK) return st;
-  dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
-  if (skip)
+  if (skip) {
+    dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
     attention_kernel<false, true><<<grid, Q2_THREADS, Q2_SMEM_BYTES, s>>>(tq, tk, tv, a);
-  else
-    attention_kernel<false, false><<<grid, Q2_THREADS, Q2_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  } else {
+    // CTA pairs (a cluster of two along x), 512 query rows per pair
+    dim3 grid(2 * ((L + 4 * BQ - 1) / (4 * BQ)), H);
+    attention_pair_kernel<<<grid, Q2_THREADS, P2_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  }
   return cuda_fail(cudaGetLastError(), "attention launch");
 }
 

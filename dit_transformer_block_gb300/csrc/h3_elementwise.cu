@@ -69,7 +69,9 @@ constexpr int QK_WARPS = 8;
 constexpr int QK_BATCH = 8;  // head pairs loaded per batch (16 heads)
 
 struct RopeTable {
-  double omega[QK_HEAD_DIM / 2];  // angle per unit position for each pair
+  // turns per unit position of each pair, omega / (2 pi) in 0.64 fixed point
+  // (omega / (2 pi) rounded to double, then scaled exactly by 2^64)
+  uint64_t turn[QK_HEAD_DIM / 2];
   int axis[QK_HEAD_DIM / 2];      // which position (t, h, w) drives the pair
   // split-half layout, per 8-channel slice s of a head: the slice holding the
   // partners, whether s holds first elements, and the pair of its channel 0
@@ -78,16 +80,15 @@ struct RopeTable {
   int half_pair0[QK_HEAD_DIM / 8];
 };
 
-constexpr double kTwoPi = 6.283185307179586476925286766559;
-constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
-
-// Angle of pair pr at position p: formed and reduced modulo 2*pi in FP64,
-// then sin/cos in FP32 on an argument in [-pi, pi].
-__device__ __forceinline__ void rope_angle(int32_t p, double omega, float& sn, float& cs) {
-  const double phi = static_cast<double>(p) * omega;
-  const double turns = rint(phi * kInvTwoPi);
-  const float red = static_cast<float>(fma(-turns, kTwoPi, phi));
-  sincosf(red, &sn, &cs);
+// Angle of a pair at position p: its turns p * omega / (2 pi) modulo 1, exact
+// in 64-bit fixed point (the integer product wraps modulo 2^64, i.e. whole
+// turns), read as a signed fraction t of a half turn in [-1, 1) (one rounding
+// to float32), then sin and cos of pi * t in FP32. No FP64 arithmetic, whose
+// rate on this GPU is a small fraction of FP32's.
+__device__ __forceinline__ void rope_angle(int32_t p, uint64_t turn, float& sn, float& cs) {
+  const uint64_t f = static_cast<uint64_t>(static_cast<int64_t>(p)) * turn;
+  const float t = __ll2float_rn(static_cast<int64_t>(f)) * 0x1p-63f;
+  sincospif(t, &sn, &cs);
 }
 
 // One thread per (row, pair): out[row * 64 + pr] = (cos, sin).
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(256)
   const int64_t row = i / (QK_HEAD_DIM / 2);
   const int pr = static_cast<int>(i - row * (QK_HEAD_DIM / 2));
   float sn, cs;
-  rope_angle(__ldg(pos + 3 * row + tab.axis[pr]), tab.omega[pr], sn, cs);
+  rope_angle(__ldg(pos + 3 * row + tab.axis[pr]), tab.turn[pr], sn, cs);
   out[i] = make_float2(cs, sn);
 }
 
@@ -127,6 +128,19 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
   const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp + 4));
   const float gain[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 
+  // the first batch of heads is requested before the angles are formed, so
+  // the loads are in flight meanwhile
+  uint4 v[QK_BATCH];
+  auto load_batch = [&](int h0) {
+#pragma unroll
+    for (int i = 0; i < QK_BATCH; ++i) {
+      const int head = h0 + 2 * i + half;
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (head < H) v[i] = *reinterpret_cast<const uint4*>(base + head * QK_HEAD_DIM);
+    }
+  };
+  load_batch(0);
+
   // Angles of this lane's pairs: 4 interleaved pairs; or, split-half, 8 pairs
   // shared with the partner lane, each lane evaluating 4 of them
   constexpr int NP = HALF ? 8 : 4;
@@ -139,7 +153,7 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const int pr = pair0 + t;
-    rope_angle(p3[tab.axis[pr]], tab.omega[pr], s4[t], c4[t]);
+    rope_angle(p3[tab.axis[pr]], tab.turn[pr], s4[t], c4[t]);
   }
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
@@ -157,13 +171,7 @@ __global__ void __launch_bounds__(QK_WARPS * 32)
   }
 
   for (int h0 = 0; h0 < H; h0 += 2 * QK_BATCH) {
-    uint4 v[QK_BATCH];
-#pragma unroll
-    for (int i = 0; i < QK_BATCH; ++i) {
-      const int head = h0 + 2 * i + half;
-      v[i] = make_uint4(0, 0, 0, 0);
-      if (head < H) v[i] = *reinterpret_cast<const uint4*>(base + head * QK_HEAD_DIM);
-    }
+    if (h0 > 0) load_batch(h0);
 #pragma unroll
     for (int i = 0; i < QK_BATCH; ++i) {
       const int head = h0 + 2 * i + half;
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(T)
     const int t = threadIdx.x;
     if (t < QK_HEAD_DIM / 2) {
       float sn, cs;
-      rope_angle(__ldg(pos + 3LL * row + tab.axis[t]), tab.omega[t], sn, cs);
+      rope_angle(__ldg(pos + 3LL * row + tab.axis[t]), tab.turn[t], sn, cs);
       rope_out[static_cast<int64_t>(row) * (QK_HEAD_DIM / 2) + t] = make_float2(cs, sn);
     }
   }
@@ -530,6 +538,8 @@ h3_status launch_swiglu(const void* gate_up, void* out, int L, int F, cudaStream
   return cuda_fail(cudaGetLastError(), "swiglu launch");
 }
 
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+
 static RopeTable rope_table(const int* axis_dims, float theta) {
   RopeTable tab{};
   int pr = 0;
@@ -537,7 +547,11 @@ static RopeTable rope_table(const int* axis_dims, float theta) {
   for (int a = 0; a < 3; ++a) {
     const int d = axis_dims[a];
     for (int j = 0; j < d / 2; ++j, ++pr) {
-      tab.omega[pr] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(d));
+      const double omega =
+          std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(d));
+      // omega / (2 pi) < 1: scaled by 2^64 it is an integer below 2^63 with
+      // at most 53 significant bits, which the conversion keeps exactly
+      tab.turn[pr] = static_cast<uint64_t>(std::ldexp(omega / kTwoPi, 64));
       tab.axis[pr] = a;
     }
     // split-half slices (meaningful when d % 16 == 0): slice s of the first

@@ -137,13 +137,15 @@ h3_status launch_quantize_fp8_rows(const void* x, int64_t ldx, void* q, int64_t 
                                    int R, int K, cudaStream_t s);
 
 // o[:L] = attention(q, k, v); q/k/v rows of stride ld_in elements, o of ld_out.
-// skip_eps > 0: Skip-Softmax, a key tile is left out for a query tile when
-// every valid row's tile maximum is below eps times the row's exact running
-// maximum over the kept tiles; kept (optional, [ceil(L/128), H]) receives the
-// number of key tiles kept per (query tile, head).
+// skip_eps < 0: dense attention (the CTA-pair kernel). skip_eps >= 0:
+// Skip-Softmax (the one-CTA kernel with its vote), a key tile is left out for
+// a query tile when every valid row's tile maximum is below eps times the
+// row's exact running maximum over the kept tiles (eps = 0 never skips); kept
+// (optional, [ceil(L/128), H]) receives the number of key tiles kept per
+// (query tile, head).
 h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
                            void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
-                           float skip_eps = 0.f, int* kept = nullptr);
+                           float skip_eps = -1.f, int* kept = nullptr);
 
 // SAGE-style FP8 attention: operands (h3_sage.cu) and the FP8 attention
 // kernel (h3_attention.cu). Codes [L, H*128] bytes with row stride ldc; sq,

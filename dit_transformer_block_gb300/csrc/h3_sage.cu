@@ -2,11 +2,13 @@
 // P and V quantised to FP8 for the QK and PV products).
 //
 //   1. kv_stats_partial / kv_stats_final: per (head, channel) mean of K and
-//      absmax of V over the L valid rows: chunk partial sums in FP64, then an
-//      FP64 combine, a division by L in FP64 and one rounding to float32. A
-//      sum of at most 2^17 bf16 values is exact in FP64 unless a channel holds
-//      a nonzero |k| < 2^-27, so the mean is the exact mean rounded once,
-//      whatever the order of the additions;
+//      absmax of V over the L valid rows. The K sum is exact: each 512-row
+//      chunk is summed in 64-bit fixed point (units of 2^-40; exact for
+//      nonzero |k| in [2^-33, 2^14), which bf16 keys of unit-RMS heads always
+//      are), a chunk holding a value outside that range is summed in FP64
+//      instead, and the chunks are combined in 128-bit integers. The exact sum
+//      is rounded once to double, divided by L in FP64 and rounded once to
+//      float32: the exact mean rounded once, whatever the order of the rows;
 //   2. qk_tile_quant: Q, and K minus its mean, to E4M3 per (128-row tile,
 //      head) block with absmax scaling;
 //   3. v_quant: V to E4M3 per (head, channel) with the V absmax.
@@ -26,58 +28,81 @@ namespace {
 constexpr int DH = 128;
 constexpr int ST_ROWS = 512;  // rows per statistics chunk
 
+// bf16 bits -> the value in units of 2^-40 when its exponent field lies in
+// [94, 140] (magnitude in [2^-33, 2^14)), as a two's-complement integer of at
+// most 55 bits; `in_range` tells whether it did (zero counts as in range).
+__device__ __forceinline__ int64_t bf16_fixed40(uint32_t bits, bool& in_range) {
+  const uint32_t e = (bits >> 7) & 0xFFu;
+  const uint32_t mag_bits = bits & 0x7FFFu;
+  in_range = mag_bits == 0u || (e >= 94u && e <= 140u);
+  const uint32_t sh = e >= 94u ? min(e - 94u, 46u) : 0u;
+  const int64_t mag = e >= 94u ? static_cast<int64_t>((128u | (bits & 0x7Fu))) << sh : 0;
+  return (bits & 0x8000u) ? -mag : mag;
+}
+
 // grid (chunks, H), 128 threads: thread d owns channel d of head blockIdx.y.
-// Four independent FP64 partial sums per thread (the additions are exact, so
-// their grouping does not change the result).
+// psum_i: the chunk's K sum in units of 2^-40 (at most 512 terms below 2^54,
+// so no overflow); psum_d: 0, or the chunk's K sum in FP64 when one of its
+// values lies outside the fixed-point range (psum_i is then 0).
 __global__ void __launch_bounds__(DH)
     kv_stats_partial_kernel(const __nv_bfloat16* __restrict__ k,
                             const __nv_bfloat16* __restrict__ v, int64_t ld, int L,
-                            double* __restrict__ psum, float* __restrict__ pmax) {
+                            int64_t* __restrict__ psum_i, double* __restrict__ psum_d,
+                            float* __restrict__ pmax) {
   const int chunk = blockIdx.x, h = blockIdx.y, d = threadIdx.x, H = gridDim.y;
   const int r0 = chunk * ST_ROWS, r1 = min(L, r0 + ST_ROWS);
   const int64_t col = static_cast<int64_t>(h) * DH + d;
-  double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
+  const uint16_t* kb = reinterpret_cast<const uint16_t*>(k);
+  int64_t acc = 0;
+  bool all_in = true;
   float mx = 0.f;
-  int r = r0;
-  for (; r + 4 <= r1; r += 4) {
+  for (int r = r0; r < r1; ++r) {
     const int64_t off = static_cast<int64_t>(r) * ld + col;
-    const float k0 = __bfloat162float(k[off]), k1 = __bfloat162float(k[off + ld]);
-    const float k2 = __bfloat162float(k[off + 2 * ld]), k3 = __bfloat162float(k[off + 3 * ld]);
-    const float v0 = fabsf(__bfloat162float(v[off])), v1 = fabsf(__bfloat162float(v[off + ld]));
-    const float v2 = fabsf(__bfloat162float(v[off + 2 * ld]));
-    const float v3 = fabsf(__bfloat162float(v[off + 3 * ld]));
-    s0 = __dadd_rn(s0, static_cast<double>(k0));
-    s1 = __dadd_rn(s1, static_cast<double>(k1));
-    s2 = __dadd_rn(s2, static_cast<double>(k2));
-    s3 = __dadd_rn(s3, static_cast<double>(k3));
-    mx = fmaxf(mx, max3f(v0, v1, fmaxf(v2, v3)));
-  }
-  for (; r < r1; ++r) {
-    const int64_t off = static_cast<int64_t>(r) * ld + col;
-    s0 = __dadd_rn(s0, static_cast<double>(__bfloat162float(k[off])));
+    bool in;
+    acc += bf16_fixed40(kb[off], in);
+    all_in &= in;
     mx = fmaxf(mx, fabsf(__bfloat162float(v[off])));
   }
+  double dsum = 0.0;
+  if (!all_in) {  // rare: a value too small or too large for the fixed point
+    acc = 0;
+    for (int r = r0; r < r1; ++r)
+      dsum = __dadd_rn(dsum, static_cast<double>(
+                                 __bfloat162float(k[static_cast<int64_t>(r) * ld + col])));
+  }
   const int64_t o = (static_cast<int64_t>(chunk) * H + h) * DH + d;
-  psum[o] = __dadd_rn(__dadd_rn(s0, s1), __dadd_rn(s2, s3));
+  psum_i[o] = acc;
+  psum_d[o] = dsum;
   pmax[o] = mx;
 }
 
-// grid H, 128 threads: combine the chunks (FP64), mean = sum / L in FP64,
-// rounded once to float32.
+// grid H, 128 threads: combine the chunks, mean = sum / L in FP64, rounded
+// once to float32.
 __global__ void __launch_bounds__(DH)
-    kv_stats_final_kernel(const double* __restrict__ psum, const float* __restrict__ pmax,
-                          int chunks, int L, float* __restrict__ k_mean, float* __restrict__ sv,
+    kv_stats_final_kernel(const int64_t* __restrict__ psum_i, const double* __restrict__ psum_d,
+                          const float* __restrict__ pmax, int chunks, int L,
+                          float* __restrict__ k_mean, float* __restrict__ sv,
                           float* __restrict__ inv_v) {
   const int h = blockIdx.x, d = threadIdx.x, H = gridDim.x;
-  double s = 0.0;
+  __int128 si = 0;
+  double sd = 0.0;
   float mx = 0.f;
   for (int ch = 0; ch < chunks; ++ch) {
     const int64_t o = (static_cast<int64_t>(ch) * H + h) * DH + d;
-    s = __dadd_rn(s, psum[o]);
+    si += psum_i[o];
+    sd = __dadd_rn(sd, psum_d[o]);
     mx = fmaxf(mx, pmax[o]);
   }
+  // the integer sum rounded once to double (exact below 2^53 units): split
+  // into a high part that is a multiple of 2^32 and a low part, both exact in
+  // double when |si| < 2^85, then one rounding in their sum
+  const int64_t hi = static_cast<int64_t>(si >> 32);
+  const double whole =
+      __dadd_rn(static_cast<double>(hi) * 4294967296.0,
+                static_cast<double>(static_cast<uint32_t>(si & 0xFFFFFFFFu)));
+  const double sum = __dadd_rn(whole * 0x1p-40, sd);
   const int i = h * DH + d;
-  k_mean[i] = __double2float_rn(__ddiv_rn(s, static_cast<double>(L)));
+  k_mean[i] = __double2float_rn(__ddiv_rn(sum, static_cast<double>(L)));
   sv[i] = __fdiv_rn(mx, 448.0f);
   inv_v[i] = mx > 0.f ? __fdiv_rn(448.0f, mx) : 0.f;
 }
@@ -174,7 +199,7 @@ __global__ void __launch_bounds__(256)
 
 size_t sage_scratch_bytes(int L, int H) {
   const size_t chunks = (static_cast<size_t>(L) + ST_ROWS - 1) / ST_ROWS;
-  return chunks * H * DH * (sizeof(double) + sizeof(float)) +
+  return chunks * H * DH * (sizeof(int64_t) + sizeof(double) + sizeof(float)) +
          static_cast<size_t>(H) * DH * sizeof(float);
 }
 
@@ -183,14 +208,16 @@ h3_status launch_sage_quantize(const void* q, const void* k, const void* v, int6
                                float* sq, float* sk, float* sv, float* k_mean, void* scratch,
                                cudaStream_t s) {
   const int chunks = (L + ST_ROWS - 1) / ST_ROWS;
-  double* psum = static_cast<double*>(scratch);
-  float* pmax = reinterpret_cast<float*>(psum + static_cast<size_t>(chunks) * H * DH);
-  float* inv_v = pmax + static_cast<size_t>(chunks) * H * DH;
+  const size_t n = static_cast<size_t>(chunks) * H * DH;
+  int64_t* psum_i = static_cast<int64_t*>(scratch);
+  double* psum_d = reinterpret_cast<double*>(psum_i + n);
+  float* pmax = reinterpret_cast<float*>(psum_d + n);
+  float* inv_v = pmax + n;
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   const auto* kk = static_cast<const __nv_bfloat16*>(k);
   const auto* vv = static_cast<const __nv_bfloat16*>(v);
-  kv_stats_partial_kernel<<<dim3(chunks, H), DH, 0, s>>>(kk, vv, ld, L, psum, pmax);
-  kv_stats_final_kernel<<<H, DH, 0, s>>>(psum, pmax, chunks, L, k_mean, sv, inv_v);
+  kv_stats_partial_kernel<<<dim3(chunks, H), DH, 0, s>>>(kk, vv, ld, L, psum_i, psum_d, pmax);
+  kv_stats_final_kernel<<<H, DH, 0, s>>>(psum_i, psum_d, pmax, chunks, L, k_mean, sv, inv_v);
   const int tiles = (L + 127) / 128;
   qk_tile_quant_kernel<<<dim3(tiles, H, 2), QT_THREADS, 0, s>>>(qq, kk, ld, k_mean, L, qc, kc, ldc,
                                                                sq, sk);

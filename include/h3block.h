@@ -104,7 +104,9 @@ h3_status h3_mod_norm_residual(float* resid, const void* delta, const float* gat
  *   q_gain, k_gain [Dh] float32
  *   pos     [S, 3] int32
  *   axis_dims  HOST array of 3 even non-negative ints summing to Dh
- * Dh == 128. FP32 arithmetic; the angle is formed and reduced in FP64.
+ * Dh == 128. FP32 arithmetic; the angle is reduced exactly in fixed point
+ * (turns = pos * theta^(-2j/d) / (2 pi) modulo 1 in 64-bit integer arithmetic,
+ * the per-pair factor rounded to double) and its sin/cos taken in FP32.
  */
 h3_status h3_qk_norm_rope(void* q, void* k, const float* q_gain, const float* k_gain,
                           const int32_t* pos, const int* axis_dims, int S, int L, int H,
@@ -161,9 +163,10 @@ h3_status h3_attention_varlen_skip(const void* q, const void* k, const void* v, 
  * quantised to FP8 for the QK and PV products). Two steps:
  *
  * h3_sage_quantize: K is smoothed by subtracting its per-(head, channel)
- * mean over the L valid keys (summed in FP64, divided by L in FP64 and
- * rounded once to float32: the exact mean rounded once for any bf16 input
- * without nonzero values below 2^-27 in magnitude), Q and the smoothed K are
+ * mean over the L valid keys (their exact sum, taken in 64-bit fixed point
+ * for keys whose nonzero magnitudes lie in [2^-33, 2^14) and in FP64 for a
+ * 512-row chunk holding any other value, rounded once to double, divided by
+ * L in double and rounded to float32), Q and the smoothed K are
  * quantised to E4M3 per (128-row tile, head) block and V per (head, channel),
  * all with absmax scaling (inv = 448 / amax, code = E4M3_satfinite(x * inv),
  * scale = amax / 448, float32 steps).
@@ -225,7 +228,8 @@ h3_status h3_linear_swiglu(const void* x, const void* w_gu, void* out, int S, in
  * projection's epilogue, which reads this table):
  *   table[i, p] = (cos phi, sin phi), phi = pos[i, a] * theta^(-2j / axis_dims[a])
  * for channel pair p of a 128-channel head (section a, pair j within it, as in
- * h3_qk_norm_rope), angle formed and reduced in FP64, cos/sin in FP32.
+ * h3_qk_norm_rope), angle reduced to turns modulo 1 in 64-bit fixed point as
+ * h3_qk_norm_rope does it, cos/sin in FP32.
  *   pos   [S, 3] int32; axis_dims HOST [3], even, sum 128
  *   table [S, 64, 2] float32 (rows >= L not written)
  */
