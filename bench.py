@@ -582,20 +582,23 @@ def run_ours(a):
 
     # ---- end to end through the C-ABI with host buffers: every step uploads
     # its residual, modulation and positions from pinned memory and downloads
-    # the updated residual. Uploads and downloads run on streams of their own
-    # with two device buffer sets, so step k+1's upload and step k-1's
-    # download overlap step k's compute; the timed region spans the first
-    # upload to the last download.
+    # the updated residual. All copies run in order on one copy stream (an
+    # upload and a download running at the same time slowed each other down
+    # several-fold on this host link), three device buffer sets: step k+3's
+    # upload is queued right behind step k's download and has two block
+    # times to land (single uploads sometimes took 40+ ms instead of 6); the
+    # timed region spans the first upload to the last download.
+    NBUF = 3
     pin = lambda t: t.detach().to("cpu").pin_memory()
     h_one = (pin(inp["resid"]), pin(inp["mod"]), pin(inp["pos"]))
-    h_in = [h_one, h_one]  # both buffer sets upload the same host data
+    h_in = [h_one] * NBUF  # every buffer set uploads the same host data
     h_one_out = torch.empty_like(h_one[0]).pin_memory()
-    h_out = [h_one_out, h_one_out]
+    h_out = [h_one_out] * NBUF
     d_buf = [(torch.empty_like(inp["resid"]), torch.empty_like(inp["mod"]),
-              torch.empty_like(inp["pos"])) for _ in range(2)]
+              torch.empty_like(inp["pos"])) for _ in range(NBUF)]
     h2d = sum(t.numel() * t.element_size() for t in h_in[0])
     d2h = h_out[0].numel() * 4
-    up_s, down_s = torch.cuda.Stream(), torch.cuda.Stream()
+    copy_s = torch.cuda.Stream()
     comp_s = torch.cuda.Stream()  # not the legacy default stream, which would serialise the copies
 
     def e2e_run(n, timeline=False):
@@ -607,29 +610,34 @@ def run_ours(a):
         dn0 = [ev() for _ in range(n)]
         down = [ev() for _ in range(n)]
         host = []  # host seconds spent enqueueing: upload, block, download
+
+        def upload(k):  # on copy_s, into buffer set k % NBUF
+            up0[k].record(copy_s)
+            for d, h in zip(d_buf[k % NBUF], h_in[k % NBUF]):
+                d.copy_(h, non_blocking=True)
+            up[k].record(copy_s)
+
+        with torch.cuda.stream(copy_s):
+            for k in range(min(n, NBUF)):
+                upload(k)
         for k in range(n):
-            b = k % 2
+            b = k % NBUF
             h0 = time.perf_counter()
-            with torch.cuda.stream(up_s):
-                if k >= 2:
-                    up_s.wait_event(down[k - 2])  # buffer b is free again
-                up0[k].record(up_s)
-                for d, h in zip(d_buf[b], h_in[b]):
-                    d.copy_(h, non_blocking=True)
-                up[k].record(up_s)
-            h1 = time.perf_counter()
             comp_s.wait_event(up[k])
             c0[k].record(comp_s)
             h3.block_forward(cfg, weights, d_buf[b][0], d_buf[b][1], d_buf[b][2], ws,
                              stream=comp_s)
             done[k].record(comp_s)
-            h2 = time.perf_counter()
-            with torch.cuda.stream(down_s):
-                down_s.wait_event(done[k])
-                dn0[k].record(down_s)
+            h1 = time.perf_counter()
+            with torch.cuda.stream(copy_s):
+                copy_s.wait_event(done[k])
+                dn0[k].record(copy_s)
                 h_out[b].copy_(d_buf[b][0], non_blocking=True)
-                down[k].record(down_s)
-            host.append((h1 - h0, h2 - h1, time.perf_counter() - h2))
+                down[k].record(copy_s)
+                h2 = time.perf_counter()
+                if k + NBUF < n:
+                    upload(k + NBUF)  # buffer set b: its download is queued just before
+            host.append((time.perf_counter() - h2, h1 - h0, h2 - h1))
         torch.cuda.synchronize()
         if not timeline:
             return None
@@ -645,6 +653,11 @@ def run_ours(a):
             # host time spent in the calls that enqueue each part of a step
             "host_enqueue_ms": {name: mean([1e3 * h[i] for h in host])
                                 for i, name in enumerate(("upload", "block", "download"))},
+            # device times (ms from the first upload) of four middle steps:
+            # upload start/end, block start/end, download start/end
+            "schedule_ms": {str(k): [round(up0[0].elapsed_time(e[k]), 2)
+                                     for e in (up0, up, c0, done, dn0, down)]
+                            for k in range(n // 2, min(n, n // 2 + 4))},
         }
 
     e2e_run(2)
@@ -724,8 +737,9 @@ def run_ours(a):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": h3.BLOCK_LAUNCHES * a.steps,
         "e2e_note": (f"{a.e2e_steps} steps timed from the first upload to the last download "
-                     "(pipeline fill and drain included); uploads and downloads on their own "
-                     "streams, two buffer sets: copies overlap compute"),
+                     "(pipeline fill and drain included); uploads and downloads in order on one "
+                     "copy stream beside the compute stream, three buffer sets: copies overlap "
+                     "compute"),
         "e2e_timeline": e2e_timeline,
         "clocks": clocks.summary(),
         "extras": extras,

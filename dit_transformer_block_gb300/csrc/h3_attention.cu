@@ -555,27 +555,36 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
 //   warps 0-3 / 4-7: softmax of the CTA's query tile 0 / 1 (as in the one-CTA
 //     kernel); after each tile one lane per warp arrives on the even CTA's P
 //     barrier of that group;
-//   warp 8: TMA producer of the CTA's own halves: its Q tiles once, then the
-//     K and V halves through a ring of 16 KB slots, on its own barriers;
+//   warp 8: TMA producer of the CTA's own halves: its Q tiles once, then, per
+//     KV step, its K half and V half together into one 32 KB stage of a
+//     4-stage ring, on its own barriers;
 //   warp 9: allocates tensor memory (both CTAs together); in the even CTA one
 //     lane issues the MMAs (order PV0(j), QK0(j+1), PV1(j), QK1(j+1)) and
 //     commits to the barriers of both CTAs; in the odd CTA one lane relays:
-//     each time one of its own copies has landed it arrives on the even CTA's
-//     barrier of that slot, so the MMA issuer sees both halves.
+//     each time one of its own stages has landed it arrives on the even CTA's
+//     barrier of that stage, so the MMA issuer sees both halves.
+// The tensor pipe takes about one MMA ahead of its issuer, so every commit or
+// barrier wait of the issuing thread between two products is time the pipe
+// may idle. Per KV step the issuer therefore commits three times (S0, S1 and
+// the stage it frees; O is committed once, after the last product: a
+// softmax warp knows the previous P V has finished when its next S arrives,
+// since that commit covers every earlier product) and waits three times (P0,
+// P1 and the stage two steps ahead).
 // Every wait is bounded; both CTAs meet at a cluster barrier before they free
 // tensor memory, after the MMA issuer has waited for its last MMAs.
-constexpr int P2_SLOTS = 8;
-constexpr int HALF_BYTES = TILE_BYTES / 2;  // 64 keys x 128 ch, or 128 keys x 64 ch (bf16)
-constexpr size_t P2_SMEM_BYTES = 1024 + 2 * TILE_BYTES + P2_SLOTS * HALF_BYTES + 256;
+constexpr int P2_STAGES = 4;
+constexpr int HALF_BYTES = TILE_BYTES / 2;   // 64 keys x 128 ch, or 128 keys x 64 ch (bf16)
+constexpr int STAGE2_BYTES = 2 * HALF_BYTES; // K half at 0, V half at HALF_BYTES
+constexpr size_t P2_SMEM_BYTES = 1024 + 2 * TILE_BYTES + P2_STAGES * STAGE2_BYTES + 256;
 
 enum BarP {
   BP_Q = 0,
   BP_FULL = 1,
-  BP_EMPTY = BP_FULL + P2_SLOTS,
-  BP_S = BP_EMPTY + P2_SLOTS,
+  BP_EMPTY = BP_FULL + P2_STAGES,
+  BP_S = BP_EMPTY + P2_STAGES,
   BP_P = BP_S + 2,
   BP_O = BP_P + 2,
-  BP_DRAIN = BP_O + 2,
+  BP_DRAIN = BP_O + 1,
   BP_NUM = BP_DRAIN + 1
 };
 static_assert(BP_NUM * 8 + 16 <= 256, "barrier region");
@@ -587,8 +596,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sKV = smem;                          // P2_SLOTS halves
-  uint8_t* sQ = smem + P2_SLOTS * HALF_BYTES;   // 2 tiles
+  uint8_t* sKV = smem;                             // P2_STAGES stages
+  uint8_t* sQ = smem + P2_STAGES * STAGE2_BYTES;   // 2 tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BP_NUM);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
@@ -604,8 +613,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < BP_NUM; ++i) {
       uint32_t count = 1;
-      // the even CTA's Q and slot barriers also take the odd CTA's relay
-      if (i == BP_Q || (i >= BP_FULL && i < BP_FULL + P2_SLOTS)) count = leader ? 2 : 1;
+      // the even CTA's Q and stage barriers also take the odd CTA's relay
+      if (i == BP_Q || (i >= BP_FULL && i < BP_FULL + P2_STAGES)) count = leader ? 2 : 1;
       if (i == BP_P || i == BP_P + 1) count = 8;  // one lane per softmax warp, both CTAs
       mbar_init(bar(i), count);
     }
@@ -633,33 +642,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         tma_load_2d(smem_u32(sQ + g * TILE_BYTES + BOX_BYTES), &tmQ, bar(BP_Q), col0 + 64, row);
       }
       int issued = 0;
-      for (int t = 0; t < 2 * n; ++t) {  // even t: K half of tile t/2, odd t: V half
-        const int slot = t % P2_SLOTS;
-        const uint32_t use = static_cast<uint32_t>(t / P2_SLOTS);
-        if (!mbar_wait_cluster(bar(BP_EMPTY + slot), (use & 1u) ^ 1u, a.err,
-                               ERR_WAIT_ATTN_PRODUCER))
+      for (int j = 0; j < n; ++j) {
+        const int st = j % P2_STAGES;
+        const uint32_t use = static_cast<uint32_t>(j / P2_STAGES);
+        if (!mbar_wait(bar(BP_EMPTY + st), (use & 1u) ^ 1u, a.err, ERR_WAIT_ATTN_PRODUCER))
           break;
-        const uint32_t full = bar(BP_FULL + slot);
-        mbar_arrive_expect_tx(full, HALF_BYTES);
-        const uint32_t dst = smem_u32(sKV + slot * HALF_BYTES);
-        const int key0 = (t >> 1) * BKV;
-        if ((t & 1) == 0) {
-          const int k_row = key0 + 64 * static_cast<int>(rank);
-          tma_load_2d(dst, &tmK, full, col0, k_row);
-          tma_load_2d(dst + HALF_BYTES / 2, &tmK, full, col0 + 64, k_row);
-        } else {
-          tma_load_2d(dst, &tmV, full, col0 + 64 * static_cast<int>(rank), key0);
-        }
-        issued = t + 1;
+        const uint32_t full = bar(BP_FULL + st);
+        mbar_arrive_expect_tx(full, STAGE2_BYTES);
+        const uint32_t dst = smem_u32(sKV + st * STAGE2_BYTES);
+        const int key0 = j * BKV;
+        const int k_row = key0 + 64 * static_cast<int>(rank);
+        tma_load_2d(dst, &tmK, full, col0, k_row);
+        tma_load_2d(dst + HALF_BYTES / 2, &tmK, full, col0 + 64, k_row);
+        tma_load_2d(dst + HALF_BYTES, &tmV, full, col0 + 64 * static_cast<int>(rank), key0);
+        issued = j + 1;
       }
       // No copy of this CTA may still be landing when it exits: wait, bounded,
-      // for Q and for the last load of every slot (long done in a normal run).
+      // for Q and for the last load of every stage (long done in a normal run).
       const uint64_t t0 = globaltimer_ns();
       const uint64_t lim = drain_limit_ns(a.err);
-      mbar_wait_cluster_drain(bar(BP_Q), 0u, t0, lim);
-      for (int t = issued > P2_SLOTS ? issued - P2_SLOTS : 0; t < issued; ++t)
-        mbar_wait_cluster_drain(bar(BP_FULL + t % P2_SLOTS),
-                                static_cast<uint32_t>(t / P2_SLOTS) & 1u, t0, lim);
+      mbar_wait_drain(bar(BP_Q), 0u, t0, lim);
+      for (int j = issued > P2_STAGES ? issued - P2_STAGES : 0; j < issued; ++j)
+        mbar_wait_drain(bar(BP_FULL + j % P2_STAGES), static_cast<uint32_t>(j / P2_STAGES) & 1u,
+                        t0, lim);
     }
   } else if (warp == 9) {
     if (leader && lane == 0) {
@@ -668,14 +673,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(2 * BQ, DH, true);
       const uint32_t kv_addr = smem_u32(sKV), q_addr = smem_u32(sQ);
       constexpr uint16_t kBoth = 3;
-      auto slot_of = [](int t) { return t % P2_SLOTS; };
-      auto wait_full = [&](int t) {
-        return mbar_wait_cluster(bar(BP_FULL + slot_of(t)),
-                                 static_cast<uint32_t>(t / P2_SLOTS) & 1u, a.err,
-                                 ERR_WAIT_ATTN_MMA);
+      auto stage_addr = [&](int j) { return kv_addr + (j % P2_STAGES) * STAGE2_BYTES; };
+      auto wait_full = [&](int j) {
+        return mbar_wait(bar(BP_FULL + j % P2_STAGES),
+                         static_cast<uint32_t>(j / P2_STAGES) & 1u, a.err, ERR_WAIT_ATTN_MMA);
       };
       auto qk = [&](int g, int j) {  // S_g = Q_g K_j^T over both CTAs' rows
-        const uint32_t k_addr = kv_addr + slot_of(2 * j) * HALF_BYTES;
+        const uint32_t k_addr = stage_addr(j);
         const uint32_t qa = q_addr + g * TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
@@ -687,58 +691,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         mma_commit_pair_mc(bar(BP_S + g), kBoth);
       };
       auto pv = [&](int g, int j) {  // O_g += P_g V_j
-        const uint32_t v_addr = kv_addr + slot_of(2 * j + 1) * HALF_BYTES;
+        const uint32_t v_addr = stage_addr(j) + HALF_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
           mma_ts_pair(tmem + 256 + g * 128, tmem + g * 128 + kk * 8,
                       sdesc_sw128(v_addr + kk * 2048, HALF_BYTES, 1024), idesc_pv,
                       (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_pair_mc(bar(BP_O + g), kBoth);
       };
-      bool ok = mbar_wait_cluster(bar(BP_Q), 0, a.err, ERR_WAIT_ATTN_MMA) && wait_full(0);
+      // At the top of step j, stage j + 1 has landed in both CTAs (stage j
+      // before it): each step waits for stage j + 2 right after issuing its
+      // first two products, while the pipe works through them.
+      bool ok = mbar_wait(bar(BP_Q), 0, a.err, ERR_WAIT_ATTN_MMA) && wait_full(0);
       if (ok) {
         tc_fence_after();
         qk(0, 0);
         qk(1, 0);
-        mma_commit_pair_mc(bar(BP_EMPTY + slot_of(0)), kBoth);
+        ok = n < 2 || wait_full(1);
       }
       for (int j = 0; ok && j < n; ++j) {
         const uint32_t par = static_cast<uint32_t>(j) & 1u;
-        if (!wait_full(2 * j + 1) ||
-            !mbar_wait_cluster(bar(BP_P), par, a.err, ERR_WAIT_ATTN_MMA))
-          break;
+        const bool more = j + 1 < n;
+        if (!mbar_wait(bar(BP_P), par, a.err, ERR_WAIT_ATTN_MMA)) break;
         tc_fence_after();
         pv(0, j);
-        const bool more = j + 1 < n;
-        if (more) {
-          if (!wait_full(2 * j + 2)) break;
-          tc_fence_after();
-          qk(0, j + 1);
-        }
-        if (!mbar_wait_cluster(bar(BP_P + 1), par, a.err, ERR_WAIT_ATTN_MMA)) break;
+        if (more) qk(0, j + 1);
+        if (j + 2 < n && !wait_full(j + 2)) break;
+        if (!mbar_wait(bar(BP_P + 1), par, a.err, ERR_WAIT_ATTN_MMA)) break;
         tc_fence_after();
         pv(1, j);
-        mma_commit_pair_mc(bar(BP_EMPTY + slot_of(2 * j + 1)), kBoth);
-        if (more) {
-          qk(1, j + 1);
-          mma_commit_pair_mc(bar(BP_EMPTY + slot_of(2 * j + 2)), kBoth);
-        }
+        mma_commit_pair_mc(bar(BP_EMPTY + j % P2_STAGES), kBoth);  // K_j and V_j consumed
+        if (more) qk(1, j + 1);
       }
+      // O of both groups is complete once every product issued so far is
+      mma_commit_pair_mc(bar(BP_O), kBoth);
       // Every MMA issued here must be done with both CTAs' shared and tensor
       // memory before either frees them: commit and wait, bounded.
       mma_commit_pair_mc(bar(BP_DRAIN), 1);
-      mbar_wait_cluster_drain(bar(BP_DRAIN), 0u, globaltimer_ns(), drain_limit_ns(a.err));
+      mbar_wait_drain(bar(BP_DRAIN), 0u, globaltimer_ns(), drain_limit_ns(a.err));
     } else if (!leader && lane == 0) {
       // ------------------------------------------------------------ relay
-      const uint32_t lead_q = mapa_shared(bar(BP_Q), 0);
-      if (mbar_wait_cluster(bar(BP_Q), 0, a.err, ERR_WAIT_ATTN_PRODUCER)) {
-        mbar_arrive_cluster(lead_q);
-        for (int t = 0; t < 2 * n; ++t) {
-          const int slot = t % P2_SLOTS;
-          if (!mbar_wait_cluster(bar(BP_FULL + slot), static_cast<uint32_t>(t / P2_SLOTS) & 1u,
-                                 a.err, ERR_WAIT_ATTN_PRODUCER))
+      if (mbar_wait(bar(BP_Q), 0, a.err, ERR_WAIT_ATTN_PRODUCER)) {
+        mbar_arrive_remote(mapa_shared(bar(BP_Q), 0));
+        for (int j = 0; j < n; ++j) {
+          const int st = j % P2_STAGES;
+          if (!mbar_wait(bar(BP_FULL + st), static_cast<uint32_t>(j / P2_STAGES) & 1u, a.err,
+                         ERR_WAIT_ATTN_PRODUCER))
             break;
-          mbar_arrive_cluster(mapa_shared(bar(BP_FULL + slot), 0));
+          mbar_arrive_remote(mapa_shared(bar(BP_FULL + st), 0));
         }
       }
     }
@@ -749,24 +748,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + tile * 128;
     const uint32_t tO = tmem + lane_base + 256 + tile * 128;
-    const uint32_t p_bar = mapa_shared(bar(BP_P + tile), 0);  // the even CTA's
+    const uint32_t p_bar_peer = mapa_shared(bar(BP_P + tile), 0);  // the even CTA's
     float m = -INFINITY, l = 0.f, m_keep = -INFINITY;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      if (!mbar_wait_cluster(bar(BP_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
-                             ERR_WAIT_ATTN_SOFTMAX)) {
+      if (!mbar_wait(bar(BP_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
+                     ERR_WAIT_ATTN_SOFTMAX)) {
         ok = false;
         break;
       }
       tc_fence_after();
       softmax_tile<false, false>(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l, 0.f, m_keep,
                                  true, nullptr, 0u, 0u, a.err, ok);
+      // P written (the tensor-memory stores waited for): one lane per warp
+      // tells the even CTA's MMA issuer
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(p_bar);
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(bar(BP_P + tile));
+        else
+          mbar_arrive_remote(p_bar_peer);
+      }
     }
-    if (ok && mbar_wait_cluster(bar(BP_O + tile), static_cast<uint32_t>(n - 1) & 1u, a.err,
-                                ERR_WAIT_ATTN_SOFTMAX)) {
+    if (ok && mbar_wait(bar(BP_O), 0u, a.err, ERR_WAIT_ATTN_SOFTMAX)) {
       tc_fence_after();
       const int row = p0 + 2 * BQ * tile + BQ * static_cast<int>(rank) + quarter * 32 + lane;
       store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L, nullptr);

@@ -120,53 +120,18 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
-// the peer's), releasing this thread's prior writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
+// Arrive on an mbarrier of the peer CTA, given by its shared::cluster address
+// (mapa_shared), with the default release at CTA scope. A cluster-scope
+// release here costs each arriving warp about a thousand cycles of memory
+// barrier; tensor-memory data handed over this way is ordered by the
+// tcgen05.wait / tcgen05.fence pair around the arrive and the wait instead.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Every thread of both CTAs of the cluster: all of them arrive, then wait.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// mbar_wait with cluster-scope acquire: for barriers that the peer CTA of a
-// pair arrives on (its threads, or tcgen05.commit multicast from the pair's
-// MMA issuer).
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const DevErr& e,
-                                                  uint32_t code) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
-      if (*(volatile uint32_t*)e.word != 0u) return false;
-      if (globaltimer_ns() - t0 > e.timeout_ns) {
-        atomicCAS(e.word, 0u, code);
-        return false;
-      }
-    }
-  }
-}
-__device__ __forceinline__ bool mbar_wait_cluster_drain(uint32_t bar, uint32_t parity,
-                                                        uint64_t t0, uint64_t limit_ns) {
-  while (!mbar_try_wait_cluster(bar, parity))
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  return true;
 }
 
 // ---------------------------------------------------------------- TMA
