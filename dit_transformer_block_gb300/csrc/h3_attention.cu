@@ -557,7 +557,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
 //     barrier of that group;
 //   warp 8: TMA producer of the CTA's own halves: its Q tiles once, then, per
 //     KV step, its K half and V half together into one 32 KB stage of a
-//     4-stage ring, on its own barriers;
+//     4-stage ring, on its own barriers (a stage is freed by group 1's
+//     softmax, below);
 //   warp 9: allocates tensor memory (both CTAs together); in the even CTA one
 //     lane issues the MMAs (order PV0(j), QK0(j+1), PV1(j), QK1(j+1)) and
 //     commits to the barriers of both CTAs; in the odd CTA one lane relays:
@@ -565,11 +566,12 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
 //     barrier of that stage, so the MMA issuer sees both halves.
 // The tensor pipe takes about one MMA ahead of its issuer, so every commit or
 // barrier wait of the issuing thread between two products is time the pipe
-// may idle. Per KV step the issuer therefore commits three times (S0, S1 and
-// the stage it frees; O is committed once, after the last product: a
-// softmax warp knows the previous P V has finished when its next S arrives,
-// since that commit covers every earlier product) and waits three times (P0,
-// P1 and the stage two steps ahead).
+// may idle. Per KV step the issuer therefore commits twice (S0 and S1) and
+// waits three times (P0, P1 and the stage two steps ahead). A commit covers
+// every product issued before it, so when a softmax warp sees its next S it
+// knows its previous P V has finished (O is committed once, after the last
+// product), and when group 1's softmax sees S1(j) every product that read
+// stage j - 1 has finished: one of its lanes in each CTA frees that stage.
 // Every wait is bounded; both CTAs meet at a cluster barrier before they free
 // tensor memory, after the MMA issuer has waited for its last MMAs.
 constexpr int P2_STAGES = 4;
@@ -719,7 +721,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         if (!mbar_wait(bar(BP_P + 1), par, a.err, ERR_WAIT_ATTN_MMA)) break;
         tc_fence_after();
         pv(1, j);
-        mma_commit_pair_mc(bar(BP_EMPTY + j % P2_STAGES), kBoth);  // K_j and V_j consumed
         if (more) qk(1, j + 1);
       }
       // O of both groups is complete once every product issued so far is
@@ -757,6 +758,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         ok = false;
         break;
       }
+      // S1(j) ready means every product issued before it has finished, among
+      // them all that read stage j - 1: one lane of each CTA frees that stage
+      // for its producer (no commit of the MMA issuer needed)
+      if (tile == 1 && quarter == 0 && lane == 0 && j > 0)
+        mbar_arrive(bar(BP_EMPTY + (j - 1) % P2_STAGES));
       tc_fence_after();
       softmax_tile<false, false>(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l, 0.f, m_keep,
                                  true, nullptr, 0u, 0u, a.err, ok);
