@@ -41,7 +41,7 @@ constexpr int B_BYTES = BN * BK * 2;        // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;              // two accumulators of BN columns
-constexpr int GROUP_M = 16;                 // raster: 16 M-blocks per N sweep
+constexpr int GROUP_M = 32;                 // raster: 32 M-blocks per N sweep
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
 
 struct GemmArgs {

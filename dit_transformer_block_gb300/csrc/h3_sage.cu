@@ -40,7 +40,10 @@ __device__ __forceinline__ int64_t bf16_fixed40(uint32_t bits, bool& in_range) {
   return (bits & 0x8000u) ? -mag : mag;
 }
 
-// grid (chunks, H), 128 threads: thread d owns channel d of head blockIdx.y.
+// grid (chunks, H), 128 threads. Thread t reads channels 8 (t % 16) ..
+// 8 (t % 16) + 7 of head blockIdx.y with 16-byte loads, on every eighth row of
+// the chunk starting at row t / 16; the eight row lanes of a channel are then
+// added exactly in shared memory and thread d writes channel d.
 // psum_i: the chunk's K sum in units of 2^-40 (at most 512 terms below 2^54,
 // so no overflow); psum_d: 0, or the chunk's K sum in FP64 when one of its
 // values lies outside the fixed-point range (psum_i is then 0).
@@ -49,31 +52,71 @@ __global__ void __launch_bounds__(DH)
                             const __nv_bfloat16* __restrict__ v, int64_t ld, int L,
                             int64_t* __restrict__ psum_i, double* __restrict__ psum_d,
                             float* __restrict__ pmax) {
-  const int chunk = blockIdx.x, h = blockIdx.y, d = threadIdx.x, H = gridDim.y;
+  __shared__ long long s_acc[8][DH];
+  __shared__ uint32_t s_vmax[8][DH];
+  __shared__ uint32_t s_in[8][DH];
+  const int chunk = blockIdx.x, h = blockIdx.y, H = gridDim.y;
+  const int cg = threadIdx.x & 15, rl = threadIdx.x >> 4;
   const int r0 = chunk * ST_ROWS, r1 = min(L, r0 + ST_ROWS);
-  const int64_t col = static_cast<int64_t>(h) * DH + d;
-  const uint16_t* kb = reinterpret_cast<const uint16_t*>(k);
-  int64_t acc = 0;
-  bool all_in = true;
-  float mx = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    const int64_t off = static_cast<int64_t>(r) * ld + col;
-    bool in;
-    acc += bf16_fixed40(kb[off], in);
-    all_in &= in;
-    mx = fmaxf(mx, fabsf(__bfloat162float(v[off])));
+  const int64_t col = static_cast<int64_t>(h) * DH + cg * 8;
+  int64_t acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint32_t vmax[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // |v| as bf16 bits (ordered as magnitudes)
+  uint32_t in = 0xFFu;                          // bit c: channel c stayed in range
+  int r = r0 + rl;
+  auto take = [&](uint4 kr, uint4 vr) {
+    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+    const uint32_t vw[4] = {vr.x, vr.y, vr.z, vr.w};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t kb = (c & 1) ? (kw[c >> 1] >> 16) : (kw[c >> 1] & 0xFFFFu);
+      const uint32_t vb = (c & 1) ? (vw[c >> 1] >> 16) : (vw[c >> 1] & 0xFFFFu);
+      bool ok;
+      acc[c] += bf16_fixed40(kb, ok);
+      in &= ok ? 0xFFu : ~(1u << c);
+      vmax[c] = max(vmax[c], vb & 0x7FFFu);
+    }
+  };
+  // two rows per iteration, all four loads first
+  for (; r + 8 < r1; r += 16) {
+    const int64_t o0 = static_cast<int64_t>(r) * ld + col, o1 = o0 + 8 * ld;
+    const uint4 k0 = __ldg(reinterpret_cast<const uint4*>(k + o0));
+    const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(v + o0));
+    const uint4 k1 = __ldg(reinterpret_cast<const uint4*>(k + o1));
+    const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(v + o1));
+    take(k0, v0);
+    take(k1, v1);
+  }
+  if (r < r1) {
+    const int64_t o0 = static_cast<int64_t>(r) * ld + col;
+    take(__ldg(reinterpret_cast<const uint4*>(k + o0)), __ldg(reinterpret_cast<const uint4*>(v + o0)));
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    s_acc[rl][cg * 8 + c] = acc[c];
+    s_vmax[rl][cg * 8 + c] = vmax[c];
+    s_in[rl][cg * 8 + c] = (in >> c) & 1u;
+  }
+  __syncthreads();
+  const int d = threadIdx.x;
+  int64_t sum = 0;
+  uint32_t vm = 0, all_in = 1;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    sum += s_acc[i][d];
+    vm = max(vm, s_vmax[i][d]);
+    all_in &= s_in[i][d];
   }
   double dsum = 0.0;
   if (!all_in) {  // rare: a value too small or too large for the fixed point
-    acc = 0;
-    for (int r = r0; r < r1; ++r)
-      dsum = __dadd_rn(dsum, static_cast<double>(
-                                 __bfloat162float(k[static_cast<int64_t>(r) * ld + col])));
+    sum = 0;
+    for (int rr = r0; rr < r1; ++rr)
+      dsum = __dadd_rn(dsum, static_cast<double>(__bfloat162float(
+                                 k[static_cast<int64_t>(rr) * ld + static_cast<int64_t>(h) * DH + d])));
   }
   const int64_t o = (static_cast<int64_t>(chunk) * H + h) * DH + d;
-  psum_i[o] = acc;
+  psum_i[o] = sum;
   psum_d[o] = dsum;
-  pmax[o] = mx;
+  pmax[o] = __uint_as_float(vm << 16);
 }
 
 // grid H, 128 threads: combine the chunks, mean = sum / L in FP64, rounded

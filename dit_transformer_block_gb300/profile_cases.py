@@ -1,6 +1,6 @@
 """Small, fixed cases for ncu captures of the library's kernels.
 
-    python -m dit_transformer_block_gb300.profile_cases [attention] [gemm] [elementwise] [fp8]
+    python -m dit_transformer_block_gb300.profile_cases [attention] [gemm] [elementwise] [fp8] [sage]
 
 Each selected kernel runs twice on inputs larger than L2 (129 MB) but a few
 hundred MB in total, so that an `ncu --set full -k <kernel> -s 1 -c 1`
@@ -15,6 +15,8 @@ capture of the second launch ends within a minute or two:
               modulation/LN/residual on 16384 x 5376
   fp8         FP8 GEMM (QKV shape, M = 8192), per-row FP8 quantisation of
               8192 x 5376, SAGE quantisation and FP8 attention at S = L = 16384
+  sage        SAGE quantisation alone (K mean, V absmax, Q/K tile and V codes)
+              at S = L = 16384, 42 heads
 """
 from __future__ import annotations
 
@@ -26,7 +28,7 @@ from dit_transformer_block_gb300 import build, h3
 
 
 def main(argv):
-    which = set(argv) or {"attention", "gemm", "elementwise", "fp8"}
+    which = set(argv) or {"attention", "gemm", "elementwise", "fp8", "sage"}
     build.build()
     h3.lib()
     dev = "cuda"
@@ -85,6 +87,10 @@ def main(argv):
         oa = torch.empty_like(qa)
         ops = h3.sage_quantize(qa, ka, va, S)
         runs.append(lambda: h3.attention_fp8(ops, oa, S))
+    if "sage" in which:
+        S = 16384
+        qs, ks, vs = rnd(S, 42, 128), rnd(S, 42, 128), rnd(S, 42, 128)
+        runs.append(lambda: h3.sage_quantize(qs, ks, vs, S))
     for _ in range(2):
         for fn in runs:
             fn()
