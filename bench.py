@@ -682,7 +682,7 @@ def run_ours(a):
     ew_ms = stage_ms[0] + stage_ms[4]
     attn_tf = work["attn_flop"] / attn_ms / 1e9
     gemm_tf = work["gemm_flop"] / gemm_ms / 1e9
-    traffic = profile_traffic("h3_attention.cu", "attention_full_size.md")
+    traffic = profile_traffic("h3_attention.cu", "attention_pair_small_case.md")
     stages_roofline = {}
     for name, t, (bound, amount, unit) in zip(h3.STAGE_NAMES, stage_ms,
                                               stage_work(S, L, D, H, Dh, F)):
@@ -727,7 +727,7 @@ def run_ours(a):
         "elementwise_gbs": round(work["elementwise_bytes"] / ew_ms / 1e6, 1),
         "stages_ms": {n: round(t, 3) for n, t in zip(h3.STAGE_NAMES, stage_ms)},
         "stages_roofline": stages_roofline,
-        "roofline": {"bound": "tensor", "kernel": "attention_kernel",
+        "roofline": {"bound": "tensor", "kernel": "attention_pair_kernel",
                      "achieved": round(attn_tf, 1), "peak": pk["bf16_sustained"],
                      "unit": "TFLOP/s", "frac": round(attn_tf / pk["bf16_sustained"], 3),
                      "traffic": traffic,
