@@ -172,7 +172,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
     if ((threadIdx.x & 31) == 0) flags[quarter] = warp_skip;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(vote_bar);
-    if (!mbar_wait(vote_bar, vote_parity, err, ERR_WAIT_ATTN_SOFTMAX)) {
+    if (!mbar_wait_warp(vote_bar, vote_parity, err, ERR_WAIT_ATTN_SOFTMAX)) {
       ok = false;
       return true;
     }
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       sq_tile = (qt * BQ < a.L) ? __ldg(a.sq + qt * a.H + blockIdx.y) : 0.f;
     }
     for (int j = 0; j < n; ++j) {
-      if (!mbar_wait(bar(B2_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
+      if (!mbar_wait_warp(bar(B2_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
                      ERR_WAIT_ATTN_SOFTMAX)) {
         ok = false;
         break;
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B2_P + tile));
     }
-    if (ok && mbar_wait(bar(B2_O + tile), static_cast<uint32_t>(n - 1) & 1u, a.err,
+    if (ok && mbar_wait_warp(bar(B2_O + tile), static_cast<uint32_t>(n - 1) & 1u, a.err,
                         ERR_WAIT_ATTN_SOFTMAX)) {
       tc_fence_after();
       const int row = q0 + tile * BQ + quarter * 32 + lane;
@@ -753,7 +753,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
     float m = -INFINITY, l = 0.f, m_keep = -INFINITY;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      if (!mbar_wait(bar(BP_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
+      if (!mbar_wait_warp(bar(BP_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
                      ERR_WAIT_ATTN_SOFTMAX)) {
         ok = false;
         break;
@@ -777,7 +777,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
           mbar_arrive_remote(p_bar_peer);
       }
     }
-    if (ok && mbar_wait(bar(BP_O), 0u, a.err, ERR_WAIT_ATTN_SOFTMAX)) {
+    if (ok && mbar_wait_warp(bar(BP_O), 0u, a.err, ERR_WAIT_ATTN_SOFTMAX)) {
       tc_fence_after();
       const int row = p0 + 2 * BQ * tile + BQ * static_cast<int>(rank) + quarter * 32 + lane;
       store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L, nullptr);

@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, a, mb, nb);
-      if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, a.err, ERR_WAIT_GEMM_EPILOGUE)) break;
+      if (!mbar_wait_warp(smem_u32(&tfull[acc]), acc_phase, a.err, ERR_WAIT_GEMM_EPILOGUE)) break;
       tc_fence_after();
       const int row = mb * BM + quarter * 32 + lane;
       const bool row_ok = row < a.M;

@@ -90,6 +90,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const D
   }
 }
 
+// mbar_wait for the lanes of a warp that go on to warp-collective
+// instructions (tcgen05.ld / st .sync.aligned): every lane waits, and the
+// result is the same for the whole warp (false if any lane's wait failed),
+// so that no lane leaves while the others enter a collective.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const DevErr& e,
+                                               uint32_t code) {
+  const bool ok = mbar_wait(bar, parity, e, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Waits for a phase that copies this CTA issued will complete, ignoring the
 // device error word (so a CTA that is leaving because of an error still lets
 // its own copies land first), until limit_ns after t0. Returns whether the
