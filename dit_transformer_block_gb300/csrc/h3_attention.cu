@@ -289,7 +289,10 @@ __device__ __forceinline__ void store_o_row(uint32_t tO, float l, __nv_bfloat16*
 //   * warp 8: TMA producer (Q0, Q1 once; K_j and V_j through a 4-slot ring);
 //   * warp 9: TMEM allocator (512 columns: S0, S1, O0, O1) and MMA issuer in
 //     the order PV0(j), QK0(j+1), PV1(j), QK1(j+1), so each tile's softmax has
-//     the other tile's two MMAs (1024 tensor clocks) to finish in;
+//     the other tile's two MMAs (1024 tensor clocks) to finish in; it commits
+//     S0 and S1 once per KV step and O once at the end, and tile 1's softmax
+//     frees the K/V slots (a commit covers every earlier product, so S1(j)
+//     ready means K_j and V_{j-1} have been read);
 //   * P_i is written over S_i; QK_i(j+1) is issued right behind PV_i(j) (MMAs
 //     of one thread execute in issue order).
 // Each K/V tile is read from shared memory by two Q tiles, which halves the
@@ -447,14 +450,12 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
                      (j > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        mma_commit(bar(B2_O + i));
       };
       bool ok = mbar_wait(bar(B2_Q), 0, a.err, ERR_WAIT_ATTN_MMA) && wait_full(0);
       if (ok) {
         tc_fence_after();
         qk(0, 0);
         qk(1, 0);
-        mma_commit(bar(B2_KV_EMPTY + slot_of(0)));
       }
       for (int j = 0; ok && j < n; ++j) {
         const uint32_t par = static_cast<uint32_t>(j) & 1u;
@@ -470,12 +471,11 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         if (!mbar_wait(bar(B2_P + 1), par, a.err, ERR_WAIT_ATTN_MMA)) break;
         tc_fence_after();
         pv(1, j);
-        mma_commit(bar(B2_KV_EMPTY + slot_of(2 * j + 1)));
-        if (more) {
-          qk(1, j + 1);
-          mma_commit(bar(B2_KV_EMPTY + slot_of(2 * j + 2)));
-        }
+        if (more) qk(1, j + 1);
       }
+      // O of both tiles is complete once every product issued so far is
+      mma_commit(bar(B2_O));
+      mma_commit(bar(B2_O + 1));
       if (SKIP && a.kept != nullptr && ok) {
         for (int i = 0; i < 2; ++i) {
           const int qt = blockIdx.x * 2 + i;
@@ -510,6 +510,12 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         ok = false;
         break;
       }
+      // S1(j) covers every product issued before it: K_j and V_{j-1} have
+      // been read by both tiles, so one lane of tile 1 frees their slots
+      if (tile == 1 && quarter == 0 && lane == 0) {
+        mbar_arrive(bar(B2_KV_EMPTY + (2 * j) % KV_SLOTS));
+        if (j > 0) mbar_arrive(bar(B2_KV_EMPTY + (2 * j - 1) % KV_SLOTS));
+      }
       tc_fence_after();
       float mul = a.scale_log2;
       // a zero tile scale would turn masked (-inf) scores into NaN: keep the
@@ -522,8 +528,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B2_P + tile));
     }
-    if (ok && mbar_wait_warp(bar(B2_O + tile), static_cast<uint32_t>(n - 1) & 1u, a.err,
-                        ERR_WAIT_ATTN_SOFTMAX)) {
+    if (ok && mbar_wait_warp(bar(B2_O + tile), 0u, a.err, ERR_WAIT_ATTN_SOFTMAX)) {
       tc_fence_after();
       const int row = q0 + tile * BQ + quarter * 32 + lane;
       store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L,
