@@ -549,52 +549,143 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
 // over 512 query rows as two M = 256 groups: group g covers rows
 // p0 + 256 g .. p0 + 256 g + 255, and CTA r holds rows p0 + 256 g + 128 r ..
 // + 127 of it (its query tile g). Every product is one M = 256 MMA issued by
-// one thread of the even CTA; each CTA supplies its own 128 rows of A (Q, or P
-// from its tensor memory) and half of B: keys 64 r .. 64 r + 63 of K_j for
+// the MMA warp of the even CTA; each CTA supplies its own 128 rows of A (Q, or
+// P from its shared memory) and half of B: keys 64 r .. 64 r + 63 of K_j for
 // S = Q K^T, head channels 64 r .. 64 r + 63 of V_j for O += P V. So each SM
 // reads half of every K/V tile from its own shared memory and receives the
-// other half from its peer: per KV step a CTA loads 32 KB instead of 64 KB
-// and its tensor core reads 128 KB of shared memory instead of 192 KB, for
-// the same FLOPs.
+// other half from its peer.
+//
+// P goes to shared memory (bf16, laid out like a Q tile), not over S in
+// tensor memory, so S_g is free as soon as the softmax has read it into
+// registers: QK_g(j+1) is issued while the softmax of tile j still runs, and
+// the chain from one S_g to the next is no longer softmax + both products of
+// the group + the hand-offs, which left the tensor pipe idle for part of every
+// KV step. The softmax of a group forms its whole P row in registers and
+// waits for the group's previous P V only before storing it (or before an O
+// rescale), so that product overlaps the exponentials.
 // Roles per CTA (320 threads):
-//   warps 0-3 / 4-7: softmax of the CTA's query tile 0 / 1 (as in the one-CTA
-//     kernel); after each tile one lane per warp arrives on the even CTA's P
-//     barrier of that group;
+//   warps 0-3 / 4-7: softmax of the CTA's query tile 0 / 1: S from tensor
+//     memory into registers, one lane per warp tells the even CTA's MMA warp
+//     that S is free, then the tile's P is written to shared memory and one
+//     lane per warp tells the MMA warp that P is ready;
 //   warp 8: TMA producer of the CTA's own halves: its Q tiles once, then, per
 //     KV step, its K half and V half together into one 32 KB stage of a
-//     4-stage ring, on its own barriers (a stage is freed by group 1's
-//     softmax, below);
-//   warp 9: allocates tensor memory (both CTAs together); in the even CTA one
-//     lane issues the MMAs (order PV0(j), QK0(j+1), PV1(j), QK1(j+1)) and
-//     commits to the barriers of both CTAs; in the odd CTA one lane relays:
-//     each time one of its own stages has landed it arrives on the even CTA's
-//     barrier of that stage, so the MMA issuer sees both halves.
-// The tensor pipe takes about one MMA ahead of its issuer, so every commit or
-// barrier wait of the issuing thread between two products is time the pipe
-// may idle. Per KV step the issuer therefore commits twice (S0 and S1) and
-// waits three times (P0, P1 and the stage two steps ahead). A commit covers
-// every product issued before it, so when a softmax warp sees its next S it
-// knows its previous P V has finished (O is committed once, after the last
-// product), and when group 1's softmax sees S1(j) every product that read
-// stage j - 1 has finished: one of its lanes in each CTA frees that stage.
+//     3-stage ring, on its own barriers;
+//   warp 9: allocates tensor memory (both CTAs together; S0, S1, O0, O1); in
+//     the even CTA the whole warp runs the issue loop and one elected lane
+//     issues each MMA and commit (both CTAs' barriers); in the odd CTA one
+//     lane relays: each time one of its own stages has landed it arrives on
+//     the even CTA's barrier of that stage, so the MMA issuer sees both halves.
+// A stage is freed by a commit after the last product that reads it (PV1).
 // Every wait is bounded; both CTAs meet at a cluster barrier before they free
 // tensor memory, after the MMA issuer has waited for its last MMAs.
-constexpr int P2_STAGES = 4;
+constexpr int P2_STAGES = 3;
 constexpr int HALF_BYTES = TILE_BYTES / 2;   // 64 keys x 128 ch, or 128 keys x 64 ch (bf16)
 constexpr int STAGE2_BYTES = 2 * HALF_BYTES; // K half at 0, V half at HALF_BYTES
-constexpr size_t P2_SMEM_BYTES = 1024 + 2 * TILE_BYTES + P2_STAGES * STAGE2_BYTES + 256;
+// stages, Q tiles, P tiles, barriers (227 KB is the per-CTA limit)
+constexpr size_t P2_SMEM_BYTES =
+    1024 + P2_STAGES * STAGE2_BYTES + 2 * TILE_BYTES + 2 * TILE_BYTES + 256;
+static_assert(P2_SMEM_BYTES <= 227 * 1024, "pair kernel shared memory");
 
 enum BarP {
   BP_Q = 0,
-  BP_FULL = 1,
-  BP_EMPTY = BP_FULL + P2_STAGES,
-  BP_S = BP_EMPTY + P2_STAGES,
-  BP_P = BP_S + 2,
-  BP_O = BP_P + 2,
+  BP_FULL = 1,                    // stage landed (both CTAs' halves, via the relay)
+  BP_EMPTY = BP_FULL + P2_STAGES, // stage read by every product (MMA commit)
+  BP_S = BP_EMPTY + P2_STAGES,    // S_g written (MMA commit)
+  BP_SFREE = BP_S + 2,            // S_g read by the softmax (8 warp arrivals)
+  BP_P = BP_SFREE + 2,            // P_g written (8 warp arrivals)
+  BP_PVD = BP_P + 2,              // P_g V_j done (MMA commit)
+  BP_O = BP_PVD + 2,
   BP_DRAIN = BP_O + 1,
   BP_NUM = BP_DRAIN + 1
 };
 static_assert(BP_NUM * 8 + 16 <= 256, "barrier region");
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// The online softmax of softmax_tile<false, false> (its exact pass) for one
+// KV tile, with the row's 128 scores already in registers (sr) and P written
+// to shared memory: p_row = the P tile's shared-memory address + 128 * row,
+// r7 = row & 7 (the 128-byte swizzle of a K-major bf16 tile: 16-byte chunk c
+// of a row sits at chunk (c & 7) ^ r7 of box c >> 3). The same operations in
+// the same order as softmax_tile's exact pass, so P, m and l are bitwise
+// those of the one-CTA kernel. The whole P row is formed in registers first
+// and stored last: wait_pv() (the previous P V of this tile has finished with
+// P and O) is called only before the stores, or before an O rescale, so that
+// wait overlaps the exponentials. Returns false when wait_pv() fails.
+template <class WaitPV>
+__device__ __forceinline__ bool softmax_tile_smem(uint32_t (&sr)[128], uint32_t p_row, uint32_t r7,
+                                                  uint32_t tO, int valid, bool o_live,
+                                                  float scale_log2, float& m, float& l,
+                                                  WaitPV&& wait_pv) {
+  if (valid < BKV) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c >= valid) sr[c] = 0xff800000u;
+  }
+  float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 128; c += 8) {
+    ma = max3f(ma, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+    mb = max3f(mb, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+    mc = max3f(mc, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+    md = max3f(md, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+  }
+  const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
+  bool pv_done = !o_live;  // the first tile has no earlier product
+  if (__any_sync(0xffffffffu, mx > m + RESCALE_THRESHOLD)) {
+    const float m_new = fmaxf(m, mx);
+    const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
+    l *= alpha;
+    if (o_live) {
+      if (!wait_pv()) return false;
+      pv_done = true;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t ov[16];
+        tmem_ld16(tO + c * 16, ov);
+        tmem_ld_wait();
+        tmem_reg_fence(ov);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+        tmem_st16(tO + c * 16, ov);
+      }
+      tmem_st_wait();
+    }
+    m = m_new;
+  }
+  const float neg_m = -m;
+  float la = 0.f, lb = 0.f, lc = 0.f, ld = 0.f;
+  uint32_t pk[64];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float x0, x1;
+      ffma2_bc(x0, x1, __uint_as_float(sr[c * 32 + 2 * i]), __uint_as_float(sr[c * 32 + 2 * i + 1]),
+               scale_log2, neg_m);
+      const float p0 = ex2_approx(x0);
+      const float p1 = ex2_approx(x1);
+      if (i & 1)
+        fadd2(lc, ld, p0, p1);
+      else
+        fadd2(la, lb, p0, p1);
+      pk[c * 16 + i] = pack_bf16x2(p0, p1);
+    }
+  }
+  l += (la + lb) + (lc + ld);
+  if (!pv_done && !wait_pv()) return false;
+#pragma unroll
+  for (uint32_t chunk = 0; chunk < 16; ++chunk)  // keys 8 chunk .. 8 chunk + 7
+    st_shared_v4(p_row + (chunk >> 3) * BOX_BYTES + (((chunk & 7u) ^ r7) << 4), pk[4 * chunk],
+                 pk[4 * chunk + 1], pk[4 * chunk + 2], pk[4 * chunk + 3]);
+  return true;
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
     attention_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -605,7 +696,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sKV = smem;                             // P2_STAGES stages
   uint8_t* sQ = smem + P2_STAGES * STAGE2_BYTES;   // 2 tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * TILE_BYTES);
+  uint8_t* sP = sQ + 2 * TILE_BYTES;               // 2 tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BP_NUM);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -622,7 +714,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       uint32_t count = 1;
       // the even CTA's Q and stage barriers also take the odd CTA's relay
       if (i == BP_Q || (i >= BP_FULL && i < BP_FULL + P2_STAGES)) count = leader ? 2 : 1;
-      if (i == BP_P || i == BP_P + 1) count = 8;  // one lane per softmax warp, both CTAs
+      // one lane per softmax warp of the group, both CTAs
+      if (i >= BP_SFREE && i < BP_PVD) count = 8;
       mbar_init(bar(i), count);
     }
     fence_mbar_init();
@@ -674,67 +767,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
                         t0, lim);
     }
   } else if (warp == 9) {
-    if (leader && lane == 0) {
+    if (leader) {
       // -------------------------------------------------------- MMA issuer
+      // The whole warp runs the loop; one elected lane issues. Descriptors
+      // are a base plus a constant offset (start address field, in 16-byte
+      // units; shared-memory addresses stay below 2^18, so no carry).
       constexpr uint32_t idesc_qk = idesc_bf16_f32(2 * BQ, BKV, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(2 * BQ, DH, true);
-      const uint32_t kv_addr = smem_u32(sKV), q_addr = smem_u32(sQ);
+      const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dp = sdesc_sw128(smem_u32(sP), 16, 1024);
+      const uint64_t dk = sdesc_sw128(smem_u32(sKV), 16, 1024);
+      const uint64_t dv = sdesc_sw128(smem_u32(sKV) + HALF_BYTES, HALF_BYTES, 1024);
       constexpr uint16_t kBoth = 3;
-      auto stage_addr = [&](int j) { return kv_addr + (j % P2_STAGES) * STAGE2_BYTES; };
+      auto wait = [&](int b, uint32_t parity) {
+        return mbar_wait_warp(bar(b), parity, a.err, ERR_WAIT_ATTN_MMA);
+      };
       auto wait_full = [&](int j) {
-        return mbar_wait(bar(BP_FULL + j % P2_STAGES),
-                         static_cast<uint32_t>(j / P2_STAGES) & 1u, a.err, ERR_WAIT_ATTN_MMA);
+        return wait(BP_FULL + j % P2_STAGES, static_cast<uint32_t>(j / P2_STAGES) & 1u);
+      };
+      // 16-byte offset of K step kk (16 elements) in a K-major 128-byte-swizzled tile
+      auto kmaj = [](int kk, int box_bytes) {
+        return static_cast<uint32_t>(((kk >> 2) * box_bytes + (kk & 3) * 32) >> 4);
       };
       auto qk = [&](int g, int j) {  // S_g = Q_g K_j^T over both CTAs' rows
-        const uint32_t k_addr = stage_addr(j);
-        const uint32_t qa = q_addr + g * TILE_BYTES;
+        const uint64_t kd = dk + static_cast<uint32_t>((j % P2_STAGES) * (STAGE2_BYTES >> 4));
+        const uint64_t qd = dq + static_cast<uint32_t>(g * (TILE_BYTES >> 4));
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t q_off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          const uint32_t k_off = (kk >> 2) * (HALF_BYTES / 2) + (kk & 3) * 32;
-          mma_ss_pair(tmem + g * 128, sdesc_sw128(qa + q_off, 16, 1024),
-                      sdesc_sw128(k_addr + k_off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_pair_mc(bar(BP_S + g), kBoth);
+        for (int kk = 0; kk < DH / 16; ++kk)
+          mma_ss_pair_el(tmem + g * 128, qd + kmaj(kk, BOX_BYTES), kd + kmaj(kk, HALF_BYTES / 2),
+                         idesc_qk, kk > 0 ? 1u : 0u);
+        mma_commit_pair_mc_el(bar(BP_S + g), kBoth);
       };
       auto pv = [&](int g, int j) {  // O_g += P_g V_j
-        const uint32_t v_addr = stage_addr(j) + HALF_BYTES;
+        const uint64_t vd = dv + static_cast<uint32_t>((j % P2_STAGES) * (STAGE2_BYTES >> 4));
+        const uint64_t pd = dp + static_cast<uint32_t>(g * (TILE_BYTES >> 4));
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_ts_pair(tmem + 256 + g * 128, tmem + g * 128 + kk * 8,
-                      sdesc_sw128(v_addr + kk * 2048, HALF_BYTES, 1024), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ss_pair_el(tmem + 256 + g * 128, pd + kmaj(kk, BOX_BYTES), vd + kk * (2048 >> 4),
+                         idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_pair_mc_el(bar(BP_PVD + g), kBoth);
       };
-      // At the top of step j, stage j + 1 has landed in both CTAs (stage j
-      // before it): each step waits for stage j + 2 right after issuing its
-      // first two products, while the pipe works through them.
-      bool ok = mbar_wait(bar(BP_Q), 0, a.err, ERR_WAIT_ATTN_MMA) && wait_full(0);
+      bool ok = wait(BP_Q, 0u) && wait_full(0);
       if (ok) {
         tc_fence_after();
         qk(0, 0);
         qk(1, 0);
-        ok = n < 2 || wait_full(1);
       }
+      // Per KV step: QK0(j+1) as soon as the softmax has read S0(j), then
+      // PV0(j), QK1(j+1), PV1(j); a stage is free once PV1 of it is done.
       for (int j = 0; ok && j < n; ++j) {
         const uint32_t par = static_cast<uint32_t>(j) & 1u;
         const bool more = j + 1 < n;
-        if (!mbar_wait(bar(BP_P), par, a.err, ERR_WAIT_ATTN_MMA)) break;
+        if (more) {
+          if (!wait_full(j + 1) || !wait(BP_SFREE, par)) break;
+          tc_fence_after();
+          qk(0, j + 1);
+        }
+        if (!wait(BP_P, par)) break;
         tc_fence_after();
         pv(0, j);
-        if (more) qk(0, j + 1);
-        if (j + 2 < n && !wait_full(j + 2)) break;
-        if (!mbar_wait(bar(BP_P + 1), par, a.err, ERR_WAIT_ATTN_MMA)) break;
+        if (more) {
+          if (!wait(BP_SFREE + 1, par)) break;
+          tc_fence_after();
+          qk(1, j + 1);
+        }
+        if (!wait(BP_P + 1, par)) break;
         tc_fence_after();
         pv(1, j);
-        if (more) qk(1, j + 1);
+        mma_commit_pair_mc_el(bar(BP_EMPTY + j % P2_STAGES), kBoth);  // K_j, V_j read
       }
       // O of both groups is complete once every product issued so far is
-      mma_commit_pair_mc(bar(BP_O), kBoth);
+      mma_commit_pair_mc_el(bar(BP_O), kBoth);
       // Every MMA issued here must be done with both CTAs' shared and tensor
       // memory before either frees them: commit and wait, bounded.
-      mma_commit_pair_mc(bar(BP_DRAIN), 1);
+      mma_commit_pair_mc_el(bar(BP_DRAIN), 1);
       mbar_wait_drain(bar(BP_DRAIN), 0u, globaltimer_ns(), drain_limit_ns(a.err));
-    } else if (!leader && lane == 0) {
+    } else if (lane == 0) {
       // ------------------------------------------------------------ relay
       if (mbar_wait(bar(BP_Q), 0, a.err, ERR_WAIT_ATTN_PRODUCER)) {
         mbar_arrive_remote(mapa_shared(bar(BP_Q), 0));
@@ -754,38 +862,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + tile * 128;
     const uint32_t tO = tmem + lane_base + 256 + tile * 128;
-    const uint32_t p_bar_peer = mapa_shared(bar(BP_P + tile), 0);  // the even CTA's
-    float m = -INFINITY, l = 0.f, m_keep = -INFINITY;
+    const uint32_t row = static_cast<uint32_t>(quarter * 32 + lane);
+    const uint32_t p_row = smem_u32(sP + tile * TILE_BYTES) + row * 128;
+    // one lane per warp tells the even CTA's MMA warp
+    auto tell = [&](int b) {
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(bar(b));
+        else
+          mbar_arrive_remote(mapa_shared(bar(b), 0));
+      }
+    };
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait_warp(bar(BP_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
-                     ERR_WAIT_ATTN_SOFTMAX)) {
+                          ERR_WAIT_ATTN_SOFTMAX)) {
         ok = false;
         break;
       }
-      // S1(j) ready means every product issued before it has finished, among
-      // them all that read stage j - 1: one lane of each CTA frees that stage
-      // for its producer (no commit of the MMA issuer needed)
-      if (tile == 1 && quarter == 0 && lane == 0 && j > 0)
-        mbar_arrive(bar(BP_EMPTY + (j - 1) % P2_STAGES));
       tc_fence_after();
-      softmax_tile<false, false>(tS, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l, 0.f, m_keep,
-                                 true, nullptr, 0u, 0u, a.err, ok);
-      // P written (the tensor-memory stores waited for): one lane per warp
-      // tells the even CTA's MMA issuer
+      uint32_t sr[128];
+      {
+        uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+        uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+        uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+        uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+        tmem_ld32(tS + 0, c0);
+        tmem_ld32(tS + 32, c1);
+        tmem_ld32(tS + 64, c2);
+        tmem_ld32(tS + 96, c3);
+        tmem_ld_wait();
+        tmem_reg_fence(sr);
+      }
+      // S read: the next Q K^T of this group may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if (leader)
-          mbar_arrive(bar(BP_P + tile));
-        else
-          mbar_arrive_remote(p_bar_peer);
+      tell(BP_SFREE + tile);
+      // P_g V_{j-1} must be done before P_g is overwritten and O_g rescaled
+      auto wait_pv = [&]() {
+        const bool done = mbar_wait_warp(bar(BP_PVD + tile), static_cast<uint32_t>(j - 1) & 1u,
+                                         a.err, ERR_WAIT_ATTN_SOFTMAX);
+        tc_fence_after();
+        return done;
+      };
+      if (!softmax_tile_smem(sr, p_row, row & 7u, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l,
+                             wait_pv)) {
+        ok = false;
+        break;
       }
+      // P written (generic-proxy stores, made visible to the tensor core's
+      // reads) and any O rescale stored: tell the MMA warp
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      tell(BP_P + tile);
     }
     if (ok && mbar_wait_warp(bar(BP_O), 0u, a.err, ERR_WAIT_ATTN_SOFTMAX)) {
       tc_fence_after();
-      const int row = p0 + 2 * BQ * tile + BQ * static_cast<int>(rank) + quarter * 32 + lane;
-      store_o_row(tO, l, a.o + static_cast<int64_t>(row) * a.ld_out + col0, row < a.L, nullptr);
+      const int orow = p0 + 2 * BQ * tile + BQ * static_cast<int>(rank) + static_cast<int>(row);
+      store_o_row(tO, l, a.o + static_cast<int64_t>(orow) * a.ld_out + col0, orow < a.L, nullptr);
     }
   }
 
