@@ -933,6 +933,314 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// FP8 (SAGE) attention, one CTA per pair of 128-row query tiles of one head,
+// with the same hand-off as the pair kernel: the softmax reads S_i into
+// registers and frees it at once, so QK_i(j+1) overlaps the softmax of tile
+// j; P_i (E4M3 codes) is formed in registers and stored to shared memory after
+// PV_i(j-1) has finished with it; every product is an SS kind::f8f6f4 MMA.
+//   warps 0-3 / 4-7: softmax of query tile 0 / 1 (thread = query row = TMEM
+//     lane of S_i and O_i);
+//   warp 8: TMA producer: Q0, Q1 once, then K_j and V_j (128 rows of 128
+//     codes, 16 KB each) together into one 32 KB stage of a 4-stage ring;
+//   warp 9: allocates TMEM (S0, S1, O0, O1); the whole warp runs the issue
+//     loop, one elected lane issues: per KV step QK0(j+1), PV0(j), QK1(j+1),
+//     PV1(j), then a commit frees stage j.
+// Scores of (query tile t, key tile j, head h) are scaled by sq[t H + h] *
+// sk[j H + h] (with the softmax scale); output channel d by sv[h 128 + d].
+constexpr int F8_TILE = BQ * DH;          // 16 KB: one tile of E4M3 codes
+constexpr int F8_STAGES = 4;
+constexpr int F8_STAGE_BYTES = 2 * F8_TILE;  // K_j at 0, V_j at F8_TILE
+constexpr size_t F8_SMEM_BYTES = 1024 + F8_STAGES * F8_STAGE_BYTES + 2 * F8_TILE + 2 * F8_TILE + 256;
+static_assert(F8_SMEM_BYTES <= 227 * 1024, "fp8 attention shared memory");
+
+enum BarF8 {
+  BF_Q = 0,
+  BF_FULL = 1,
+  BF_EMPTY = BF_FULL + F8_STAGES,
+  BF_S = BF_EMPTY + F8_STAGES,  // S_i written (MMA commit)
+  BF_SFREE = BF_S + 2,          // S_i read by the softmax (4 warp arrivals)
+  BF_P = BF_SFREE + 2,          // P_i written (4 warp arrivals)
+  BF_PVD = BF_P + 2,            // P_i V_j done (MMA commit)
+  BF_O = BF_PVD + 2,
+  BF_DRAIN = BF_O + 1,
+  BF_NUM = BF_DRAIN + 1
+};
+static_assert(BF_NUM * 8 + 16 <= 256, "barrier region");
+
+// softmax_tile<true, false>'s arithmetic for one KV tile (integer running max
+// within 1 of the true one, P carried as 224 P, E4M3 codes), with the row's
+// scores already in registers (sr) and the codes stored to shared memory at
+// p_row = the P tile's address + 128 * row, 16-byte chunk c of the row at
+// chunk c ^ r7 (r7 = row & 7: the 128-byte swizzle of a K-major tile). The
+// codes, m and l are bitwise those of softmax_tile<true, false>. wait_pv() is
+// called before the stores, or before an O rescale. Returns false when it
+// fails.
+template <class WaitPV>
+__device__ __forceinline__ bool softmax_tile_f8_smem(uint32_t (&sr)[128], uint32_t p_row,
+                                                     uint32_t r7, uint32_t tO, int valid,
+                                                     bool o_live, float scale_log2, float& m,
+                                                     float& l, WaitPV&& wait_pv) {
+  if (valid < BKV) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c >= valid) sr[c] = 0xff800000u;
+  }
+  float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 128; c += 8) {
+    ma = max3f(ma, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+    mb = max3f(mb, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+    mc = max3f(mc, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+    md = max3f(md, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+  }
+  const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
+  bool pv_done = !o_live;
+  if (__any_sync(0xffffffffu, mx > m + 1.0f)) {
+    const float m_new = ceilf(fmaxf(m, mx));
+    const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
+    l *= alpha;
+    if (o_live) {
+      if (!wait_pv()) return false;
+      pv_done = true;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t ov[16];
+        tmem_ld16(tO + c * 16, ov);
+        tmem_ld_wait();
+        tmem_reg_fence(ov);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+        tmem_st16(tO + c * 16, ov);
+      }
+      tmem_st_wait();
+    }
+    m = m_new;
+  }
+  const float neg_m = kLog2P8Scale - m;
+  float la = 0.f, lb = 0.f, lc = 0.f, ld = 0.f;
+  uint32_t pk[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float x0, x1, x2, x3;
+    ffma2_bc(x0, x1, __uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]), scale_log2,
+             neg_m);
+    ffma2_bc(x2, x3, __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]), scale_log2,
+             neg_m);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+    fadd2(la, lb, p0, p1);
+    fadd2(lc, ld, p2, p3);
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
+    pk[i] = lo | (hi << 16);
+  }
+  l += (la + lb) + (lc + ld);
+  if (!pv_done && !wait_pv()) return false;
+#pragma unroll
+  for (uint32_t c = 0; c < 8; ++c)  // keys 16 c .. 16 c + 15
+    st_shared_v4(p_row + ((c ^ r7) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+  return true;
+}
+
+__global__ void __launch_bounds__(Q2_THREADS, 1)
+    attention_f8_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sKV = smem;                                // F8_STAGES stages
+  uint8_t* sQ = smem + F8_STAGES * F8_STAGE_BYTES;    // 2 tiles
+  uint8_t* sP = sQ + 2 * F8_TILE;                     // 2 tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * F8_TILE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BF_NUM);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q0 = blockIdx.x * 2 * BQ;
+  const int col0 = blockIdx.y * DH;  // byte column of the head's codes
+  const int n = a.num_kv;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < BF_NUM; ++i) mbar_init(bar(i), (i >= BF_SFREE && i < BF_PVD) ? 4 : 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(bar(BF_Q), 2 * F8_TILE);
+      for (int i = 0; i < 2; ++i)
+        tma_load_2d(smem_u32(sQ + i * F8_TILE), &tmQ, bar(BF_Q), col0, q0 + i * BQ);
+      int issued = 0;
+      for (int j = 0; j < n; ++j) {
+        const int st = j % F8_STAGES;
+        const uint32_t use = static_cast<uint32_t>(j / F8_STAGES);
+        if (!mbar_wait(bar(BF_EMPTY + st), (use & 1u) ^ 1u, a.err, ERR_WAIT_ATTN_PRODUCER)) break;
+        const uint32_t full = bar(BF_FULL + st);
+        mbar_arrive_expect_tx(full, F8_STAGE_BYTES);
+        const uint32_t dst = smem_u32(sKV + st * F8_STAGE_BYTES);
+        tma_load_2d(dst, &tmK, full, col0, j * BKV);
+        tma_load_2d(dst + F8_TILE, &tmV, full, col0, j * BKV);
+        issued = j + 1;
+      }
+      // no copy of this CTA may still be landing when it exits
+      const uint64_t t0 = globaltimer_ns();
+      const uint64_t lim = drain_limit_ns(a.err);
+      mbar_wait_drain(bar(BF_Q), 0u, t0, lim);
+      for (int j = issued > F8_STAGES ? issued - F8_STAGES : 0; j < issued; ++j)
+        mbar_wait_drain(bar(BF_FULL + j % F8_STAGES), static_cast<uint32_t>(j / F8_STAGES) & 1u,
+                        t0, lim);
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc_qk = idesc_e4m3_f32(BQ, BKV);
+    constexpr uint32_t idesc_pv = idesc_e4m3_f32(BQ, DH) | (1u << 16);  // V MN-major
+    const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dp = sdesc_sw128(smem_u32(sP), 16, 1024);
+    const uint64_t dk = sdesc_sw128(smem_u32(sKV), 16, 1024);
+    const uint64_t dv = sdesc_sw128(smem_u32(sKV) + F8_TILE, F8_TILE, 1024);
+    auto wait = [&](int b, uint32_t parity) {
+      return mbar_wait_warp(bar(b), parity, a.err, ERR_WAIT_ATTN_MMA);
+    };
+    auto wait_full = [&](int j) {
+      return wait(BF_FULL + j % F8_STAGES, static_cast<uint32_t>(j / F8_STAGES) & 1u);
+    };
+    auto stage = [](int j) { return static_cast<uint32_t>((j % F8_STAGES) * (F8_STAGE_BYTES >> 4)); };
+    auto qk = [&](int i, int j) {  // S_i = Q_i K_j^T; 32 codes (32 bytes) per instruction
+      const uint64_t qd = dq + static_cast<uint32_t>(i * (F8_TILE >> 4));
+      const uint64_t kd = dk + stage(j);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss_f8_el(tmem + i * 128, qd + kk * 2, kd + kk * 2, idesc_qk, kk > 0 ? 1u : 0u);
+      mma_commit_el(bar(BF_S + i));
+    };
+    auto pv = [&](int i, int j) {  // O_i += P_i V_j; 32 keys (32 rows of V, 4 KB) per instruction
+      const uint64_t pd = dp + static_cast<uint32_t>(i * (F8_TILE >> 4));
+      const uint64_t vd = dv + stage(j);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss_f8_el(tmem + 256 + i * 128, pd + kk * 2, vd + kk * (4096 >> 4), idesc_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_el(bar(BF_PVD + i));
+    };
+    bool ok = wait(BF_Q, 0u) && wait_full(0);
+    if (ok) {
+      tc_fence_after();
+      qk(0, 0);
+      qk(1, 0);
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      const uint32_t par = static_cast<uint32_t>(j) & 1u;
+      const bool more = j + 1 < n;
+      if (more) {
+        if (!wait_full(j + 1) || !wait(BF_SFREE, par)) break;
+        tc_fence_after();
+        qk(0, j + 1);
+      }
+      if (!wait(BF_P, par)) break;
+      tc_fence_after();
+      pv(0, j);
+      if (more) {
+        if (!wait(BF_SFREE + 1, par)) break;
+        tc_fence_after();
+        qk(1, j + 1);
+      }
+      if (!wait(BF_P + 1, par)) break;
+      tc_fence_after();
+      pv(1, j);
+      mma_commit_el(bar(BF_EMPTY + j % F8_STAGES));  // K_j, V_j read
+    }
+    mma_commit_el(bar(BF_O));
+    // every MMA must be done with shared and tensor memory before the CTA
+    // frees them: commit and wait, bounded
+    mma_commit_el(bar(BF_DRAIN));
+    mbar_wait_drain(bar(BF_DRAIN), 0u, globaltimer_ns(), drain_limit_ns(a.err));
+  } else {
+    // ---------------------------------------------------------- softmax
+    const int tile = warp >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + tile * 128;
+    const uint32_t tO = tmem + lane_base + 256 + tile * 128;
+    const uint32_t row = static_cast<uint32_t>(quarter * 32 + lane);
+    const uint32_t p_row = smem_u32(sP + tile * F8_TILE) + row * 128;
+    const int qt = blockIdx.x * 2 + tile;  // 128-row query tile index
+    const float sq_tile = (qt * BQ < a.L) ? __ldg(a.sq + qt * a.H + blockIdx.y) : 0.f;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait_warp(bar(BF_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
+                          ERR_WAIT_ATTN_SOFTMAX)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[128];
+      {
+        uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+        uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+        uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+        uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+        tmem_ld32(tS + 0, c0);
+        tmem_ld32(tS + 32, c1);
+        tmem_ld32(tS + 64, c2);
+        tmem_ld32(tS + 96, c3);
+        tmem_ld_wait();
+        tmem_reg_fence(sr);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BF_SFREE + tile));  // S_i read
+      // a zero tile scale would turn masked (-inf) scores into NaN: keep the
+      // multiplier positive
+      const float mul =
+          fmaxf(a.scale_log2 * sq_tile * __ldg(a.sk + j * a.H + blockIdx.y), 1e-30f);
+      auto wait_pv = [&]() {  // P_i V_{j-1} done with P_i and O_i
+        const bool done = mbar_wait_warp(bar(BF_PVD + tile), static_cast<uint32_t>(j - 1) & 1u,
+                                         a.err, ERR_WAIT_ATTN_SOFTMAX);
+        tc_fence_after();
+        return done;
+      };
+      if (!softmax_tile_f8_smem(sr, p_row, row & 7u, tO, a.L - j * BKV, j > 0, mul, m, l,
+                                wait_pv)) {
+        ok = false;
+        break;
+      }
+      fence_proxy_async_smem();  // the codes, for the tensor core's reads
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BF_P + tile));
+    }
+    if (ok && mbar_wait_warp(bar(BF_O), 0u, a.err, ERR_WAIT_ATTN_SOFTMAX)) {
+      tc_fence_after();
+      const int orow = q0 + tile * BQ + static_cast<int>(row);
+      store_o_row(tO, l, a.o + static_cast<int64_t>(orow) * a.ld_out + col0, orow < a.L,
+                  a.sv + blockIdx.y * DH);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 template <bool F8, bool SKIP>
@@ -987,7 +1295,9 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
 h3_status launch_attention_fp8(const void* qc, const void* kc, const void* vc, int64_t ld_codes,
                                const float* sq, const float* sk, const float* sv, void* o,
                                int64_t ld_out, int L, int H, float scale, cudaStream_t s) {
-  h3_status st = set_attention_smem<true, false>();
+  static std::atomic<bool> done[64];
+  h3_status st = set_smem_limit(done, attention_f8_kernel, F8_SMEM_BYTES,
+                                "attention (fp8): set shared memory size");
   if (st != H3_OK) return st;
   AttnArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
@@ -1005,9 +1315,8 @@ h3_status launch_attention_fp8(const void* qc, const void* kc, const void* vc, i
   if ((st = make_tmap_u8_2d(&tq, qc, width, L, ld_codes, 128, BQ)) != H3_OK) return st;
   if ((st = make_tmap_u8_2d(&tk, kc, width, L, ld_codes, 128, BKV)) != H3_OK) return st;
   if ((st = make_tmap_u8_2d(&tv, vc, width, L, ld_codes, 128, BKV)) != H3_OK) return st;
-  const size_t smem = 1024 + (2 + KV_SLOTS) * (TILE_BYTES / 2) + 256;
   dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
-  attention_kernel<true, false><<<grid, Q2_THREADS, smem, s>>>(tq, tk, tv, a);
+  attention_f8_kernel<<<grid, Q2_THREADS, F8_SMEM_BYTES, s>>>(tq, tk, tv, a);
   return cuda_fail(cudaGetLastError(), "attention (fp8) launch");
 }
 
