@@ -574,15 +574,21 @@ def sage_quantize(q, k, v, L: int, tile: int = 128):
     return dict(qc=qc, sq=sq, kc=kc, sk=sk, vc=vc, sv=sv[0], k_mean=k_mean)
 
 
-def _sage_weights(ops, h, rows, L, scale, tile):
-    """Softmax weights p = 2^(z - max z) of head h for the given query rows
-    (exact row maximum), float64 [len(rows), L]."""
+def _sage_logits(ops, h, rows, L, scale, tile):
+    """Base-2 logits z = (Q codes . K codes) * sq * sk * scale / ln 2 of head h
+    for the given query rows against the L valid keys, float64 [len(rows), L]."""
     qc, kc = ops["qc"], ops["kc"]
     sq = ops["sq"].astype(np.float64)
     sk = ops["sk"].astype(np.float64)
     key_tile = np.arange(L) // tile
     s = (qc[rows, h, :] @ kc[:L, h, :].T) * sq[rows // tile, h][:, None] * sk[key_tile, h][None, :]
-    z = s * scale / np.log(2.0)
+    return s * scale / np.log(2.0)
+
+
+def _sage_weights(ops, h, rows, L, scale, tile):
+    """Softmax weights p = 2^(z - max z) of head h for the given query rows
+    (exact row maximum), float64 [len(rows), L]."""
+    z = _sage_logits(ops, h, rows, L, scale, tile)
     return np.exp2(z - z.max(axis=1, keepdims=True))
 
 
@@ -600,6 +606,76 @@ def attention_sage(ops, L: int, scale: float, rows=None, tile: int = 128):
         pc = round_e4m3(_E4M3_MAX * p)
         out[:, h, :] = (pc @ vc[:L, h, :]) * sv[h][None, :] / (_E4M3_MAX * p.sum(axis=1, keepdims=True))
     return round_bf16(out)
+
+
+def _sage_skip_tiles(ops, L, scale, eps, tile):
+    """Skip-Softmax on the FP8 logits ([vLLM-Omni H3 blog] section 4.3, Fig. 6:
+    Skip-Softmax uses the QK result to leave out whole softmax and P x V
+    tiles; the tile rule is the one of attention_skip): for each 128-row query
+    tile and head, walk the key tiles in order, keeping for every row the
+    maximum logit over the tiles kept so far; a key tile is left out when
+    every row's maximum logit in it lies more than log2(1/eps) below that
+    running maximum (eps = 0: nothing is left out; the first key tile is
+    always kept). Yields (h, query tile index, rows, kept tile mask, kept key
+    columns, logits of the rows against the kept keys)."""
+    H = ops["vc"].shape[1]
+    nq = nk = (L + tile - 1) // tile
+    thresh = np.inf if eps <= 0 else np.log2(1.0 / eps)
+    for h in range(H):
+        for qi in range(nq):
+            rows = np.arange(qi * tile, min(L, (qi + 1) * tile))
+            z = _sage_logits(ops, h, rows, L, scale, tile)
+            m = np.full(len(rows), -np.inf)
+            keep = np.zeros(nk, bool)
+            for kj in range(nk):
+                c0, c1 = kj * tile, min(L, (kj + 1) * tile)
+                tmax = z[:, c0:c1].max(axis=1)
+                if np.all(tmax < m - thresh):
+                    continue
+                keep[kj] = True
+                m = np.maximum(m, tmax)
+            cols = np.flatnonzero(np.repeat(keep, tile)[:L])
+            yield h, qi, rows, keep, cols, z[:, cols]
+
+
+def attention_sage_skip(ops, L: int, scale: float, eps: float, tile: int = 128):
+    """SAGE attention with Skip-Softmax: the key tiles _sage_skip_tiles keeps
+    go through attention_sage's steps (weights against the row maximum of the
+    kept keys, E4M3 codes of 448 p, the sum of the unrounded weights); the
+    left-out tiles take no part. Returns (out [L, H, Dh] bf16 values,
+    kept [n_qtiles, H, n_ktiles] bool)."""
+    vc = ops["vc"]
+    sv = ops["sv"].astype(np.float64)
+    H, Dh = vc.shape[1], vc.shape[2]
+    nt = (L + tile - 1) // tile
+    out = np.empty((L, H, Dh))
+    kept = np.zeros((nt, H, nt), bool)
+    for h, qi, rows, keep, cols, z in _sage_skip_tiles(ops, L, scale, eps, tile):
+        kept[qi, h] = keep
+        p = np.exp2(z - z.max(axis=1, keepdims=True))
+        pc = round_e4m3(_E4M3_MAX * p)
+        out[rows, h, :] = ((pc @ vc[cols, h, :]) * sv[h][None, :]
+                           / (_E4M3_MAX * p.sum(axis=1, keepdims=True)))
+    return round_bf16(out), kept
+
+
+def sage_skip_error_terms(ops, L: int, scale: float, eps: float, tile: int = 128):
+    """sage_error_terms over the key tiles attention_sage_skip keeps, for
+    every valid row: (a1, a0, v2, u2), each [L, H, Dh] float64."""
+    vc = ops["vc"]
+    sv = ops["sv"].astype(np.float64)
+    H, Dh = vc.shape[1], vc.shape[2]
+    a1 = np.empty((L, H, Dh)); a0 = np.empty_like(a1)
+    v2 = np.empty_like(a1); u2 = np.empty_like(a1)
+    for h, qi, rows, keep, cols, z in _sage_skip_tiles(ops, L, scale, eps, tile):
+        p = np.exp2(z - z.max(axis=1, keepdims=True))
+        tot = p.sum(axis=1, keepdims=True)
+        w = np.abs(vc[cols, h, :] * sv[h][None, :])
+        a1[rows, h, :] = (p @ w) / tot
+        a0[rows, h, :] = w.sum(axis=0)[None, :] / tot
+        v2[rows, h, :] = ((p * p) @ (w * w)) / (tot * tot)
+        u2[rows, h, :] = (w * w).sum(axis=0)[None, :] / (tot * tot)
+    return a1, a0, v2, u2
 
 
 def sage_error_terms(ops, L: int, scale: float, rows=None, tile: int = 128):

@@ -872,3 +872,148 @@ def _sage_weights_ceil_max(ops, h, rows, L, scale, tile):
 def test_planted_sage_mistake_is_caught(mut):
     with pytest.raises(AssertionError):
         check_sage(_mutant(**mut))
+
+
+# ------------------------------------------- SAGE attention with Skip-Softmax
+def _hand_ops(logits, tile=128):
+    """SAGE operands whose base-2 logits (at scale ln 2) are given directly:
+    logits [R, L] for R query rows, one head. Head dim 2: q = (1, b_i),
+    k = (a_j, c_j) so that z_ij = a_j + b_i c_j; here b_i c_j carries the
+    per-row part (zero unless a pin sets it). V codes are a fixed ramp."""
+    R, L = logits.shape
+    nt = (max(R, L) + tile - 1) // tile
+    qc = np.zeros((max(R, L), 1, 2)); qc[:, 0, 0] = 1.0
+    kc = np.zeros((L, 1, 2)); kc[:, 0, 0] = logits[0]
+    extra = logits - logits[0][None, :]
+    rows, cols = np.nonzero(extra)
+    for i, j in zip(rows, cols):  # one per-row exception per key at most
+        qc[i, 0, 1] = 1.0
+        kc[j, 0, 1] = extra[i, j]
+    vc = np.zeros((L, 1, 3))
+    vc[:, 0, 0] = np.arange(L) % 7 - 3.0
+    vc[:, 0, 1] = np.arange(L) % 5 - 2.0
+    vc[:, 0, 2] = 1.0
+    return dict(qc=qc, sq=np.ones((nt, 1), np.float32), kc=kc, sk=np.ones((nt, 1), np.float32),
+                vc=vc, sv=np.ones((1, 3), np.float32))
+
+
+def check_sage_skip(o):
+    r = rng(90)
+    # eps = 0 leaves nothing out: exactly attention_sage
+    L, H, Dh = 300, 2, 32
+    q = bf16_values(r.standard_normal((L, H, Dh)))
+    k = bf16_values(r.standard_normal((L, H, Dh)))
+    v = bf16_values(r.standard_normal((L, H, Dh)))
+    ops = o.sage_quantize(q, k, v, L)
+    out0, kept0 = o.attention_sage_skip(ops, L, Dh ** -0.5, 0.0)
+    assert kept0.all() and np.array_equal(out0, o.attention_sage(ops, L, Dh ** -0.5))
+    t0 = o.sage_skip_error_terms(ops, L, Dh ** -0.5, 0.0)
+    for x, y in zip(t0, o.sage_error_terms(ops, L, Dh ** -0.5)):
+        assert np.allclose(x, y, rtol=1e-12, atol=0)
+    # hand-built logits (scale ln 2: the logit is the dot product): three key
+    # tiles; tiles 0 and 2 in [0, 1], tile 1 in [-5.5, -4.6], i.e. 5.6 or
+    # more below the running maximum of the kept tiles (tile 0's maximum is
+    # above 0.99). eps = 1/16 (threshold 4) leaves tile 1 out for every query
+    # tile (a threshold of log2(16) / ln 2 = 5.77 would keep it), and the
+    # result is attention_sage over the other 256 keys; the left-out weights
+    # (up to 2^-5.6) are large enough that counting them would move the output
+    # by more than 1 %.
+    L = 384
+    base = np.concatenate([r.uniform(0, 1, 128), r.uniform(-5.5, -4.6, 128), r.uniform(0, 1, 128)])
+    assert base[:128].max() - base[128:256].max() < 5.77
+    logits = np.repeat(base[None], L, axis=0)
+    ops = _hand_ops(logits)
+    out, kept = o.attention_sage_skip(ops, L, math.log(2.0), 2.0 ** -4)
+    assert np.array_equal(kept, np.repeat(np.array([[[True, False, True]]]), 3, axis=0))
+    keep = np.r_[0:128, 256:384]
+    red = dict(ops, kc=ops["kc"][keep], vc=ops["vc"][keep], sk=ops["sk"][[0, 2]])
+    want = o.attention_sage(red, 256, math.log(2.0), rows=np.arange(L))
+    assert np.allclose(out, want, rtol=2 ** -8, atol=1e-12)
+    # the V rows of the left-out tile do not matter; in dense attention they do
+    vc_v = ops["vc"].copy()
+    vc_v[128:256] = 50.0
+    ops_v = dict(ops, vc=vc_v)
+    assert np.array_equal(o.attention_sage_skip(ops_v, L, math.log(2.0), 2.0 ** -4)[0], out)
+    assert np.max(np.abs(o.attention_sage(ops_v, L, math.log(2.0)) - out)) > 0.1
+    # the error terms are those of the kept keys
+    terms = o.sage_skip_error_terms(ops, L, math.log(2.0), 2.0 ** -4)
+    for x, y in zip(terms, o.sage_error_terms(red, 256, math.log(2.0), rows=np.arange(L))):
+        assert np.allclose(x, y, rtol=1e-9, atol=0)
+    # the threshold is log2(1/eps): tile 1 exactly 3.5 below tile 0's maximum
+    # (its own maximum; every row the same) is kept at eps = 1/16
+    base_b = base.copy()
+    base_b[128:256] = base[:128].max() - 3.5
+    _, kept_b = o.attention_sage_skip(_hand_ops(np.repeat(base_b[None], L, axis=0)), L,
+                                      math.log(2.0), 2.0 ** -4)
+    assert kept_b.all()
+    # a tile is left out only when every row of the query tile falls below:
+    # row 5 sees key 200 at logit 4, so query tile 0 keeps key tile 1
+    logits_c = logits.copy()
+    logits_c[5, 200] = 4.0
+    _, kept_c = o.attention_sage_skip(_hand_ops(logits_c), L, math.log(2.0), 2.0 ** -4)
+    assert kept_c[0, 0, 1] and not kept_c[1, 0, 1] and not kept_c[2, 0, 1]
+    # the first key tile is always kept, however far below the later ones
+    base_d = base[[*range(128, 256), *range(0, 128), *range(256, 384)]]
+    _, kept_d = o.attention_sage_skip(_hand_ops(np.repeat(base_d[None], L, axis=0)), L,
+                                      math.log(2.0), 2.0 ** -4)
+    assert kept_d[:, :, 0].all() and kept_d[:, :, 1:].all()
+
+
+def test_sage_skip():
+    check_sage_skip(O)
+
+
+def _skip_tiles_natural_log(ops, L, scale, eps, tile):
+    # threshold ln(1/eps) instead of log2(1/eps)
+    yield from O._sage_skip_tiles(ops, L, scale, eps ** math.log(2.0), tile)
+
+
+def _skip_tiles_log_ratio(ops, L, scale, eps, tile):
+    # threshold log2(1/eps) / ln 2 (the logits' base mixed up the other way)
+    yield from O._sage_skip_tiles(ops, L, scale, eps ** (1 / math.log(2.0)), tile)
+
+
+def _skip_tiles_any_row(ops, L, scale, eps, tile):
+    # leave a tile out when ANY row falls below (instead of every row)
+    H = ops["vc"].shape[1]
+    nt = (L + tile - 1) // tile
+    thresh = np.inf if eps <= 0 else np.log2(1.0 / eps)
+    for h in range(H):
+        for qi in range(nt):
+            rows = np.arange(qi * tile, min(L, (qi + 1) * tile))
+            z = O._sage_logits(ops, h, rows, L, scale, tile)
+            m = np.full(len(rows), -np.inf)
+            keep = np.zeros(nt, bool)
+            for kj in range(nt):
+                tmax = z[:, kj * tile:min(L, (kj + 1) * tile)].max(axis=1)
+                if np.any(tmax < m - thresh):
+                    continue
+                keep[kj] = True
+                m = np.maximum(m, tmax)
+            cols = np.flatnonzero(np.repeat(keep, tile)[:L])
+            yield h, qi, rows, keep, cols, z[:, cols]
+
+
+def _sage_skip_sum_all(ops, L, scale, eps, tile=128):
+    # the row sum over every key, left-out tiles included
+    vc, sv = ops["vc"], ops["sv"].astype(np.float64)
+    nt = (L + tile - 1) // tile
+    out = np.empty((L,) + vc.shape[1:])
+    kept = np.zeros((nt, vc.shape[1], nt), bool)
+    for h, qi, rows, keep, cols, z in O._sage_skip_tiles(ops, L, scale, eps, tile):
+        kept[qi, h] = keep
+        zall = O._sage_logits(ops, h, rows, L, scale, tile)
+        p = np.exp2(z - z.max(axis=1, keepdims=True))
+        pall = np.exp2(zall - z.max(axis=1, keepdims=True))
+        out[rows, h, :] = (O.round_e4m3(448.0 * p) @ vc[cols, h, :]) * sv[h][None, :] \
+            / (448.0 * pall.sum(axis=1, keepdims=True))
+    return O.round_bf16(out), kept
+
+
+@pytest.mark.parametrize("mut", [dict(_sage_skip_tiles=_skip_tiles_natural_log),
+                                 dict(_sage_skip_tiles=_skip_tiles_log_ratio),
+                                 dict(_sage_skip_tiles=_skip_tiles_any_row),
+                                 dict(attention_sage_skip=_sage_skip_sum_all)])
+def test_planted_sage_skip_mistake_is_caught(mut):
+    with pytest.raises(AssertionError):
+        check_sage_skip(_mutant(**mut))
