@@ -362,6 +362,8 @@ def measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk):
       attention     attention alone on its full-size workload (unit-RMS q, k)
       sage_quantize, attention_fp8   the FP8 (SAGE) operands and attention on
                     the same inputs
+      skip_softmax  Skip-Softmax (BF16 and with SAGE FP8) on the same inputs
+                    and on frame-local inputs, with the kept-tile fraction
       fp8_block     the block with online FP8 projections
       stack4        4 blocks in one h3_stack_forward call (fused boundaries)
       frames_to_u8  output preparation of the 10 s, 1344 x 768 clip"""
@@ -410,7 +412,36 @@ def measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk):
                             "achieved_gbs": round(L * H * 128 * 9 / ms / 1e6, 1)}
     ms = timeit(lambda: h3.attention_fp8(ops, o_at, L), 3)
     out["attention_fp8"] = {"ms": round(ms, 3), "tflops_dense_equivalent": round(flop / ms / 1e9, 1)}
-    del at, o_at, ops
+    # Skip-Softmax (eps 1e-3) on the same inputs (no tile falls far enough
+    # below to be left out: the cost of the vote), then on frame-local inputs
+    # (frames of 1,024 rows, seed 5) with and without it, BF16 and FP8
+    nq = (L + 127) // 128
+    kept = torch.empty(nq, H, dtype=torch.int32, device=o_at.device)
+    eps = 1e-3
+    skip = {"eps": eps}
+    ms = timeit(lambda: h3.attention_fp8_skip(ops, o_at, L, skip_eps=eps, kept=kept), 3)
+    skip["fp8_unit_rms"] = {"ms": round(ms, 3),
+                            "kept_fraction": round(kept.sum().item() / (nq * H * nq), 4)}
+    del at, ops
+    loc = I.frame_local_attention_inputs(S, L, H, 128, frame=1024, seed=5,
+                                         device=inp["resid"].device)
+    skip["workload_local"] = ("q = n + 16 e, k = n' + 16 e (n, n' ~ N(0,1), e a random unit "
+                              "direction per 1,024-row frame and head), v ~ N(0,1), bf16 "
+                              "[58816, 42, 128], seed 5")
+    ms = timeit(lambda: h3.attention_varlen(loc["q"], loc["k"], loc["v"], o_at, L), 3)
+    skip["bf16_local_dense_ms"] = round(ms, 3)
+    ms = timeit(lambda: h3.attention_varlen_skip(loc["q"], loc["k"], loc["v"], o_at, L,
+                                                 skip_eps=eps, kept=kept), 3)
+    skip["bf16_local"] = {"ms": round(ms, 3),
+                          "kept_fraction": round(kept.sum().item() / (nq * H * nq), 4)}
+    ops = h3.sage_quantize(loc["q"], loc["k"], loc["v"], L)
+    ms = timeit(lambda: h3.attention_fp8(ops, o_at, L), 3)
+    skip["fp8_local_dense_ms"] = round(ms, 3)
+    ms = timeit(lambda: h3.attention_fp8_skip(ops, o_at, L, skip_eps=eps, kept=kept), 3)
+    skip["fp8_local"] = {"ms": round(ms, 3),
+                         "kept_fraction": round(kept.sum().item() / (nq * H * nq), 4)}
+    out["skip_softmax"] = skip
+    del loc, o_at, ops, kept
     r = inp["resid"].clone()
     w8 = h3.quantize_block_weights_fp8(inp)
     ws8 = torch.empty(h3.block_workspace_bytes_fp8(cfg), dtype=torch.uint8, device=r.device)

@@ -386,6 +386,30 @@ h3_status h3_attention_fp8(const void* qc, const void* kc, const void* vc, const
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+h3_status h3_attention_fp8_skip(const void* qc, const void* kc, const void* vc, const float* sq,
+                                const float* sk, const float* sv, void* o, int S, int L, int H,
+                                int Dh, float softmax_scale, float skip_eps, int32_t* kept_tiles,
+                                h3_stream_t stream) {
+  clear_error();
+  H3_REQUIRE(skip_eps >= 0.f && skip_eps < 1.f, H3_ERR_INVALID_ARG,
+             "skip_eps=%g must be in [0, 1)", static_cast<double>(skip_eps));
+  h3_status st = check_rows(S, L);
+  if (st != H3_OK) return st;
+  H3_REQUIRE(qc && kc && vc && sq && sk && sv && o, H3_ERR_INVALID_ARG,
+             "a required pointer is NULL");
+  H3_REQUIRE(Dh == 128, H3_ERR_UNSUPPORTED, "head_dim %d unsupported (128 only)", Dh);
+  H3_REQUIRE(H > 0 && H <= 65535, H3_ERR_INVALID_ARG, "H=%d", H);
+  H3_REQUIRE(softmax_scale > 0.f, H3_ERR_INVALID_ARG, "softmax_scale must be > 0");
+  H3_REQUIRE(aligned16(qc) && aligned16(kc) && aligned16(vc) && aligned16(o), H3_ERR_MISALIGNED,
+             "codes and o must be 16-byte aligned");
+  H3_REQUIRE(reinterpret_cast<uintptr_t>(kept_tiles) % 4 == 0, H3_ERR_MISALIGNED,
+             "kept_tiles must be 4-byte aligned");
+  if (L == 0) return H3_OK;
+  const int64_t ld = static_cast<int64_t>(H) * Dh;
+  return launch_attention_fp8(qc, kc, vc, ld, sq, sk, sv, o, ld, L, H, softmax_scale,
+                              reinterpret_cast<cudaStream_t>(stream), skip_eps, kept_tiles);
+}
+
 h3_status h3_swiglu(const void* gate_up, void* out, int S, int L, int F, h3_stream_t stream) {
   clear_error();
   h3_status st = check_rows(S, L);

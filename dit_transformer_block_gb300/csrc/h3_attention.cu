@@ -68,24 +68,62 @@ struct AttnArgs {
 // columns. valid = keys of this tile that are < L (>= BKV: none masked).
 // o_live: O already holds earlier tiles (so raising the max rescales it).
 // m, l: running max (times scale_log2) and row sum. Warp-collective.
-// Skip-Softmax (SKIP): the four warps of a query tile vote; when every valid
-// row's tile maximum lies more than skip_log2 below m_keep, the row's exact
-// running maximum over the key tiles kept so far (rows >= L, row_valid
-// false, vote to skip), the tile is skipped (no exp2, no P; flags[quarter]
-// tells the MMA warp to leave out its P V product) and the function returns
-// true; otherwise m_keep takes in the tile's maximum. The vote is exchanged
-// through flags and the mbarrier vote_bar (one arrival per warp, phase
-// vote_parity), waited on with the usual limit; if that wait runs out, ok is
-// cleared and the function returns at once.
+// Skip-Softmax (SKIP): the four warps of a query tile vote (skip_vote, step
+// vote_tag); when every valid row's tile maximum lies more than skip_log2
+// below m_keep, the row's exact running maximum over the key tiles kept so
+// far (rows >= L, row_valid false, vote to skip), the tile is skipped (no
+// exp2, no P; the posts in flags tell the MMA warp to leave out its P V
+// product) and the function returns true; otherwise m_keep takes in the
+// tile's maximum. If the vote's wait runs out, ok is cleared and the function
+// returns at once.
 // F8: P is written as E4M3 codes (four per column, 32 columns) and the
 // running max is kept an integer, so every P is an exact power-of-two multiple
 // of the P against any other integer reference.
+// Skip-Softmax vote of the four warps of a query tile on one KV tile (step
+// vote_tag): each warp posts 2 * vote_tag + (every row of the warp votes to
+// skip) in flags[quarter]. A warp that keeps the tile is done (one keeping
+// warp keeps it); a warp that votes to skip reads the other three posts until
+// all carry this step (bounded: on a timeout or another CTA's error, ok is
+// cleared). Returns whether the tile is kept. The MMA warp reads the same
+// posts (bit 0) after the tile's P barrier. A post is not overwritten before
+// every warp has read it: flags alternate between two slots by step parity,
+// and a warp reaches step j + 2 only after all four have taken S(j + 1).
+__device__ __forceinline__ bool skip_vote(bool row_skip, volatile uint32_t* flags,
+                                          uint32_t vote_tag, const DevErr& err, bool& ok) {
+  const bool warp_skip = __all_sync(0xffffffffu, row_skip);
+  const int quarter = (threadIdx.x >> 5) & 3;
+  if ((threadIdx.x & 31) == 0) flags[quarter] = (vote_tag << 1) | (warp_skip ? 1u : 0u);
+  __syncwarp();
+  if (!warp_skip) return true;
+  uint32_t f0, f1, f2, f3;
+  uint32_t spins = 0;
+  uint64_t t0 = 0;
+  while (true) {
+    f0 = flags[0], f1 = flags[1], f2 = flags[2], f3 = flags[3];
+    if (((f0 | f1 | f2 | f3) >> 1) == vote_tag && ((f0 & f1 & f2 & f3) >> 1) == vote_tag) break;
+    if ((++spins & 63u) == 0) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) t0 = now;
+      if (*(volatile uint32_t*)err.word != 0u || now - t0 > err.timeout_ns) {
+        atomicCAS(err.word, 0u, ERR_WAIT_ATTN_SOFTMAX);
+        break;
+      }
+    }
+  }
+  if (!__all_sync(0xffffffffu, ((f0 & f1 & f2 & f3) >> 1) == vote_tag &&
+                                   ((f0 | f1 | f2 | f3) >> 1) == vote_tag)) {
+    ok = false;
+    return false;
+  }
+  return !(f0 & f1 & f2 & f3 & 1u);
+}
+
 template <bool F8, bool SKIP>
 __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid, bool o_live,
                                              float scale_log2, float& m, float& l,
                                              float skip_log2, float& m_keep, bool row_valid,
-                                             volatile uint32_t* flags, uint32_t vote_bar,
-                                             uint32_t vote_parity, const DevErr& err, bool& ok) {
+                                             volatile uint32_t* flags, uint32_t vote_tag,
+                                             const DevErr& err, bool& ok) {
   uint32_t sr[128];
   {
     uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
@@ -166,17 +204,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, int valid
   const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
   if constexpr (SKIP) {
     // never on the first tile for a valid row (m_keep = -inf)
-    const bool row_skip = !row_valid || mx < m_keep - skip_log2;
-    const uint32_t warp_skip = __all_sync(0xffffffffu, row_skip) ? 1u : 0u;
-    const int quarter = (threadIdx.x >> 5) & 3;
-    if ((threadIdx.x & 31) == 0) flags[quarter] = warp_skip;
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(vote_bar);
-    if (!mbar_wait_warp(vote_bar, vote_parity, err, ERR_WAIT_ATTN_SOFTMAX)) {
-      ok = false;
-      return true;
-    }
-    if (flags[0] & flags[1] & flags[2] & flags[3]) return true;
+    if (!skip_vote(!row_valid || mx < m_keep - skip_log2, flags, vote_tag, err, ok)) return true;
     m_keep = fmaxf(m_keep, mx);
   }
   // Raise the running max only when it is exceeded by more than the
@@ -309,8 +337,7 @@ enum Bar2 {
   B2_P = B2_S + 2,
   B2_O = B2_P + 2,
   B2_DRAIN = B2_O + 2,  // the MMA thread's last commit, waited on before exit
-  B2_VOTE = B2_DRAIN + 1,  // Skip-Softmax vote of each query tile's four warps
-  B2_NUM = B2_VOTE + 2
+  B2_NUM = B2_DRAIN + 1
 };
 // barriers, the TMEM address word (padded to 16 bytes) and 16 vote flags
 static_assert(B2_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
@@ -345,9 +372,9 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
   const int n = a.num_kv;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B2_NUM; ++i)
-      mbar_init(bar(i), (i == B2_P || i == B2_P + 1) ? 128 : (i >= B2_VOTE ? 4 : 1));
+    for (int i = 0; i < B2_NUM; ++i) mbar_init(bar(i), (i == B2_P || i == B2_P + 1) ? 128 : 1);
     fence_mbar_init();
+    for (int i = 0; i < 16; ++i) skip_flags[i] = 0xffffffffu;  // no step's tag
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -431,7 +458,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       auto pv = [&](int i, int j) {  // O_i += P_i V_j (left out when the tile was skipped)
         const uint32_t v_addr = kv_addr + slot_of(2 * j + 1) * T_BYTES;
         volatile uint32_t* f = skip_flags + (i * 2 + (j & 1)) * 4;
-        const bool skipped = SKIP && (f[0] & f[1] & f[2] & f[3]);
+        const bool skipped = SKIP && (f[0] & f[1] & f[2] & f[3] & 1u);
         if (!skipped) {
           ++kept[i];
           if constexpr (F8) {
@@ -523,7 +550,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       if constexpr (F8) mul = fmaxf(mul * sq_tile * __ldg(a.sk + j * a.H + blockIdx.y), 1e-30f);
       softmax_tile<F8, SKIP>(tS, tO, a.L - j * BKV, j > 0, mul, m, l, a.skip_log2, m_keep,
                              row_valid, skip_flags + (tile * 2 + (j & 1)) * 4,
-                             bar(B2_VOTE + tile), static_cast<uint32_t>(j) & 1u, a.err, ok);
+                             static_cast<uint32_t>(j), a.err, ok);
       if (!ok) break;
       tc_fence_before();
       mbar_arrive(bar(B2_P + tile));
@@ -966,7 +993,8 @@ enum BarF8 {
   BF_DRAIN = BF_O + 1,
   BF_NUM = BF_DRAIN + 1
 };
-static_assert(BF_NUM * 8 + 16 <= 256, "barrier region");
+// barriers, the TMEM address word (padded to 16 bytes) and 16 vote flags
+static_assert(BF_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
 
 // softmax_tile<true, false>'s arithmetic for one KV tile (integer running max
 // within 1 of the true one, P carried as 224 P, E4M3 codes), with the row's
@@ -974,13 +1002,22 @@ static_assert(BF_NUM * 8 + 16 <= 256, "barrier region");
 // p_row = the P tile's address + 128 * row, 16-byte chunk c of the row at
 // chunk c ^ r7 (r7 = row & 7: the 128-byte swizzle of a K-major tile). The
 // codes, m and l are bitwise those of softmax_tile<true, false>. wait_pv() is
-// called before the stores, or before an O rescale. Returns false when it
-// fails.
-template <class WaitPV>
-__device__ __forceinline__ bool softmax_tile_f8_smem(uint32_t (&sr)[128], uint32_t p_row,
-                                                     uint32_t r7, uint32_t tO, int valid,
-                                                     bool o_live, float scale_log2, float& m,
-                                                     float& l, WaitPV&& wait_pv) {
+// called before the stores, or before an O rescale.
+// SKIP: Skip-Softmax as in softmax_tile<false, true>: the tile's four warps
+// vote through flags[quarter], each tagged with vote_tag (the KV step); when
+// every valid row's tile maximum lies more than skip_log2 below m_keep (the
+// row's exact running maximum over the kept tiles; rows >= L vote to skip),
+// nothing is computed or stored and the MMA warp leaves out the tile's P V.
+// Returns F8_KEPT, F8_SKIPPED, or F8_FAILED when a wait failed.
+enum : int { F8_KEPT = 0, F8_SKIPPED = 1, F8_FAILED = -1 };
+template <bool SKIP, class WaitPV>
+__device__ __forceinline__ int softmax_tile_f8_smem(uint32_t (&sr)[128], uint32_t p_row,
+                                                    uint32_t r7, uint32_t tO, int valid,
+                                                    bool o_live, float scale_log2, float& m,
+                                                    float& l, WaitPV&& wait_pv, float skip_log2,
+                                                    float& m_keep, bool row_valid,
+                                                    volatile uint32_t* flags, uint32_t vote_tag,
+                                                    const DevErr& err) {
   if (valid < BKV) {
 #pragma unroll
     for (int c = 0; c < 128; ++c)
@@ -995,13 +1032,20 @@ __device__ __forceinline__ bool softmax_tile_f8_smem(uint32_t (&sr)[128], uint32
     md = max3f(md, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
   }
   const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
+  if constexpr (SKIP) {
+    // never on the first tile for a valid row (m_keep = -inf)
+    bool ok = true;
+    if (!skip_vote(!row_valid || mx < m_keep - skip_log2, flags, vote_tag, err, ok))
+      return ok ? F8_SKIPPED : F8_FAILED;
+    m_keep = fmaxf(m_keep, mx);
+  }
   bool pv_done = !o_live;
   if (__any_sync(0xffffffffu, mx > m + 1.0f)) {
     const float m_new = ceilf(fmaxf(m, mx));
     const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
     l *= alpha;
     if (o_live) {
-      if (!wait_pv()) return false;
+      if (!wait_pv()) return F8_FAILED;
       pv_done = true;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -1036,13 +1080,16 @@ __device__ __forceinline__ bool softmax_tile_f8_smem(uint32_t (&sr)[128], uint32
     pk[i] = lo | (hi << 16);
   }
   l += (la + lb) + (lc + ld);
-  if (!pv_done && !wait_pv()) return false;
+  if (!pv_done && !wait_pv()) return F8_FAILED;
 #pragma unroll
   for (uint32_t c = 0; c < 8; ++c)  // keys 16 c .. 16 c + 15
     st_shared_v4(p_row + ((c ^ r7) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-  return true;
+  return F8_KEPT;
 }
 
+// SKIP: Skip-Softmax compiled in (a separate instance, so the plain kernel
+// carries none of its votes or branches).
+template <bool SKIP>
 __global__ void __launch_bounds__(Q2_THREADS, 1)
     attention_f8_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
@@ -1055,6 +1102,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
   uint8_t* sP = sQ + 2 * F8_TILE;                     // 2 tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * F8_TILE);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BF_NUM);
+  // Skip-Softmax votes: [tile][parity of j][quarter]
+  volatile uint32_t* skip_flags = tmem_slot + 4;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
@@ -1066,6 +1115,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < BF_NUM; ++i) mbar_init(bar(i), (i >= BF_SFREE && i < BF_PVD) ? 4 : 1);
     fence_mbar_init();
+    for (int i = 0; i < 16; ++i) skip_flags[i] = 0xffffffffu;  // no step's tag
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -1128,14 +1178,22 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         mma_ss_f8_el(tmem + i * 128, qd + kk * 2, kd + kk * 2, idesc_qk, kk > 0 ? 1u : 0u);
       mma_commit_el(bar(BF_S + i));
     };
+    int kept[2] = {0, 0};  // Skip-Softmax: key tiles kept per query tile
+    bool any_pv[2] = {false, false};
     auto pv = [&](int i, int j) {  // O_i += P_i V_j; 32 keys (32 rows of V, 4 KB) per instruction
-      const uint64_t pd = dp + static_cast<uint32_t>(i * (F8_TILE >> 4));
-      const uint64_t vd = dv + stage(j);
+      volatile uint32_t* f = skip_flags + (i * 2 + (j & 1)) * 4;
+      const bool skipped = SKIP && (f[0] & f[1] & f[2] & f[3] & 1u);
+      if (!skipped) {  // (the first tile is never skipped)
+        ++kept[i];
+        const uint64_t pd = dp + static_cast<uint32_t>(i * (F8_TILE >> 4));
+        const uint64_t vd = dv + stage(j);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_ss_f8_el(tmem + 256 + i * 128, pd + kk * 2, vd + kk * (4096 >> 4), idesc_pv,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_el(bar(BF_PVD + i));
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss_f8_el(tmem + 256 + i * 128, pd + kk * 2, vd + kk * (4096 >> 4), idesc_pv,
+                       (any_pv[i] || kk > 0) ? 1u : 0u);
+        any_pv[i] = true;
+      }
+      mma_commit_el(bar(BF_PVD + i));  // also for a skipped tile: the phase counts steps
     };
     bool ok = wait(BF_Q, 0u) && wait_full(0);
     if (ok) {
@@ -1165,6 +1223,12 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       mma_commit_el(bar(BF_EMPTY + j % F8_STAGES));  // K_j, V_j read
     }
     mma_commit_el(bar(BF_O));
+    if (SKIP && a.kept != nullptr && ok && lane == 0) {
+      for (int i = 0; i < 2; ++i) {
+        const int qt = blockIdx.x * 2 + i;
+        if (qt * BQ < a.L) a.kept[qt * a.H + blockIdx.y] = kept[i];
+      }
+    }
     // every MMA must be done with shared and tensor memory before the CTA
     // frees them: commit and wait, bounded
     mma_commit_el(bar(BF_DRAIN));
@@ -1181,6 +1245,8 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
     const int qt = blockIdx.x * 2 + tile;  // 128-row query tile index
     const float sq_tile = (qt * BQ < a.L) ? __ldg(a.sq + qt * a.H + blockIdx.y) : 0.f;
     float m = -INFINITY, l = 0.f;
+    float m_keep = -INFINITY;  // Skip-Softmax: exact running max of the kept tiles
+    const bool row_valid = q0 + tile * BQ + static_cast<int>(row) < a.L;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait_warp(bar(BF_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
@@ -1215,8 +1281,10 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         tc_fence_after();
         return done;
       };
-      if (!softmax_tile_f8_smem(sr, p_row, row & 7u, tO, a.L - j * BKV, j > 0, mul, m, l,
-                                wait_pv)) {
+      if (softmax_tile_f8_smem<SKIP>(sr, p_row, row & 7u, tO, a.L - j * BKV, j > 0, mul, m, l,
+                                     wait_pv, a.skip_log2, m_keep, row_valid,
+                                     skip_flags + (tile * 2 + (j & 1)) * 4,
+                                     static_cast<uint32_t>(j), a.err) == F8_FAILED) {
         ok = false;
         break;
       }
@@ -1272,7 +1340,7 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   a.num_kv = (L + BKV - 1) / BKV;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.skip_log2 = skip_eps > 0.f ? -log2f(skip_eps) : INFINITY;
-  a.kept = skip ? kept : nullptr;
+  a.kept = skip_eps > 0.f ? kept : nullptr;  // the counts only when tiles may be skipped
   if ((st = dev_err(&a.err)) != H3_OK) return st;
   CUtensorMap tq, tk, tv;
   const uint64_t width = static_cast<uint64_t>(H) * DH;
@@ -1294,10 +1362,14 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
 
 h3_status launch_attention_fp8(const void* qc, const void* kc, const void* vc, int64_t ld_codes,
                                const float* sq, const float* sk, const float* sv, void* o,
-                               int64_t ld_out, int L, int H, float scale, cudaStream_t s) {
-  static std::atomic<bool> done[64];
-  h3_status st = set_smem_limit(done, attention_f8_kernel, F8_SMEM_BYTES,
-                                "attention (fp8): set shared memory size");
+                               int64_t ld_out, int L, int H, float scale, cudaStream_t s,
+                               float skip_eps, int* kept) {
+  const bool skip = skip_eps >= 0.f;
+  static std::atomic<bool> done[64], done_skip[64];
+  h3_status st = skip ? set_smem_limit(done_skip, attention_f8_kernel<true>, F8_SMEM_BYTES,
+                                       "attention (fp8, skip): set shared memory size")
+                      : set_smem_limit(done, attention_f8_kernel<false>, F8_SMEM_BYTES,
+                                       "attention (fp8): set shared memory size");
   if (st != H3_OK) return st;
   AttnArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
@@ -1309,6 +1381,8 @@ h3_status launch_attention_fp8(const void* qc, const void* kc, const void* vc, i
   a.sq = sq;
   a.sk = sk;
   a.sv = sv;
+  a.skip_log2 = skip_eps > 0.f ? -log2f(skip_eps) : INFINITY;
+  a.kept = skip_eps > 0.f ? kept : nullptr;  // the counts only when tiles may be skipped
   if ((st = dev_err(&a.err)) != H3_OK) return st;
   CUtensorMap tq, tk, tv;
   const uint64_t width = static_cast<uint64_t>(H) * DH;  // bytes per row of codes
@@ -1316,7 +1390,10 @@ h3_status launch_attention_fp8(const void* qc, const void* kc, const void* vc, i
   if ((st = make_tmap_u8_2d(&tk, kc, width, L, ld_codes, 128, BKV)) != H3_OK) return st;
   if ((st = make_tmap_u8_2d(&tv, vc, width, L, ld_codes, 128, BKV)) != H3_OK) return st;
   dim3 grid((L + 2 * BQ - 1) / (2 * BQ), H);
-  attention_f8_kernel<<<grid, Q2_THREADS, F8_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  if (skip)
+    attention_f8_kernel<true><<<grid, Q2_THREADS, F8_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  else
+    attention_f8_kernel<false><<<grid, Q2_THREADS, F8_SMEM_BYTES, s>>>(tq, tk, tv, a);
   return cuda_fail(cudaGetLastError(), "attention (fp8) launch");
 }
 

@@ -155,8 +155,11 @@ h3_status launch_sage_quantize(const void* q, const void* k, const void* v, int6
                                int H, uint8_t* qc, uint8_t* kc, uint8_t* vc, int64_t ldc,
                                float* sq, float* sk, float* sv, float* k_mean, void* scratch,
                                cudaStream_t s);
+// skip_eps >= 0: Skip-Softmax on the FP8 logits (kept tile counts to `kept`
+// [ceil(L/128), H] when not null), as in launch_attention.
 h3_status launch_attention_fp8(const void* qc, const void* kc, const void* vc, int64_t ld_codes,
                                const float* sq, const float* sk, const float* sv, void* o,
-                               int64_t ld_out, int L, int H, float scale, cudaStream_t s);
+                               int64_t ld_out, int L, int H, float scale, cudaStream_t s,
+                               float skip_eps = -1.f, int* kept = nullptr);
 
 }  // namespace h3

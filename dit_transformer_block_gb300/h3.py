@@ -66,6 +66,7 @@ _SIGS = {
     "h3_sage_quantize": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                               _P]),
     "h3_attention_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
+    "h3_attention_fp8_skip": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P]),
     "h3_attention_varlen_skip": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P]),
     "h3_linear": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "h3_linear_swiglu": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
@@ -271,6 +272,22 @@ def attention_fp8(ops: dict, o, L=None, scale=None, stream=None):
     _check("attention_fp8", lib().h3_attention_fp8(
         _p(ops["qc"]), _p(ops["kc"]), _p(ops["vc"]), _p(ops["sq"]), _p(ops["sk"]),
         _p(ops["sv"]), _p(o), S, L, H, Dh, scale, _s(stream)))
+
+
+def attention_fp8_skip(ops: dict, o, L=None, scale=None, skip_eps=0.0, kept=None, stream=None):
+    """attention_fp8 with Skip-Softmax tile skipping on the FP8 logits
+    (skip_eps = 0: attention_fp8 bit for bit). kept (optional): int32
+    [ceil(L/128), H], receives the key tiles kept per (query tile, head)."""
+    S, H, Dh = o.shape
+    L = S if L is None else L
+    scale = Dh ** -0.5 if scale is None else scale
+    if kept is not None:
+        _need(kept, torch.int32, "kept")
+        if tuple(kept.shape) != ((L + 127) // 128, H):
+            raise ValueError(f"kept must be [{(L + 127) // 128}, {H}]")
+    _check("attention_fp8_skip", lib().h3_attention_fp8_skip(
+        _p(ops["qc"]), _p(ops["kc"]), _p(ops["vc"]), _p(ops["sq"]), _p(ops["sk"]),
+        _p(ops["sv"]), _p(o), S, L, H, Dh, scale, skip_eps, _p(kept), _s(stream)))
 
 
 def swiglu(gate_up, out, L=None, stream=None):

@@ -143,6 +143,26 @@ def attention_inputs(S: int, L: int, H: int, Dh: int, seed: int, device="cpu") -
     return dict(q=q, k=k, v=v)
 
 
+def frame_local_attention_inputs(S: int, L: int, H: int, Dh: int, frame: int, seed: int,
+                                 device="cpu", strength: float = 16.0) -> dict:
+    """Attention inputs with frame locality (tokens of one frame attend mostly
+    to each other): rows are grouped into frames of `frame` consecutive rows;
+    every (frame, head) draws a random unit direction e, and q = n_q +
+    strength * e, k = n_k + strength * e with n_q, n_k ~ N(0,1) per channel;
+    v ~ N(0,1); all bf16 [S, H, Dh]. At strength 16 and Dh = 128 a query's
+    logits against its own frame sit about 30 base-2 units above those
+    against other frames (softmax scale Dh^-1/2)."""
+    g = _gen(seed, device)
+    nf = (S + frame - 1) // frame
+    e = torch.randn(nf, H, Dh, generator=g, device=device)
+    e = e / e.norm(dim=-1, keepdim=True)
+    ef = e.repeat_interleave(frame, dim=0)[:S] * strength
+    q = (torch.randn(S, H, Dh, generator=g, device=device) + ef).to(torch.bfloat16)
+    k = (torch.randn(S, H, Dh, generator=g, device=device) + ef).to(torch.bfloat16)
+    v = torch.randn(S, H, Dh, generator=g, device=device).to(torch.bfloat16)
+    return dict(q=q, k=k, v=v)
+
+
 def swiglu_inputs(S: int, F: int, seed: int, device="cpu") -> dict:
     """gate_up ~ N(0, 1.5^2) bf16 [S, 2F] (the spread of an FFN up-projection)."""
     g = _gen(seed, device)

@@ -196,6 +196,25 @@ h3_status h3_attention_fp8(const void* qc, const void* kc, const void* vc, const
                            int Dh, float softmax_scale, h3_stream_t stream);
 
 /*
+ * h3_attention_fp8 with Skip-Softmax (blog section 4.3, Fig. 6: SAGE
+ * quantisation and Skip-Softmax together): the tile rule of
+ * h3_attention_varlen_skip applied to the FP8 logits z_ij of h3_attention_fp8
+ * (a key tile is left out for a 128-row query tile when every valid row's
+ * largest z in it lies more than log2(1/skip_eps) below the row's exact
+ * running maximum of z over the key tiles kept so far; the first key tile is
+ * never left out); the kept tiles are then handled as in h3_attention_fp8,
+ * whose result skip_eps == 0 reproduces bit for bit.
+ *   kept_tiles  [ceil(L/128), H] int32 device, or NULL: the number of key
+ *               tiles kept for every (query tile, head) (only with
+ *               skip_eps > 0; left untouched otherwise); 4-byte aligned
+ * Other arguments as h3_attention_fp8; 0 <= skip_eps < 1.
+ */
+h3_status h3_attention_fp8_skip(const void* qc, const void* kc, const void* vc, const float* sq,
+                                const float* sk, const float* sv, void* o, int S, int L, int H,
+                                int Dh, float softmax_scale, float skip_eps, int32_t* kept_tiles,
+                                h3_stream_t stream);
+
+/*
  * a5 — SwiGLU (blog section 3.2, #6283): out[i,j] = SiLU(g) * u with
  * g = gate_up[i,j], u = gate_up[i,F+j], SiLU(g) = g / (1 + exp(-g)), for i < L.
  *   gate_up [S, 2F] bf16, out [S, F] bf16. F % 8 == 0.

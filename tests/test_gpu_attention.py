@@ -93,9 +93,11 @@ def test_skip_softmax_eps_zero_is_dense_bitwise(h3lib):
     inp = I.attention_inputs(S, L, H, 128, seed=8, device=dev)
     o1 = run(h3lib, inp["q"], inp["k"], inp["v"], L)
     o2 = torch.full_like(o1, SENT)
-    h3lib.attention_varlen_skip(inp["q"], inp["k"], inp["v"], o2, L, skip_eps=0.0)
+    kept = torch.full(((L + 127) // 128, H), -1, dtype=torch.int32, device=dev)
+    h3lib.attention_varlen_skip(inp["q"], inp["k"], inp["v"], o2, L, skip_eps=0.0, kept=kept)
     h3lib.check_device_error()
     assert torch.equal(o1, o2)
+    assert bool((kept == -1).all())  # the counts are written only when eps > 0
 
 
 def test_skip_softmax_skips_the_tile_the_rule_names(h3lib):

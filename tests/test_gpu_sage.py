@@ -90,3 +90,55 @@ def test_sage_full_size_sampled(h3lib):
     terms = O.sage_error_terms(ref_ops, L, SCALE, rows=rows)
     assert_close_sage(np64(o[torch.from_numpy(rows).to(dev)]), ref, terms, L, "sage full size")
     assert bool((o[L:] == SENT).all())
+
+
+def test_sage_skip_eps_zero_is_attention_fp8_bitwise(h3lib):
+    S, L, H = 640, 600, 3
+    inp = I.attention_inputs(S, L, H, 128, seed=31, device=dev)
+    ops = h3lib.sage_quantize(inp["q"], inp["k"], inp["v"], L)
+    o_ref = torch.full_like(inp["q"], SENT)
+    h3lib.attention_fp8(ops, o_ref, L)
+    o = torch.full_like(inp["q"], SENT)
+    kept = torch.full(((L + 127) // 128, H), -1, dtype=torch.int32, device=dev)
+    h3lib.attention_fp8_skip(ops, o, L, skip_eps=0.0, kept=kept)
+    h3lib.check_device_error()
+    assert torch.equal(o, o_ref)
+    assert bool((kept == -1).all())  # left untouched at eps = 0
+
+
+@pytest.mark.parametrize("S,L,eps_log2", [(2048, 2000, 4), (1024, 1024, 2), (1408, 1300, 6)])
+def test_sage_skip_matches_oracle_rule(h3lib, S, L, eps_log2):
+    """Queries and keys with a shared direction whose per-key-tile weight
+    varies, so that whole tiles fall far below the running maximum: the
+    GPU's codes equal the oracle's, its kept-tile counts equal those of
+    oracle.attention_sage_skip, its output is within the SAGE tolerance of
+    the oracle's (error terms over the kept keys), and it differs from the
+    unskipped FP8 attention. Pad rows are not written."""
+    H = 2
+    g = torch.Generator().manual_seed(S + 7 * eps_log2)
+    q = torch.randn(S, H, 128, generator=g)
+    k = torch.randn(S, H, 128, generator=g)
+    v = torch.randn(S, H, 128, generator=g)
+    q[:, :, 0] += 8.0
+    nk = (S + 127) // 128
+    b = torch.randn(nk, H, generator=g) * 8.0
+    k[:, :, 0] += b.repeat_interleave(128, dim=0)[:S]
+    q, k, v = (t.to(torch.bfloat16).to(dev) for t in (q, k, v))
+    ops = h3lib.sage_quantize(q, k, v, L)
+    ref_ops = O.sage_quantize(np64(q), np64(k), np64(v), L)
+    assert_ops_equal(ops, ref_ops, L)
+    eps = 2.0 ** -eps_log2
+    nq = (L + 127) // 128
+    kept_gpu = torch.full((nq, H), -1, dtype=torch.int32, device=dev)
+    o = torch.full_like(q, SENT)
+    h3lib.attention_fp8_skip(ops, o, L, skip_eps=eps, kept=kept_gpu)
+    h3lib.check_device_error()
+    assert bool((o[L:] == SENT).all())
+    ref, kept = O.attention_sage_skip(ref_ops, L, SCALE, eps)
+    want = kept.sum(axis=2)
+    assert want.sum() < nq * H * nq  # tiles really are skipped
+    assert np.array_equal(kept_gpu.cpu().numpy(), want)
+    terms = O.sage_skip_error_terms(ref_ops, L, SCALE, eps)
+    assert_close_sage(np64(o[:L]), ref, terms, L, "sage + skip-softmax")
+    full = O.attention_sage(ref_ops, L, SCALE)
+    assert np.max(np.abs(ref - full)) > 0
