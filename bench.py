@@ -514,9 +514,10 @@ def run_reference(a):
 
 
 # ------------------------------------------------------------------ our arm
-def profile_traffic(kernel_file: str, profile_md: str):
+def profile_traffic(kernel_files, profile_md: str):
     """DRAM bytes per launch recorded in a committed ncu summary, if the
-    kernel source it was taken from is unchanged."""
+    kernel sources it was taken from (their texts joined in the order given)
+    are unchanged."""
     p = os.path.join(ROOT, "profiles", profile_md)
     if not os.path.exists(p):
         return None
@@ -525,10 +526,15 @@ def profile_traffic(kernel_file: str, profile_md: str):
     h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", text)
     if not m or not h:
         return None
-    src = open(os.path.join(ROOT, "dit_transformer_block_gb300", "csrc", kernel_file)).read()
+    src = "\n".join(open(os.path.join(ROOT, "dit_transformer_block_gb300", "csrc", f)).read()
+                    for f in kernel_files)
     if not code_sha256(src).startswith(h.group(1)):
         return None
     return float(m.group(1))
+
+
+# the dense attention kernel's sources, for the recorded DRAM traffic
+ATTENTION_SOURCES = ("h3_attention.cu", "h3_attn_common.cuh")
 
 
 def code_sha256(src: str) -> str:
@@ -713,7 +719,7 @@ def run_ours(a):
     ew_ms = stage_ms[0] + stage_ms[4]
     attn_tf = work["attn_flop"] / attn_ms / 1e9
     gemm_tf = work["gemm_flop"] / gemm_ms / 1e9
-    traffic = profile_traffic("h3_attention.cu", "attention_pair_small_case.md")
+    traffic = profile_traffic(ATTENTION_SOURCES, "attention_pair_small_case.md")
     stages_roofline = {}
     for name, t, (bound, amount, unit) in zip(h3.STAGE_NAMES, stage_ms,
                                               stage_work(S, L, D, H, Dh, F)):

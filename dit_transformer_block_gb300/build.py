@@ -15,7 +15,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libh3block.so")
-SOURCES = ["h3_abi.cu", "h3_elementwise.cu", "h3_gemm.cu", "h3_attention.cu", "h3_sage.cu"]
+SOURCES = ["h3_abi.cu", "h3_elementwise.cu", "h3_gemm.cu", "h3_attention.cu",
+           "h3_attention_tiles.cu", "h3_sage.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-Wall"]
