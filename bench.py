@@ -422,6 +422,10 @@ def measure_extras(h3, torch, shape, inp, cfg, ws, stream, pk):
     ms = timeit(lambda: h3.attention_fp8_skip(ops, o_at, L, skip_eps=eps, kept=kept), 3)
     skip["fp8_unit_rms"] = {"ms": round(ms, 3),
                             "kept_fraction": round(kept.sum().item() / (nq * H * nq), 4)}
+    ms = timeit(lambda: h3.attention_varlen_skip(at["q"], at["k"], at["v"], o_at, L,
+                                                 skip_eps=eps, kept=kept), 3)
+    skip["bf16_unit_rms"] = {"ms": round(ms, 3),
+                             "kept_fraction": round(kept.sum().item() / (nq * H * nq), 4)}
     del at, ops
     loc = I.frame_local_attention_inputs(S, L, H, 128, frame=1024, seed=5,
                                          device=inp["resid"].device)

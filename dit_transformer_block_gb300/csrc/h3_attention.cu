@@ -10,8 +10,9 @@
 // The online softmax is base 2 with the scale folded in (packed FP32 FMA and
 // add, 3-input max); the running max is raised only when a row's new max
 // exceeds it by more than 8 (then O and the row sum are rescaled); only the
-// last KV tile is masked. Skip-Softmax and the FP8 (SAGE) attention are in
-// h3_attention_tiles.cu.
+// last KV tile is masked. With Skip-Softmax (blog section 4.3, Fig. 6) a key
+// tile that every row of a CTA's query tile finds negligible gives those rows
+// nothing. The FP8 (SAGE) attention is in h3_attention_tiles.cu.
 #include <algorithm>
 
 #include "h3_attn_common.cuh"
@@ -57,9 +58,9 @@ namespace {
 constexpr int P2_STAGES = 3;
 constexpr int HALF_BYTES = TILE_BYTES / 2;   // 64 keys x 128 ch, or 128 keys x 64 ch (bf16)
 constexpr int STAGE2_BYTES = 2 * HALF_BYTES; // K half at 0, V half at HALF_BYTES
-// stages, Q tiles, P tiles, barriers (227 KB is the per-CTA limit)
+// stages, Q tiles, P tiles, barriers and flags (227 KB is the per-CTA limit)
 constexpr size_t P2_SMEM_BYTES =
-    1024 + P2_STAGES * STAGE2_BYTES + 2 * TILE_BYTES + 2 * TILE_BYTES + 256;
+    1024 + P2_STAGES * STAGE2_BYTES + 2 * TILE_BYTES + 2 * TILE_BYTES + 512;
 static_assert(P2_SMEM_BYTES <= 227 * 1024, "pair kernel shared memory");
 
 enum BarP {
@@ -74,23 +75,38 @@ enum BarP {
   BP_DRAIN = BP_O + 1,
   BP_NUM = BP_DRAIN + 1
 };
-static_assert(BP_NUM * 8 + 16 <= 256, "barrier region");
+// barriers, the TMEM address word (padded to 16 bytes), 16 vote flags and
+// 16 decisions of the peer CTA
+static_assert(BP_NUM * 8 + 16 + 16 * 4 + 16 * 4 <= 512, "barrier + flag region");
 
-// The online softmax of softmax_tile<false, false> (its exact pass) for one
-// KV tile, with the row's 128 scores already in registers (sr) and P written
-// to shared memory: p_row = the P tile's shared-memory address + 128 * row,
-// r7 = row & 7 (the 128-byte swizzle of a K-major bf16 tile: 16-byte chunk c
-// of a row sits at chunk (c & 7) ^ r7 of box c >> 3). The same operations in
-// the same order as softmax_tile's exact pass, so P, m and l are bitwise
-// those of the one-CTA kernel. The whole P row is formed in registers first
-// and stored last: wait_pv() (the previous P V of this tile has finished with
-// P and O) is called only before the stores, or before an O rescale, so that
-// wait overlaps the exponentials. Returns false when wait_pv() fails.
-template <class WaitPV>
-__device__ __forceinline__ bool softmax_tile_smem(uint32_t (&sr)[128], uint32_t p_row, uint32_t r7,
-                                                  uint32_t tO, int valid, bool o_live,
-                                                  float scale_log2, float& m, float& l,
-                                                  WaitPV&& wait_pv) {
+// One KV tile of the online softmax for the calling thread's query row (TMEM
+// lane), in base 2 with the scale folded in (scale_log2 = softmax scale *
+// log2(e)); the row's 128 scores are already in registers (sr); valid = keys
+// of this tile below L (>= BKV: none masked); o_live: O already holds
+// earlier tiles; m, l: running max (times scale_log2) and row sum. The
+// running max is raised only when the tile's max exceeds it by more than
+// RESCALE_THRESHOLD (then O and l are rescaled, warp-uniformly). P (bf16) is
+// written to shared memory: p_row = the P tile's shared-memory address + 128
+// * row, r7 = row & 7 (the 128-byte swizzle of a K-major bf16 tile: 16-byte
+// chunk c of a row sits at chunk (c & 7) ^ r7 of box c >> 3). The whole P row
+// is formed in registers first and stored last: wait_pv() (the previous P V
+// of this tile has finished with P and O) is called only before the stores,
+// or before an O rescale, so that wait overlaps the exponentials.
+// SKIP: Skip-Softmax: the four warps of the CTA's query tile vote (skip_vote,
+// step vote_tag); when every valid row's tile maximum lies more than
+// skip_log2 below m_keep (the row's exact running maximum over the kept
+// tiles; rows >= L vote to skip), the tile gives these rows nothing: the
+// group's P V still runs for the peer CTA's rows, so P is set to zero
+// (once: p_zero records that it already is).
+// Returns TILE_KEPT, TILE_SKIPPED, or TILE_FAILED when a wait failed.
+template <bool SKIP, class WaitPV>
+__device__ __forceinline__ int softmax_tile_smem(uint32_t (&sr)[128], uint32_t p_row, uint32_t r7,
+                                                 uint32_t tO, int valid, bool o_live,
+                                                 float scale_log2, float& m, float& l,
+                                                 WaitPV&& wait_pv, float skip_log2, float& m_keep,
+                                                 bool row_valid, volatile uint32_t* flags,
+                                                 uint32_t vote_tag, bool& p_zero,
+                                                 const DevErr& err) {
   if (valid < BKV) {
 #pragma unroll
     for (int c = 0; c < 128; ++c)
@@ -105,13 +121,32 @@ __device__ __forceinline__ bool softmax_tile_smem(uint32_t (&sr)[128], uint32_t 
     md = max3f(md, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
   }
   const float mx = max3f(ma, mb, fmaxf(mc, md)) * scale_log2;
+  if constexpr (SKIP) {
+    // never on the first tile for a valid row (m_keep = -inf)
+    bool ok = true;
+    if (!skip_vote(!row_valid || mx < m_keep - skip_log2, flags, vote_tag, err, ok)) {
+      if (!ok) return TILE_FAILED;
+      // also before the P arrive: the group's P barrier takes both CTAs'
+      // warps, and its phase must not run ahead of the previous one
+      if (o_live && !wait_pv()) return TILE_FAILED;
+      if (!p_zero) {
+#pragma unroll
+        for (uint32_t chunk = 0; chunk < 16; ++chunk)
+          st_shared_v4(p_row + (chunk >> 3) * BOX_BYTES + (((chunk & 7u) ^ r7) << 4), 0u, 0u, 0u,
+                       0u);
+        p_zero = true;
+      }
+      return TILE_SKIPPED;
+    }
+    m_keep = fmaxf(m_keep, mx);
+  }
   bool pv_done = !o_live;  // the first tile has no earlier product
   if (__any_sync(0xffffffffu, mx > m + RESCALE_THRESHOLD)) {
     const float m_new = fmaxf(m, mx);
     const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
     l *= alpha;
     if (o_live) {
-      if (!wait_pv()) return false;
+      if (!wait_pv()) return TILE_FAILED;
       pv_done = true;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -147,14 +182,18 @@ __device__ __forceinline__ bool softmax_tile_smem(uint32_t (&sr)[128], uint32_t 
     }
   }
   l += (la + lb) + (lc + ld);
-  if (!pv_done && !wait_pv()) return false;
+  if (!pv_done && !wait_pv()) return TILE_FAILED;
 #pragma unroll
   for (uint32_t chunk = 0; chunk < 16; ++chunk)  // keys 8 chunk .. 8 chunk + 7
     st_shared_v4(p_row + (chunk >> 3) * BOX_BYTES + (((chunk & 7u) ^ r7) << 4), pk[4 * chunk],
                  pk[4 * chunk + 1], pk[4 * chunk + 2], pk[4 * chunk + 3]);
-  return true;
+  if constexpr (SKIP) p_zero = false;
+  return TILE_KEPT;
 }
 
+// SKIP: Skip-Softmax compiled in (a separate instance, so the dense kernel
+// carries none of its votes or branches).
+template <bool SKIP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
     attention_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
@@ -167,6 +206,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
   uint8_t* sP = sQ + 2 * TILE_BYTES;               // 2 tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BP_NUM);
+  // Skip-Softmax votes of this CTA: [tile][parity of j][quarter]; in the even
+  // CTA, the odd CTA's decisions (1: its query tile left the key tile out),
+  // same layout
+  volatile uint32_t* skip_flags = tmem_slot + 4;
+  volatile uint32_t* peer_skip = skip_flags + 16;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const uint32_t rank = cluster_ctarank();
@@ -187,6 +231,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       mbar_init(bar(i), count);
     }
     fence_mbar_init();
+    if constexpr (SKIP)
+      for (int i = 0; i < 16; ++i) skip_flags[i] = 0xffffffffu;  // no step's tag
   }
   if (warp == 9) {
     tmem_alloc_pair(smem_u32(tmem_slot), 512);
@@ -266,14 +312,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
                          idesc_qk, kk > 0 ? 1u : 0u);
         mma_commit_pair_mc_el(bar(BP_S + g), kBoth);
       };
+      bool any_pv[2] = {false, false};
       auto pv = [&](int g, int j) {  // O_g += P_g V_j
-        const uint64_t vd = dv + static_cast<uint32_t>((j % P2_STAGES) * (STAGE2_BYTES >> 4));
-        const uint64_t pd = dp + static_cast<uint32_t>(g * (TILE_BYTES >> 4));
+        bool skipped = false;
+        if constexpr (SKIP) {  // both CTAs' query tiles left key tile j out: no product
+          volatile uint32_t* own = skip_flags + (g * 2 + (j & 1)) * 4;
+          volatile uint32_t* peer = peer_skip + (g * 2 + (j & 1)) * 4;
+          skipped = (own[0] & own[1] & own[2] & own[3] & 1u) && peer[0] == 1u;
+        }
+        if (!skipped) {
+          const uint64_t vd = dv + static_cast<uint32_t>((j % P2_STAGES) * (STAGE2_BYTES >> 4));
+          const uint64_t pd = dp + static_cast<uint32_t>(g * (TILE_BYTES >> 4));
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_ss_pair_el(tmem + 256 + g * 128, pd + kmaj(kk, BOX_BYTES), vd + kk * (2048 >> 4),
-                         idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_pair_mc_el(bar(BP_PVD + g), kBoth);
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            mma_ss_pair_el(tmem + 256 + g * 128, pd + kmaj(kk, BOX_BYTES),
+                           vd + kk * (2048 >> 4), idesc_pv, (any_pv[g] || kk > 0) ? 1u : 0u);
+          any_pv[g] = true;
+        }
+        mma_commit_pair_mc_el(bar(BP_PVD + g), kBoth);  // also when left out: phases count steps
       };
       bool ok = wait(BP_Q, 0u) && wait_full(0);
       if (ok) {
@@ -342,6 +398,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       }
     };
     float m = -INFINITY, l = 0.f;
+    float m_keep = -INFINITY;  // Skip-Softmax: exact running max of the kept tiles
+    // first row of the CTA's query tile
+    auto qrow0 = [&]() { return p0 + 2 * BQ * tile + BQ * static_cast<int>(rank); };
+    bool p_zero = false;
+    int kept = 0;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait_warp(bar(BP_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
@@ -374,21 +435,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         tc_fence_after();
         return done;
       };
-      if (!softmax_tile_smem(sr, p_row, row & 7u, tO, a.L - j * BKV, j > 0, a.scale_log2, m, l,
-                             wait_pv)) {
+      const int got = softmax_tile_smem<SKIP>(sr, p_row, row & 7u, tO, a.L - j * BKV, j > 0,
+                                              a.scale_log2, m, l, wait_pv, a.skip_log2, m_keep,
+                                              qrow0() + static_cast<int>(row) < a.L,
+                                              skip_flags + (tile * 2 + (j & 1)) * 4,
+                                              static_cast<uint32_t>(j), p_zero, a.err);
+      if (got == TILE_FAILED) {
         ok = false;
         break;
       }
+      if constexpr (SKIP) kept += got == TILE_KEPT ? 1 : 0;
       // P written (generic-proxy stores, made visible to the tensor core's
       // reads) and any O rescale stored: tell the MMA warp
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      tell(BP_P + tile);
+      if constexpr (SKIP) {
+        // with the tile's decision: the odd CTA stores it into the even CTA's
+        // shared memory with st.async, whose 4 bytes complete on the P
+        // barrier (each of the even CTA's warps adds 4 expected bytes)
+        if (lane == 0) {
+          if (leader) {
+            mbar_arrive_expect_tx(bar(BP_P + tile), 4);
+          } else {
+            const uint32_t slot =
+                smem_u32(const_cast<uint32_t*>(peer_skip) + (tile * 2 + (j & 1)) * 4 + quarter);
+            const uint32_t pb = mapa_shared(bar(BP_P + tile), 0);
+            st_async_u32(mapa_shared(slot, 0), got == TILE_SKIPPED ? 1u : 0u, pb);
+            mbar_arrive_remote(pb);
+          }
+        }
+      } else {
+        tell(BP_P + tile);
+      }
     }
+    if (SKIP && ok && a.kept != nullptr && quarter == 0 && lane == 0 && qrow0() < a.L)
+      a.kept[(qrow0() / BQ) * a.H + blockIdx.y] = kept;
     if (ok && mbar_wait_warp(bar(BP_O), 0u, a.err, ERR_WAIT_ATTN_SOFTMAX)) {
       tc_fence_after();
-      const int orow = p0 + 2 * BQ * tile + BQ * static_cast<int>(rank) + static_cast<int>(row);
+      const int orow = qrow0() + static_cast<int>(row);
       store_o_row(tO, l, a.o + static_cast<int64_t>(orow) * a.ld_out + col0, orow < a.L, nullptr);
     }
   }
@@ -403,14 +488,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
 
 }  // namespace
 
-h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
-                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
-                           float skip_eps, int* kept) {
-  if (skip_eps >= 0.f)
-    return launch_attention_skip(q, k, v, ld_in, o, ld_out, L, H, scale, s, skip_eps, kept);
-  static std::atomic<bool> done[64];
-  h3_status st = set_smem_limit(done, attention_pair_kernel, P2_SMEM_BYTES,
-                                "attention: set shared memory size");
+// The pair kernel with or without Skip-Softmax (skip_eps < 0: dense).
+static h3_status launch_pair(const void* q, const void* k, const void* v, int64_t ld_in, void* o,
+                             int64_t ld_out, int L, int H, float scale, cudaStream_t s,
+                             float skip_eps, int* kept) {
+  const bool skip = skip_eps >= 0.f;
+  static std::atomic<bool> done[64], done_skip[64];
+  h3_status st = skip ? set_smem_limit(done_skip, attention_pair_kernel<true>, P2_SMEM_BYTES,
+                                       "attention (skip): set shared memory size")
+                      : set_smem_limit(done, attention_pair_kernel<false>, P2_SMEM_BYTES,
+                                       "attention: set shared memory size");
   if (st != H3_OK) return st;
   AttnArgs a{};
   a.o = static_cast<__nv_bfloat16*>(o);
@@ -419,7 +506,8 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   a.H = H;
   a.num_kv = (L + BKV - 1) / BKV;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.skip_log2 = INFINITY;
+  a.skip_log2 = skip_eps > 0.f ? -log2f(skip_eps) : INFINITY;
+  a.kept = skip_eps > 0.f ? kept : nullptr;  // the counts only when tiles may be skipped
   if ((st = dev_err(&a.err)) != H3_OK) return st;
   CUtensorMap tq, tk, tv;
   const uint64_t width = static_cast<uint64_t>(H) * DH;
@@ -429,8 +517,17 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
   if ((st = make_tmap_bf16_2d(&tv, v, width, L, stride, 64, BKV)) != H3_OK) return st;
   // CTA pairs (a cluster of two along x), 512 query rows per pair
   dim3 grid(2 * ((L + 4 * BQ - 1) / (4 * BQ)), H);
-  attention_pair_kernel<<<grid, Q2_THREADS, P2_SMEM_BYTES, s>>>(tq, tk, tv, a);
-  return cuda_fail(cudaGetLastError(), "attention launch");
+  if (skip)
+    attention_pair_kernel<true><<<grid, Q2_THREADS, P2_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  else
+    attention_pair_kernel<false><<<grid, Q2_THREADS, P2_SMEM_BYTES, s>>>(tq, tk, tv, a);
+  return cuda_fail(cudaGetLastError(), skip ? "attention (skip) launch" : "attention launch");
+}
+
+h3_status launch_attention(const void* q, const void* k, const void* v, int64_t ld_in,
+                           void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
+                           float skip_eps, int* kept) {
+  return launch_pair(q, k, v, ld_in, o, ld_out, L, H, scale, s, skip_eps, kept);
 }
 
 }  // namespace h3

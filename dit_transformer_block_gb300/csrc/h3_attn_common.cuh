@@ -74,5 +74,47 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Skip-Softmax vote of the four warps of a query tile on one KV tile (step
+// vote_tag): each warp posts 2 * vote_tag + (every row of the warp votes to
+// skip) in flags[quarter]. A warp that keeps the tile is done (one keeping
+// warp keeps it); a warp that votes to skip reads the other three posts until
+// all carry this step (bounded: on a timeout or another CTA's error, ok is
+// cleared). Returns whether the tile is kept. The MMA warp reads the same
+// posts (bit 0) after the tile's P barrier. A post is not overwritten before
+// every warp has read it: flags alternate between two slots by step parity,
+// and a warp reaches step j + 2 only after all four have taken S(j + 1).
+__device__ __forceinline__ bool skip_vote(bool row_skip, volatile uint32_t* flags,
+                                          uint32_t vote_tag, const DevErr& err, bool& ok) {
+  const bool warp_skip = __all_sync(0xffffffffu, row_skip);
+  const int quarter = (threadIdx.x >> 5) & 3;
+  if ((threadIdx.x & 31) == 0) flags[quarter] = (vote_tag << 1) | (warp_skip ? 1u : 0u);
+  __syncwarp();
+  if (!warp_skip) return true;
+  uint32_t f0, f1, f2, f3;
+  uint32_t spins = 0;
+  uint64_t t0 = 0;
+  while (true) {
+    f0 = flags[0], f1 = flags[1], f2 = flags[2], f3 = flags[3];
+    if (((f0 | f1 | f2 | f3) >> 1) == vote_tag && ((f0 & f1 & f2 & f3) >> 1) == vote_tag) break;
+    if ((++spins & 63u) == 0) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) t0 = now;
+      if (*(volatile uint32_t*)err.word != 0u || now - t0 > err.timeout_ns) {
+        atomicCAS(err.word, 0u, ERR_WAIT_ATTN_SOFTMAX);
+        break;
+      }
+    }
+  }
+  if (!__all_sync(0xffffffffu, ((f0 & f1 & f2 & f3) >> 1) == vote_tag &&
+                                   ((f0 | f1 | f2 | f3) >> 1) == vote_tag)) {
+    ok = false;
+    return false;
+  }
+  return !(f0 & f1 & f2 & f3 & 1u);
+}
+
+// Outcome of one KV tile in a softmax warp.
+enum : int { TILE_KEPT = 0, TILE_SKIPPED = 1, TILE_FAILED = -1 };
+
 }  // namespace
 }  // namespace h3

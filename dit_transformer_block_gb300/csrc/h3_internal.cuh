@@ -147,12 +147,6 @@ h3_status launch_attention(const void* q, const void* k, const void* v, int64_t 
                            void* o, int64_t ld_out, int L, int H, float scale, cudaStream_t s,
                            float skip_eps = -1.f, int* kept = nullptr);
 
-// Skip-Softmax attention (h3_attention_tiles.cu; launch_attention calls it
-// when skip_eps >= 0).
-h3_status launch_attention_skip(const void* q, const void* k, const void* v, int64_t ld_in,
-                                void* o, int64_t ld_out, int L, int H, float scale,
-                                cudaStream_t s, float skip_eps, int* kept);
-
 // SAGE-style FP8 attention: operands (h3_sage.cu) and the FP8 attention
 // kernel (h3_attention.cu). Codes [L, H*128] bytes with row stride ldc; sq,
 // sk [ceil(L/128), H]; sv, k_mean [H, 128]; scratch of sage_scratch_bytes.

@@ -138,6 +138,18 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Stores a 32-bit value into the peer CTA's shared memory (shared::cluster
+// address) and counts its 4 bytes as completed transactions on the peer's
+// mbarrier (shared::cluster address): whoever sees that barrier's phase
+// complete sees the value.
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t value,
+                                             uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+          cluster_addr),
+      "r"(value), "r"(cluster_bar)
+      : "memory");
+}
 // Every thread of both CTAs of the cluster: all of them arrive, then wait.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
