@@ -75,9 +75,9 @@ enum BarP {
   BP_DRAIN = BP_O + 1,
   BP_NUM = BP_DRAIN + 1
 };
-// barriers, the TMEM address word (padded to 16 bytes), 16 vote flags and
-// 16 decisions of the peer CTA
-static_assert(BP_NUM * 8 + 16 + 16 * 4 + 16 * 4 <= 512, "barrier + flag region");
+// barriers, the TMEM address word (padded to 16 bytes), 16 vote flags, 16
+// decisions of the peer CTA and 4 of its own
+static_assert(BP_NUM * 8 + 16 + 16 * 4 + 16 * 4 + 4 * 4 <= 512, "barrier + flag region");
 
 // One KV tile of the online softmax for the calling thread's query row (TMEM
 // lane), in base 2 with the scale folded in (scale_log2 = softmax scale *
@@ -211,6 +211,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
   // same layout
   volatile uint32_t* skip_flags = tmem_slot + 4;
   volatile uint32_t* peer_skip = skip_flags + 16;
+  // in the even CTA, its own tiles' decisions [tile][parity of j] (each of
+  // the tile's warps writes the same value)
+  volatile uint32_t* own_skip = peer_skip + 16;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const uint32_t rank = cluster_ctarank();
@@ -316,9 +319,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       auto pv = [&](int g, int j) {  // O_g += P_g V_j
         bool skipped = false;
         if constexpr (SKIP) {  // both CTAs' query tiles left key tile j out: no product
-          volatile uint32_t* own = skip_flags + (g * 2 + (j & 1)) * 4;
-          volatile uint32_t* peer = peer_skip + (g * 2 + (j & 1)) * 4;
-          skipped = (own[0] & own[1] & own[2] & own[3] & 1u) && peer[0] == 1u;
+          const uint32_t own = own_skip[g * 2 + (j & 1)];
+          const uint32_t peer = peer_skip[(g * 2 + (j & 1)) * 4];
+          skipped = (own & peer) != 0u;
         }
         if (!skipped) {
           const uint64_t vd = dv + static_cast<uint32_t>((j % P2_STAGES) * (STAGE2_BYTES >> 4));
@@ -456,6 +459,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         // barrier (each of the even CTA's warps adds 4 expected bytes)
         if (lane == 0) {
           if (leader) {
+            own_skip[tile * 2 + (j & 1)] = got == TILE_SKIPPED ? 1u : 0u;
             mbar_arrive_expect_tx(bar(BP_P + tile), 4);
           } else {
             const uint32_t slot =
