@@ -138,7 +138,7 @@ h3_status launch_quantize_fp8_rows(const void* x, int64_t ldx, void* q, int64_t 
 
 // o[:L] = attention(q, k, v); q/k/v rows of stride ld_in elements, o of ld_out.
 // skip_eps < 0: dense attention (the CTA-pair kernel). skip_eps >= 0:
-// Skip-Softmax (the one-CTA kernel with its vote), a key tile is left out for
+// Skip-Softmax (the pair kernel's instance with its vote), a key tile is left out for
 // a query tile when every valid row's tile maximum is below eps times the
 // row's exact running maximum over the kept tiles (eps = 0 never skips); kept
 // (optional, [ceil(L/128), H]) receives the number of key tiles kept per
