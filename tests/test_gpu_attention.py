@@ -177,3 +177,25 @@ def test_skip_softmax_random_data_matches_oracle_rule(h3lib, S, L, eps_log2):
     assert_close_bf16(np64(o[:L]), ref, "skip-softmax, oracle rule")
     dense = O.attention(np64(q), np64(k), np64(v), L, 128 ** -0.5)
     assert np.max(np.abs(ref - dense)) > 0
+
+
+def test_skip_softmax_frame_local_inputs(h3lib):
+    """The frame-local inputs of the Skip-Softmax measurement (frames of
+    1,024 rows) at 4,096 rows: about half of the key tiles are left out, the
+    kept counts equal the oracle's and the output is within bf16 tolerance of
+    the oracle's attention over the kept tiles."""
+    S = L = 4096
+    H = 2
+    loc = I.frame_local_attention_inputs(S, L, H, 128, frame=1024, seed=5, device=dev)
+    eps = 1e-3
+    nq = L // 128
+    kept_gpu = torch.full((nq, H), -1, dtype=torch.int32, device=dev)
+    o = torch.full_like(loc["q"], SENT)
+    h3lib.attention_varlen_skip(loc["q"], loc["k"], loc["v"], o, L, skip_eps=eps, kept=kept_gpu)
+    h3lib.check_device_error()
+    ref, kept = O.attention_skip(np64(loc["q"]), np64(loc["k"]), np64(loc["v"]), L,
+                                 128 ** -0.5, eps)
+    want = kept.sum(axis=2)
+    assert 0.3 < want.sum() / (nq * H * nq) < 0.8
+    assert np.array_equal(kept_gpu.cpu().numpy(), want)
+    assert_close_bf16(np64(o[:L]), ref, "skip-softmax, frame-local")

@@ -142,3 +142,51 @@ def test_sage_skip_matches_oracle_rule(h3lib, S, L, eps_log2):
     assert_close_sage(np64(o[:L]), ref, terms, L, "sage + skip-softmax")
     full = O.attention_sage(ref_ops, L, SCALE)
     assert np.max(np.abs(ref - full)) > 0
+
+
+@pytest.mark.parametrize("S,L", [(128, 1), (256, 250), (1152, 1100)])
+def test_sage_skip_small_and_ragged(h3lib, S, L):
+    """Small and ragged lengths at a real threshold: codes, kept counts and
+    output against the oracle (nothing or little is skipped on these
+    unit-RMS inputs)."""
+    H = 2
+    inp = I.attention_inputs(S, L, H, 128, seed=S + 3, device=dev)
+    ops = h3lib.sage_quantize(inp["q"], inp["k"], inp["v"], L)
+    ref_ops = O.sage_quantize(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), L)
+    assert_ops_equal(ops, ref_ops, L)
+    eps = 2.0 ** -3
+    nq = (L + 127) // 128
+    kept_gpu = torch.full((nq, H), -1, dtype=torch.int32, device=dev)
+    o = torch.full_like(inp["q"], SENT)
+    h3lib.attention_fp8_skip(ops, o, L, skip_eps=eps, kept=kept_gpu)
+    h3lib.check_device_error()
+    assert bool((o[L:] == SENT).all())
+    ref, kept = O.attention_sage_skip(ref_ops, L, SCALE, eps)
+    assert np.array_equal(kept_gpu.cpu().numpy(), kept.sum(axis=2))
+    assert_close_sage(np64(o[:L]), ref, O.sage_skip_error_terms(ref_ops, L, SCALE, eps), L,
+                      "sage + skip, small")
+
+
+def test_sage_skip_frame_local_inputs(h3lib):
+    """The frame-local inputs of the Skip-Softmax measurement (frames of
+    1,024 rows), at 4,096 rows: about half of the key tiles are left out;
+    kept counts equal the oracle's and the output is within the SAGE
+    tolerance over the kept keys."""
+    S = L = 4096
+    H = 2
+    loc = I.frame_local_attention_inputs(S, L, H, 128, frame=1024, seed=5, device=dev)
+    ops = h3lib.sage_quantize(loc["q"], loc["k"], loc["v"], L)
+    ref_ops = O.sage_quantize(np64(loc["q"]), np64(loc["k"]), np64(loc["v"]), L)
+    assert_ops_equal(ops, ref_ops, L)
+    eps = 1e-3
+    nq = L // 128
+    kept_gpu = torch.full((nq, H), -1, dtype=torch.int32, device=dev)
+    o = torch.full_like(loc["q"], SENT)
+    h3lib.attention_fp8_skip(ops, o, L, skip_eps=eps, kept=kept_gpu)
+    h3lib.check_device_error()
+    ref, kept = O.attention_sage_skip(ref_ops, L, SCALE, eps)
+    want = kept.sum(axis=2)
+    assert 0.3 < want.sum() / (nq * H * nq) < 0.8
+    assert np.array_equal(kept_gpu.cpu().numpy(), want)
+    assert_close_sage(np64(o[:L]), ref, O.sage_skip_error_terms(ref_ops, L, SCALE, eps), L,
+                      "sage + skip, frame-local")
