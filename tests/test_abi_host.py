@@ -51,6 +51,30 @@ def test_attention_argument_errors(lib):
     assert h3.last_error() == ""
 
 
+def test_skip_and_fp8_attention_argument_errors(lib):
+    f = "h3_attention_varlen_skip"
+    eps = ctypes.c_float
+    assert st(lib, f, P, P, P, P, 10, 5, 2, 128, ctypes.c_float(0.1), eps(1.0), NULL, NULL) == 1
+    assert "skip_eps" in h3.last_error(), h3.last_error()
+    assert st(lib, f, P, P, P, P, 10, 5, 2, 128, ctypes.c_float(0.1), eps(-0.5), NULL, NULL) == 1
+    assert st(lib, f, P, P, P, P, 10, 11, 2, 128, ctypes.c_float(0.1), eps(0.1), NULL, NULL) == 1
+    assert st(lib, f, P, P, P, P, 10, 0, 2, 128, ctypes.c_float(0.1), eps(0.1), NULL, NULL) == 0
+    g = "h3_attention_fp8_skip"
+    args = (P, P, P, P, P, P, P)  # codes, scales, o
+    assert st(lib, g, *args, 10, 5, 2, 128, ctypes.c_float(0.1), eps(1.0), NULL, NULL) == 1
+    assert "skip_eps" in h3.last_error(), h3.last_error()
+    assert st(lib, g, *args, 10, 11, 2, 128, ctypes.c_float(0.1), eps(0.1), NULL, NULL) == 1
+    assert st(lib, g, NULL, *args[1:], 10, 5, 2, 128, ctypes.c_float(0.1), eps(0.1), NULL,
+              NULL) == 1                                                   # null codes
+    assert st(lib, g, *args, 10, 5, 2, 64, ctypes.c_float(0.1), eps(0.1), NULL, NULL) == 2
+    assert st(lib, g, PM, *args[1:], 10, 5, 2, 128, ctypes.c_float(0.1), eps(0.1), NULL,
+              NULL) == 3                                                   # misaligned codes
+    assert st(lib, g, *args, 10, 5, 2, 128, ctypes.c_float(0.1), eps(0.1),
+              ctypes.c_void_p(4096 + 2), NULL) == 3                        # misaligned counts
+    assert st(lib, g, *args, 10, 0, 2, 128, ctypes.c_float(0.1), eps(0.1), NULL, NULL) == 0
+    assert h3.last_error() == ""
+
+
 def test_elementwise_argument_errors(lib):
     assert st(lib, "h3_swiglu", P, P, 4, 5, 16, NULL) == 1
     assert st(lib, "h3_swiglu", P, P, 4, 4, 12, NULL) == 2
