@@ -84,11 +84,19 @@ def test_projection_outputs_stay_in_bounds(h3lib):
 def test_attention_outputs_stay_in_bounds(h3lib):
     S, L, H = 300, 259, 3
     q, k, v = (rnd(S, H, 128, seed=s).to(torch.bfloat16) for s in (6, 7, 8))
+    nq = (L + 127) // 128
+    o = Guarded((S, H, 128), torch.bfloat16)
+    h3lib.attention_varlen(q, k, v, o.t, L)
+    h3lib.check_device_error()
+    o.check("attention")
+    assert bool((o.t[L:] == -7.25).all())
     for skip in (0.0, 1e-3):
         o = Guarded((S, H, 128), torch.bfloat16)
-        h3lib.attention_varlen_skip(q, k, v, o.t, L, skip_eps=skip)
+        kept = Guarded((nq, H), torch.int32)
+        h3lib.attention_varlen_skip(q, k, v, o.t, L, skip_eps=skip, kept=kept.t)
         h3lib.check_device_error()
         o.check(f"attention skip_eps={skip}")
+        kept.check(f"kept tiles skip_eps={skip}")
         assert bool((o.t[L:] == -7.25).all())
     ops = h3lib.sage_quantize(q, k, v, L)
     o = Guarded((S, H, 128), torch.bfloat16)
@@ -96,6 +104,14 @@ def test_attention_outputs_stay_in_bounds(h3lib):
     h3lib.check_device_error()
     o.check("attention_fp8")
     assert bool((o.t[L:] == -7.25).all())
+    for skip in (0.0, 1e-3):
+        o = Guarded((S, H, 128), torch.bfloat16)
+        kept = Guarded((nq, H), torch.int32)
+        h3lib.attention_fp8_skip(ops, o.t, L, skip_eps=skip, kept=kept.t)
+        h3lib.check_device_error()
+        o.check(f"attention_fp8 skip_eps={skip}")
+        kept.check(f"fp8 kept tiles skip_eps={skip}")
+        assert bool((o.t[L:] == -7.25).all())
 
 
 def test_elementwise_outputs_stay_in_bounds(h3lib):
