@@ -1,6 +1,6 @@
 // Dense bidirectional attention over the valid length of a packed sequence,
-// on tcgen05 tensor cores: CTA pairs (cta_group::2, M = 256 products), S and
-// O in tensor memory, P through shared memory.
+// on tcgen05 tensor cores: CTA pairs (cta_group::2, M = 256 products), S, P
+// and O in tensor memory.
 //
 // vLLM-Omni H3 blog, section 3.1: the attention backend receives the valid
 // sequence length and the structural tail padding is dropped, so no key >= L
@@ -25,29 +25,33 @@ namespace {
 // over 512 query rows as two M = 256 groups: group g covers rows
 // p0 + 256 g .. p0 + 256 g + 255, and CTA r holds rows p0 + 256 g + 128 r ..
 // + 127 of it (its query tile g). Every product is one M = 256 MMA issued by
-// the MMA warp of the even CTA; each CTA supplies its own 128 rows of A (Q, or
-// P from its shared memory) and half of B: keys 64 r .. 64 r + 63 of K_j for
-// S = Q K^T, head channels 64 r .. 64 r + 63 of V_j for O += P V. So each SM
-// reads half of every K/V tile from its own shared memory and receives the
-// other half from its peer.
+// the MMA warp of the even CTA; each CTA supplies its own 128 rows of A (Q
+// from its shared memory, or P from its tensor memory) and half of B: keys
+// 64 r .. 64 r + 63 of K_j for S = Q K^T, head channels 64 r .. 64 r + 63 of
+// V_j for O += P V. So each SM reads half of every K/V tile from its own
+// shared memory and receives the other half from its peer.
 //
-// P goes to shared memory (bf16, laid out like a Q tile), not over S in
-// tensor memory, so S_g is free as soon as the softmax has read it into
-// registers: QK_g(j+1) is issued while the softmax of tile j still runs, and
-// the chain from one S_g to the next is no longer softmax + both products of
-// the group + the hand-offs, which left the tensor pipe idle for part of every
-// KV step. The softmax of a group forms its whole P row in registers and
-// waits for the group's previous P V only before storing it (or before an O
-// rescale), so that product overlaps the exponentials.
+// Tensor memory (512 columns): one S buffer that the two groups use in turn,
+// O_0, O_1, and P_0, P_1 in columns of their own (bf16, two per column), so
+// S is free as soon as a group's softmax has read it into registers: the
+// other group's Q K^T then overwrites it while that softmax runs, and P V
+// reads P from tensor memory. Shared memory carries only the Q tiles and the
+// K/V stages (per KV step and CTA about 160 KB of operand reads and copies,
+// against 2,048 cycles of MMA at 128 bytes per cycle); P stored with
+// tcgen05.st takes a fifth of the time the same stores to shared memory took
+// while the P V products were reading it. The softmax of a group forms its
+// whole P row in registers and waits for the group's previous P V only before
+// storing it (or before an O rescale), so that product overlaps the
+// exponentials.
 // Roles per CTA (320 threads):
 //   warps 0-3 / 4-7: softmax of the CTA's query tile 0 / 1: S from tensor
 //     memory into registers, one lane per warp tells the even CTA's MMA warp
-//     that S is free, then the tile's P is written to shared memory and one
+//     that S is free, then the tile's P is written to tensor memory and one
 //     lane per warp tells the MMA warp that P is ready;
 //   warp 8: TMA producer of the CTA's own halves: its Q tiles once, then, per
 //     KV step, its K half and V half together into one 32 KB stage of a
 //     3-stage ring, on its own barriers;
-//   warp 9: allocates tensor memory (both CTAs together; S0, S1, O0, O1); in
+//   warp 9: allocates tensor memory (both CTAs together; S, O0, O1, P0, P1); in
 //     the even CTA the whole warp runs the issue loop and one elected lane
 //     issues each MMA and commit (both CTAs' barriers); in the odd CTA one
 //     lane relays: each time one of its own stages has landed it arrives on
@@ -58,9 +62,9 @@ namespace {
 constexpr int P2_STAGES = 3;
 constexpr int HALF_BYTES = TILE_BYTES / 2;   // 64 keys x 128 ch, or 128 keys x 64 ch (bf16)
 constexpr int STAGE2_BYTES = 2 * HALF_BYTES; // K half at 0, V half at HALF_BYTES
-// stages, Q tiles, P tiles, barriers and flags (227 KB is the per-CTA limit)
+// stages, Q tiles, barriers and flags (227 KB is the per-CTA limit)
 constexpr size_t P2_SMEM_BYTES =
-    1024 + P2_STAGES * STAGE2_BYTES + 2 * TILE_BYTES + 2 * TILE_BYTES + 512;
+    1024 + P2_STAGES * STAGE2_BYTES + 2 * TILE_BYTES + 512;
 static_assert(P2_SMEM_BYTES <= 227 * 1024, "pair kernel shared memory");
 
 enum BarP {
@@ -75,6 +79,9 @@ enum BarP {
   BP_DRAIN = BP_O + 1,
   BP_NUM = BP_DRAIN + 1
 };
+// tensor-memory columns: S (one buffer, the two groups in turn), O_g, P_g
+// (two bf16 per column)
+constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 384;
 // barriers, the TMEM address word (padded to 16 bytes), 16 vote flags, 16
 // decisions of the peer CTA and 4 of its own
 static_assert(BP_NUM * 8 + 16 + 16 * 4 + 16 * 4 + 4 * 4 <= 512, "barrier + flag region");
@@ -86,9 +93,9 @@ static_assert(BP_NUM * 8 + 16 + 16 * 4 + 16 * 4 + 4 * 4 <= 512, "barrier + flag 
 // earlier tiles; m, l: running max (times scale_log2) and row sum. The
 // running max is raised only when the tile's max exceeds it by more than
 // RESCALE_THRESHOLD (then O and l are rescaled, warp-uniformly). P (bf16) is
-// written to shared memory: p_row = the P tile's shared-memory address + 128
-// * row, r7 = row & 7 (the 128-byte swizzle of a K-major bf16 tile: 16-byte
-// chunk c of a row sits at chunk (c & 7) ^ r7 of box c >> 3). The whole P row
+// written to tensor memory at tP (the row's lane; keys 2c and 2c + 1 in
+// column c, the even key in the low half), where the P V product reads it as
+// its A operand. The whole P row
 // is formed in registers first and stored last: wait_pv() (the previous P V
 // of this tile has finished with P and O) is called only before the stores,
 // or before an O rescale, so that wait overlaps the exponentials.
@@ -100,7 +107,7 @@ static_assert(BP_NUM * 8 + 16 + 16 * 4 + 16 * 4 + 4 * 4 <= 512, "barrier + flag 
 // (once: p_zero records that it already is).
 // Returns TILE_KEPT, TILE_SKIPPED, or TILE_FAILED when a wait failed.
 template <bool SKIP, class WaitPV>
-__device__ __forceinline__ int softmax_tile_smem(uint32_t (&sr)[128], uint32_t p_row, uint32_t r7,
+__device__ __forceinline__ int softmax_tile_tm(uint32_t (&sr)[128], uint32_t tP,
                                                  uint32_t tO, int valid, bool o_live,
                                                  float scale_log2, float& m, float& l,
                                                  WaitPV&& wait_pv, float skip_log2, float& m_keep,
@@ -130,10 +137,12 @@ __device__ __forceinline__ int softmax_tile_smem(uint32_t (&sr)[128], uint32_t p
       // warps, and its phase must not run ahead of the previous one
       if (o_live && !wait_pv()) return TILE_FAILED;
       if (!p_zero) {
+        uint32_t z[16];
 #pragma unroll
-        for (uint32_t chunk = 0; chunk < 16; ++chunk)
-          st_shared_v4(p_row + (chunk >> 3) * BOX_BYTES + (((chunk & 7u) ^ r7) << 4), 0u, 0u, 0u,
-                       0u);
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, z);
+        tmem_st_wait();
         p_zero = true;
       }
       return TILE_SKIPPED;
@@ -184,9 +193,9 @@ __device__ __forceinline__ int softmax_tile_smem(uint32_t (&sr)[128], uint32_t p
   l += (la + lb) + (lc + ld);
   if (!pv_done && !wait_pv()) return TILE_FAILED;
 #pragma unroll
-  for (uint32_t chunk = 0; chunk < 16; ++chunk)  // keys 8 chunk .. 8 chunk + 7
-    st_shared_v4(p_row + (chunk >> 3) * BOX_BYTES + (((chunk & 7u) ^ r7) << 4), pk[4 * chunk],
-                 pk[4 * chunk + 1], pk[4 * chunk + 2], pk[4 * chunk + 3]);
+  for (int c = 0; c < 4; ++c)  // keys 32 c .. 32 c + 31
+    tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
+  tmem_st_wait();
   if constexpr (SKIP) p_zero = false;
   return TILE_KEPT;
 }
@@ -203,8 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sKV = smem;                             // P2_STAGES stages
   uint8_t* sQ = smem + P2_STAGES * STAGE2_BYTES;   // 2 tiles
-  uint8_t* sP = sQ + 2 * TILE_BYTES;               // 2 tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * TILE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BP_NUM);
   // Skip-Softmax votes of this CTA: [tile][parity of j][quarter]; in the even
   // CTA, the odd CTA's decisions (1: its query tile left the key tile out),
@@ -292,7 +300,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(2 * BQ, BKV, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(2 * BQ, DH, true);
       const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dp = sdesc_sw128(smem_u32(sP), 16, 1024);
       const uint64_t dk = sdesc_sw128(smem_u32(sKV), 16, 1024);
       const uint64_t dv = sdesc_sw128(smem_u32(sKV) + HALF_BYTES, HALF_BYTES, 1024);
       constexpr uint16_t kBoth = 3;
@@ -306,12 +313,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       auto kmaj = [](int kk, int box_bytes) {
         return static_cast<uint32_t>(((kk >> 2) * box_bytes + (kk & 3) * 32) >> 4);
       };
-      auto qk = [&](int g, int j) {  // S_g = Q_g K_j^T over both CTAs' rows
+      auto qk = [&](int g, int j) {  // S = Q_g K_j^T over both CTAs' rows
         const uint64_t kd = dk + static_cast<uint32_t>((j % P2_STAGES) * (STAGE2_BYTES >> 4));
         const uint64_t qd = dq + static_cast<uint32_t>(g * (TILE_BYTES >> 4));
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk)
-          mma_ss_pair_el(tmem + g * 128, qd + kmaj(kk, BOX_BYTES), kd + kmaj(kk, HALF_BYTES / 2),
+          mma_ss_pair_el(tmem + TM_S, qd + kmaj(kk, BOX_BYTES), kd + kmaj(kk, HALF_BYTES / 2),
                          idesc_qk, kk > 0 ? 1u : 0u);
         mma_commit_pair_mc_el(bar(BP_S + g), kBoth);
       };
@@ -325,10 +332,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         }
         if (!skipped) {
           const uint64_t vd = dv + static_cast<uint32_t>((j % P2_STAGES) * (STAGE2_BYTES >> 4));
-          const uint64_t pd = dp + static_cast<uint32_t>(g * (TILE_BYTES >> 4));
 #pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk)
-            mma_ss_pair_el(tmem + 256 + g * 128, pd + kmaj(kk, BOX_BYTES),
+          for (int kk = 0; kk < BKV / 16; ++kk)  // P_g from tensor memory, 16 keys = 8 columns
+            mma_ts_pair_el(tmem + TM_O + g * 128, tmem + TM_P + g * 64 + kk * 8,
                            vd + kk * (2048 >> 4), idesc_pv, (any_pv[g] || kk > 0) ? 1u : 0u);
           any_pv[g] = true;
         }
@@ -338,15 +344,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
       if (ok) {
         tc_fence_after();
         qk(0, 0);
-        qk(1, 0);
+        ok = wait(BP_SFREE, 0u);
+        if (ok) {
+          tc_fence_after();
+          qk(1, 0);
+        }
       }
-      // Per KV step: QK0(j+1) as soon as the softmax has read S0(j), then
-      // PV0(j), QK1(j+1), PV1(j); a stage is free once PV1 of it is done.
+      // Per KV step: QK0(j+1) once group 1 has read S1(j), PV0(j), QK1(j+1)
+      // once group 0 has read S0(j+1), PV1(j); a stage is free once PV1 of it
+      // is done. S is read while the other group's P V runs.
       for (int j = 0; ok && j < n; ++j) {
         const uint32_t par = static_cast<uint32_t>(j) & 1u;
         const bool more = j + 1 < n;
         if (more) {
-          if (!wait_full(j + 1) || !wait(BP_SFREE, par)) break;
+          if (!wait_full(j + 1) || !wait(BP_SFREE + 1, par)) break;
           tc_fence_after();
           qk(0, j + 1);
         }
@@ -354,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         tc_fence_after();
         pv(0, j);
         if (more) {
-          if (!wait(BP_SFREE + 1, par)) break;
+          if (!wait(BP_SFREE, par ^ 1u)) break;
           tc_fence_after();
           qk(1, j + 1);
         }
@@ -387,10 +398,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
     const int tile = warp >> 2;
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + tile * 128;
-    const uint32_t tO = tmem + lane_base + 256 + tile * 128;
+    const uint32_t tS = tmem + lane_base + TM_S;
+    const uint32_t tO = tmem + lane_base + TM_O + tile * 128;
+    const uint32_t tP = tmem + lane_base + TM_P + tile * 64;
     const uint32_t row = static_cast<uint32_t>(quarter * 32 + lane);
-    const uint32_t p_row = smem_u32(sP + tile * TILE_BYTES) + row * 128;
     // one lane per warp tells the even CTA's MMA warp
     auto tell = [&](int b) {
       if (lane == 0) {
@@ -407,7 +418,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
     bool p_zero = false;
     int kept = 0;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; ok && j < n; ++j) {
       if (!mbar_wait_warp(bar(BP_S + tile), static_cast<uint32_t>(j) & 1u, a.err,
                           ERR_WAIT_ATTN_SOFTMAX)) {
         ok = false;
@@ -438,7 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         tc_fence_after();
         return done;
       };
-      const int got = softmax_tile_smem<SKIP>(sr, p_row, row & 7u, tO, a.L - j * BKV, j > 0,
+      const int got = softmax_tile_tm<SKIP>(sr, tP, tO, a.L - j * BKV, j > 0,
                                               a.scale_log2, m, l, wait_pv, a.skip_log2, m_keep,
                                               qrow0() + static_cast<int>(row) < a.L,
                                               skip_flags + (tile * 2 + (j & 1)) * 4,
@@ -448,9 +459,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q2_THREADS, 1)
         break;
       }
       if constexpr (SKIP) kept += got == TILE_KEPT ? 1 : 0;
-      // P written (generic-proxy stores, made visible to the tensor core's
-      // reads) and any O rescale stored: tell the MMA warp
-      fence_proxy_async_smem();
+      // P and any O rescale stored to tensor memory: tell the MMA warp
       tc_fence_before();
       __syncwarp();
       if constexpr (SKIP) {

@@ -296,6 +296,17 @@ __device__ __forceinline__ void mma_ss_pair_el(uint32_t d_tmem, uint64_t a_desc,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// TS form of the pair MMA: A read from tensor memory (each CTA its own 128
+// lanes at a_tmem, two bf16 per 32-bit column, element 2c in the low half of
+// column c), B from shared memory as in mma_ss_pair_el.
+__device__ __forceinline__ void mma_ts_pair_el(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_pair_mc_el(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
