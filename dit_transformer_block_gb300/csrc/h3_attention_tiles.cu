@@ -1,8 +1,9 @@
 // FP8 (SAGE) attention on one CTA per pair of 128-row query tiles (blog
 // section 4.3, Fig. 6: Q, K, P and V in FP8 for the QK and PV products;
-// Skip-Softmax as an option): S freed as soon as the softmax has read it, P
-// as E4M3 codes through shared memory. The BF16 attention (dense and
-// Skip-Softmax) is in h3_attention.cu.
+// Skip-Softmax as an option): one S buffer that the two query tiles use in
+// turn, freed as soon as a softmax has read it, and P as E4M3 codes in tensor
+// memory beside O. The BF16 attention (dense and Skip-Softmax) is in
+// h3_attention.cu.
 #include <algorithm>
 
 #include "h3_attn_common.cuh"
@@ -13,23 +14,25 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // FP8 (SAGE) attention, one CTA per pair of 128-row query tiles of one head,
-// with the same hand-off as the pair kernel: the softmax reads S_i into
-// registers and frees it at once, so QK_i(j+1) overlaps the softmax of tile
-// j; P_i (E4M3 codes) is formed in registers and stored to shared memory after
-// PV_i(j-1) has finished with it; every product is an SS kind::f8f6f4 MMA.
+// with the same hand-off and tensor-memory layout as the pair kernel: a
+// softmax reads S into registers and frees it at once, so the other tile's
+// Q K^T overlaps that softmax; P_i (E4M3 codes) is formed in registers and
+// stored to tensor memory after PV_i(j-1) has finished with it; Q K^T is an
+// SS kind::f8f6f4 MMA, P V the TS form (A = P_i from tensor memory).
 //   warps 0-3 / 4-7: softmax of query tile 0 / 1 (thread = query row = TMEM
 //     lane of S_i and O_i);
 //   warp 8: TMA producer: Q0, Q1 once, then K_j and V_j (128 rows of 128
 //     codes, 16 KB each) together into one 32 KB stage of a 4-stage ring;
-//   warp 9: allocates TMEM (S0, S1, O0, O1); the whole warp runs the issue
-//     loop, one elected lane issues: per KV step QK0(j+1), PV0(j), QK1(j+1),
-//     PV1(j), then a commit frees stage j.
+//   warp 9: allocates TMEM (S, O0, O1, P0, P1); the whole warp runs the
+//     issue loop, one elected lane issues: per KV step QK0(j+1) once tile 1
+//     has read S1(j), PV0(j), QK1(j+1) once tile 0 has read S0(j+1), PV1(j),
+//     then a commit frees stage j.
 // Scores of (query tile t, key tile j, head h) are scaled by sq[t H + h] *
 // sk[j H + h] (with the softmax scale); output channel d by sv[h 128 + d].
 constexpr int F8_TILE = BQ * DH;          // 16 KB: one tile of E4M3 codes
 constexpr int F8_STAGES = 4;
 constexpr int F8_STAGE_BYTES = 2 * F8_TILE;  // K_j at 0, V_j at F8_TILE
-constexpr size_t F8_SMEM_BYTES = 1024 + F8_STAGES * F8_STAGE_BYTES + 2 * F8_TILE + 2 * F8_TILE + 256;
+constexpr size_t F8_SMEM_BYTES = 1024 + F8_STAGES * F8_STAGE_BYTES + 2 * F8_TILE + 256;
 static_assert(F8_SMEM_BYTES <= 227 * 1024, "fp8 attention shared memory");
 
 enum BarF8 {
@@ -44,6 +47,9 @@ enum BarF8 {
   BF_DRAIN = BF_O + 1,
   BF_NUM = BF_DRAIN + 1
 };
+// tensor-memory columns: S (the two tiles in turn), O_i, P_i (four codes per
+// column)
+constexpr uint32_t TF_S = 0, TF_O = 128, TF_P = 384;
 // barriers, the TMEM address word (padded to 16 bytes) and 16 vote flags
 static_assert(BF_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
 
@@ -56,9 +62,9 @@ static_assert(BF_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
 // it by more than 1; then O and the row sum are rescaled), so every P is an
 // exact power-of-two multiple of the P against any other integer reference;
 // P is carried as 224 P (log2 224 added to the exponent), whose E4M3 codes
-// are stored to shared memory at p_row = the P tile's address + 128 * row,
-// 16-byte chunk c of the row at chunk c ^ r7 (r7 = row & 7: the 128-byte
-// swizzle of a K-major tile). The row sum l carries the same factor 224,
+// are stored to tensor memory at tP (the row's lane; keys 4c .. 4c + 3 in
+// column c, the lowest key in the low byte). The row sum l carries the same
+// factor 224,
 // which cancels in O / l. wait_pv() (the previous P V of this tile has
 // finished with P and O) is called before the stores, or before an O
 // rescale.
@@ -69,8 +75,8 @@ static_assert(BF_NUM * 8 + 16 + 16 * 4 <= 256, "barrier + flag region");
 // tile's P V.
 // Returns TILE_KEPT, TILE_SKIPPED, or TILE_FAILED when a wait failed.
 template <bool SKIP, class WaitPV>
-__device__ __forceinline__ int softmax_tile_f8_smem(uint32_t (&sr)[128], uint32_t p_row,
-                                                    uint32_t r7, uint32_t tO, int valid,
+__device__ __forceinline__ int softmax_tile_f8_tm(uint32_t (&sr)[128], uint32_t tP,
+                                                    uint32_t tO, int valid,
                                                     bool o_live, float scale_log2, float& m,
                                                     float& l, WaitPV&& wait_pv, float skip_log2,
                                                     float& m_keep, bool row_valid,
@@ -142,9 +148,9 @@ __device__ __forceinline__ int softmax_tile_f8_smem(uint32_t (&sr)[128], uint32_
   }
   l += (la + lb) + (lc + ld);
   if (!pv_done && !wait_pv()) return TILE_FAILED;
-#pragma unroll
-  for (uint32_t c = 0; c < 8; ++c)  // keys 16 c .. 16 c + 15
-    st_shared_v4(p_row + ((c ^ r7) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+  tmem_st16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));  // keys 0 .. 63
+  tmem_st16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+  tmem_st_wait();
   return TILE_KEPT;
 }
 
@@ -160,8 +166,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sKV = smem;                                // F8_STAGES stages
   uint8_t* sQ = smem + F8_STAGES * F8_STAGE_BYTES;    // 2 tiles
-  uint8_t* sP = sQ + 2 * F8_TILE;                     // 2 tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * F8_TILE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + 2 * F8_TILE);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BF_NUM);
   // Skip-Softmax votes: [tile][parity of j][quarter]
   volatile uint32_t* skip_flags = tmem_slot + 4;
@@ -221,7 +226,6 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
     constexpr uint32_t idesc_qk = idesc_e4m3_f32(BQ, BKV);
     constexpr uint32_t idesc_pv = idesc_e4m3_f32(BQ, DH) | (1u << 16);  // V MN-major
     const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
-    const uint64_t dp = sdesc_sw128(smem_u32(sP), 16, 1024);
     const uint64_t dk = sdesc_sw128(smem_u32(sKV), 16, 1024);
     const uint64_t dv = sdesc_sw128(smem_u32(sKV) + F8_TILE, F8_TILE, 1024);
     auto wait = [&](int b, uint32_t parity) {
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       const uint64_t kd = dk + stage(j);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_ss_f8_el(tmem + i * 128, qd + kk * 2, kd + kk * 2, idesc_qk, kk > 0 ? 1u : 0u);
+        mma_ss_f8_el(tmem + TF_S, qd + kk * 2, kd + kk * 2, idesc_qk, kk > 0 ? 1u : 0u);
       mma_commit_el(bar(BF_S + i));
     };
     int kept[2] = {0, 0};  // Skip-Softmax: key tiles kept per query tile
@@ -246,12 +250,11 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       const bool skipped = SKIP && (f[0] & f[1] & f[2] & f[3] & 1u);
       if (!skipped) {  // (the first tile is never skipped)
         ++kept[i];
-        const uint64_t pd = dp + static_cast<uint32_t>(i * (F8_TILE >> 4));
         const uint64_t vd = dv + stage(j);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss_f8_el(tmem + 256 + i * 128, pd + kk * 2, vd + kk * (4096 >> 4), idesc_pv,
-                       (any_pv[i] || kk > 0) ? 1u : 0u);
+          mma_ts_f8_el(tmem + TF_O + i * 128, tmem + TF_P + i * 32 + kk * 8,
+                       vd + kk * (4096 >> 4), idesc_pv, (any_pv[i] || kk > 0) ? 1u : 0u);
         any_pv[i] = true;
       }
       mma_commit_el(bar(BF_PVD + i));  // also for a skipped tile: the phase counts steps
@@ -260,13 +263,17 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
     if (ok) {
       tc_fence_after();
       qk(0, 0);
-      qk(1, 0);
+      ok = wait(BF_SFREE, 0u);
+      if (ok) {
+        tc_fence_after();
+        qk(1, 0);
+      }
     }
     for (int j = 0; ok && j < n; ++j) {
       const uint32_t par = static_cast<uint32_t>(j) & 1u;
       const bool more = j + 1 < n;
       if (more) {
-        if (!wait_full(j + 1) || !wait(BF_SFREE, par)) break;
+        if (!wait_full(j + 1) || !wait(BF_SFREE + 1, par)) break;
         tc_fence_after();
         qk(0, j + 1);
       }
@@ -274,7 +281,7 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
       tc_fence_after();
       pv(0, j);
       if (more) {
-        if (!wait(BF_SFREE + 1, par)) break;
+        if (!wait(BF_SFREE, par ^ 1u)) break;
         tc_fence_after();
         qk(1, j + 1);
       }
@@ -299,10 +306,10 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
     const int tile = warp >> 2;
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + tile * 128;
-    const uint32_t tO = tmem + lane_base + 256 + tile * 128;
+    const uint32_t tS = tmem + lane_base + TF_S;
+    const uint32_t tO = tmem + lane_base + TF_O + tile * 128;
+    const uint32_t tP = tmem + lane_base + TF_P + tile * 32;
     const uint32_t row = static_cast<uint32_t>(quarter * 32 + lane);
-    const uint32_t p_row = smem_u32(sP + tile * F8_TILE) + row * 128;
     const int qt = blockIdx.x * 2 + tile;  // 128-row query tile index
     const float sq_tile = (qt * BQ < a.L) ? __ldg(a.sq + qt * a.H + blockIdx.y) : 0.f;
     float m = -INFINITY, l = 0.f;
@@ -342,14 +349,14 @@ __global__ void __launch_bounds__(Q2_THREADS, 1)
         tc_fence_after();
         return done;
       };
-      if (softmax_tile_f8_smem<SKIP>(sr, p_row, row & 7u, tO, a.L - j * BKV, j > 0, mul, m, l,
+      if (softmax_tile_f8_tm<SKIP>(sr, tP, tO, a.L - j * BKV, j > 0, mul, m, l,
                                      wait_pv, a.skip_log2, m_keep, row_valid,
                                      skip_flags + (tile * 2 + (j & 1)) * 4,
                                      static_cast<uint32_t>(j), a.err) == TILE_FAILED) {
         ok = false;
         break;
       }
-      fence_proxy_async_smem();  // the codes, for the tensor core's reads
+      // the codes (and any O rescale) stored to tensor memory
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BF_P + tile));
