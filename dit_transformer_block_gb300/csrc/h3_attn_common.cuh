@@ -67,13 +67,6 @@ __device__ __forceinline__ void store_o_row(uint32_t tO, float l, __nv_bfloat16*
   }
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
 // Skip-Softmax vote of the four warps of a query tile on one KV tile (step
 // vote_tag): each warp posts 2 * vote_tag + (every row of the warp votes to
 // skip) in flags[quarter]. A warp that keeps the tile is done (one keeping
