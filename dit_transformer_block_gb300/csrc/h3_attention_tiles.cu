@@ -20,7 +20,7 @@ namespace {
 // stored to tensor memory after PV_i(j-1) has finished with it; Q K^T is an
 // SS kind::f8f6f4 MMA, P V the TS form (A = P_i from tensor memory).
 //   warps 0-3 / 4-7: softmax of query tile 0 / 1 (thread = query row = TMEM
-//     lane of S_i and O_i);
+//     lane of S, O_i and P_i);
 //   warp 8: TMA producer: Q0, Q1 once, then K_j and V_j (128 rows of 128
 //     codes, 16 KB each) together into one 32 KB stage of a 4-stage ring;
 //   warp 9: allocates TMEM (S, O0, O1, P0, P1); the whole warp runs the
