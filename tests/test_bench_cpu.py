@@ -1,5 +1,7 @@
 """bench.py's host-side pieces on the CPU: the work model, the oracle samples
-of the CPU baseline (on a small shape), and the job arithmetic."""
+of the CPU baseline (on a small shape), the job arithmetic, and the gate that
+reports a committed ncu traffic figure only while its kernel code is
+unchanged."""
 import os
 import sys
 
@@ -38,3 +40,31 @@ def test_oracle_samples_run_and_extrapolate():
     assert qk_ms > 0 and np.isclose(qk_all, qk_ms * SMALL.L / 16)
     at_ms, at_all = bench.oracle_attention_rows(SMALL, n=16)
     assert at_ms > 0 and np.isclose(at_all, at_ms * SMALL.L / 16)
+
+
+def test_code_hash_ignores_comments_and_blank_lines_only():
+    src = "int f(int x) {\n  return x + 1;  // one more\n}\n"
+    same = "// a header comment\nint f(int x) {\n\n  return x + 1;   \n}\n"
+    other = "int f(int x) {\n  return x + 2;  // one more\n}\n"
+    assert bench.code_sha256(src) == bench.code_sha256(same)
+    assert bench.code_sha256(src) != bench.code_sha256(other)
+
+
+def test_profile_traffic_only_while_the_kernel_code_is_unchanged(tmp_path, monkeypatch):
+    csrc = tmp_path / "dit_transformer_block_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "k.cu").write_text("__global__ void k() {}  // kernel\n")
+    (csrc / "k.cuh").write_text("constexpr int N = 4;\n")
+    files = ("k.cu", "k.cuh")
+    prefix = bench.code_sha256("__global__ void k() {}\nconstexpr int N = 4;\n")[:16]
+    (tmp_path / "profiles" / "p.md").write_text(
+        f"text\n\ndram_bytes_per_launch: 123456\nsource_sha256: {prefix}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_traffic(files, "p.md") == 123456.0
+    # a comment-only edit keeps the figure; a code edit makes it stale
+    (csrc / "k.cu").write_text("// reworded\n__global__ void k() {}  // the kernel\n")
+    assert bench.profile_traffic(files, "p.md") == 123456.0
+    (csrc / "k.cuh").write_text("constexpr int N = 8;\n")
+    assert bench.profile_traffic(files, "p.md") is None
+    assert bench.profile_traffic(files, "missing.md") is None
